@@ -1,0 +1,153 @@
+/*
+ * moe_mxfp4.h -- C ABI of the fused MXFP4 Mixture-of-Experts forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (sources are the web pages this library restates):
+ *   kernelbot-amd-moe-mxfp4-754773, flower_moe.py, custom_kernel: sort routes
+ *     by expert -> MXFP4-quantise the hidden states -> stage-1 grouped GEMM with
+ *     SiLU(gate)*up -> MXFP4-requantise the bf16 intermediate -> stage-2 grouped
+ *     GEMM whose rows are scaled by the top-k weights and summed per token.
+ *   kernelbot-amd-moe-mxfp4-723815, solution.py, fused_moe_mxfp4 / _dequant /
+ *     kernel_stage1 / kernel_stage2: tensor layouts, e2m1 and e8m0 decoding,
+ *     nibble order, gate rows before up rows, weight applied after the down GEMM.
+ *
+ * Formats: an e2m1 element is 4 bits (sign, 2 exponent bits with bias 1, 1
+ * mantissa bit); two elements per byte, element 2j in the low nibble of byte j.
+ * An e8m0 scale byte s means 2^(s-127); one scale per 32 consecutive elements
+ * along the contraction (K) dimension of a row.
+ *
+ * Ownership and threading: every pointer argument is device memory owned by
+ * the caller; inputs are only read; the library never allocates on the call
+ * path.  The scratch it needs is a caller-owned device buffer registered with
+ * moe_mxfp4_set_workspace (one per device; calls that share it must be ordered
+ * on the GPU, e.g. issued to one stream).  All work is enqueued on `stream`; the
+ * call returns after enqueueing.
+ *
+ * Error behaviour: argument and shape errors are detected on the host before
+ * any work is enqueued and returned as a status code (nothing is launched).
+ * Launch failures return MOE_ERR_CUDA.  Errors found on the device (a bounded
+ * wait that ran out) are recorded in the workspace and reported by
+ * moe_mxfp4_last_device_status.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* null pointer, negative size, topk/E out of range   */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* d_model / d_inter not a supported multiple        */
+    MOE_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned                    */
+    MOE_ERR_WORKSPACE = 4,         /* no workspace registered, or too small               */
+    MOE_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed                   */
+    MOE_ERR_DEVICE_TIMEOUT = 6     /* a bounded device-side wait ran out (see status)     */
+} moe_status_t;
+
+/*
+ * Supported shapes: T >= 0; 1 <= topk <= 16; 1 <= E <= 1024;
+ * d_model and d_inter each 128, 256 or a multiple of 512;
+ * d_model a multiple of 128 and d_inter a multiple of 64 (both hold for the above).
+ * Every pointer 16-byte aligned.
+ */
+
+/* Bytes of workspace one forward call of this shape needs (0 when the shape is
+ * not supported).  Depends only on the shape. */
+size_t moe_mxfp4_workspace_size(int T, int d_model, int d_inter, int E, int topk);
+
+/*
+ * Register the caller-owned device workspace for the current CUDA device.
+ * dev_ptr must be 256-byte aligned; bytes its size.  Passing NULL unregisters.
+ * The library keeps the pointer, never frees it.  Not thread-safe with
+ * concurrent forward calls on the same device.
+ */
+moe_status_t moe_mxfp4_set_workspace(void* dev_ptr, size_t bytes);
+
+/*
+ * Fused MXFP4 MoE forward.
+ *   hidden        bf16 [T, d_model], row-major
+ *   w13           u8   [E, 2*d_inter, d_model/2]: packed e2m1, rows [0, d_inter) gate,
+ *                      rows [d_inter, 2*d_inter) up (solution.py: W_gate / W_up split)
+ *   w13_scale     u8   [E, 2*d_inter, d_model/32]: e8m0
+ *   w2            u8   [E, d_model, d_inter/2]: packed e2m1
+ *   w2_scale      u8   [E, d_model, d_inter/32]: e8m0
+ *   topk_ids      i32  [T, topk]: expert ids; ids outside [0, E) contribute nothing
+ *   topk_weights  f32  [T, topk]: multiplies the stage-2 output of that route
+ *   out           bf16 [T, d_model]: fully overwritten:
+ *                 out[t] = bf16( sum_k w[t,k] * W2[e] . Q( bf16( silu(W13g[e] . Q(x_t))
+ *                                                        * (W13u[e] . Q(x_t)) ) ) )
+ *                 with Q the MX quantiser (shared exponent floor(log2 amax) - 2,
+ *                 round to nearest even, saturate at 6), fp32 accumulation, and the
+ *                 sum over k in ascending order (deterministic).
+ * Asynchronous on `stream`.  T == 0 returns MOE_OK and enqueues nothing.
+ */
+moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* w13_scale,
+                               const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                               const float* topk_weights, void* out, int T, int d_model,
+                               int d_inter, int E, int topk, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_mxfp4_status_string(moe_status_t status);
+
+/*
+ * Synchronise `stream`, then read the device status word of the current
+ * device's workspace.  Returns MOE_ERR_DEVICE_TIMEOUT when a kernel of the last
+ * forward call gave up on a bounded wait, MOE_OK otherwise.  Meant for tests and
+ * checked runs (it synchronises).
+ */
+moe_status_t moe_mxfp4_last_device_status(cudaStream_t stream);
+
+/* ------------------------------------------------------------------ inspection */
+
+/* Workspace regions, for tests and tools that inspect intermediate results. */
+typedef enum {
+    MOE_WS_STATUS = 0,      /* u32 [16]: [0] error bits, [1] where a wait gave up            */
+    MOE_WS_COUNTERS = 1,    /* u32 [counters]: split-K arrival counters (zeroed per call)    */
+    MOE_WS_SORTED_IDS = 2,  /* i32 [cap]: route id t*topk+k per sorted slot, T*topk = padding */
+    MOE_WS_SORTED_W = 3,    /* f32 [cap]: topk weight of the slot's route, 0 for padding      */
+    MOE_WS_BLOCK_EXPERT = 4,/* i32 [cap/block_m]: expert of each block, -1 unused             */
+    MOE_WS_SEG_START = 5,   /* i32 [E+1]: first slot of each expert; [E] = padded length      */
+    MOE_WS_ROUTE_POS = 6,   /* i32 [T*topk]: slot of each route, -1 for ids outside [0, E)    */
+    MOE_WS_NUM_VALID = 7,   /* i32 [4]: padded length, valid routes, tiles, 0                 */
+    MOE_WS_TILES = 8,       /* i32 [cap/block_m][4]: {expert, first slot, rows, 0}            */
+    MOE_WS_A1Q = 9,         /* u8 [cap][d_model/2]: quantised hidden row of each slot's token */
+    MOE_WS_A1S = 10,        /* u8 [cap][a1s_stride]: its e8m0 scales                          */
+    MOE_WS_A2Q = 11,        /* u8 [cap][d_inter/2]: quantised SwiGLU output of each slot      */
+    MOE_WS_A2S = 12,        /* u8 [cap][a2s_stride]: its e8m0 scales                          */
+    MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id    */
+    MOE_WS_PARTIAL = 14,    /* f32: split-K partial accumulators of stage 1                   */
+    MOE_WS_NUM_REGIONS = 15
+} moe_ws_region_t;
+
+typedef struct {
+    int block_m;        /* slots per padded block (segment granularity)                   */
+    int tile_rows;      /* maximum routes per GEMM tile (multiple of block_m)             */
+    int cap;            /* slots in the sorted arrays                                    */
+    int a1s_stride;     /* bytes per row of MOE_WS_A1S                                   */
+    int a2s_stride;     /* bytes per row of MOE_WS_A2S                                   */
+    int stage1_splits;  /* K splits of the stage-1 GEMM                                  */
+    int max_tiles;      /* capacity of MOE_WS_TILES                                      */
+    int reserved;
+    size_t offset[MOE_WS_NUM_REGIONS]; /* byte offset of each region in the workspace     */
+    size_t bytes[MOE_WS_NUM_REGIONS];  /* byte size of each region                        */
+    size_t workspace_bytes;            /* total (== moe_mxfp4_workspace_size)              */
+} moe_mxfp4_plan_t;
+
+/* Fill *plan with the layout the forward call uses for this shape.  Host-only;
+ * touches no device.  Returns a shape/argument status like the forward call. */
+moe_status_t moe_mxfp4_get_plan(int T, int d_model, int d_inter, int E, int topk,
+                                moe_mxfp4_plan_t* plan);
+
+/* Version string of the library build. */
+const char* moe_mxfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_MXFP4_H */

@@ -1,0 +1,202 @@
+"""Fused MXFP4 Mixture-of-Experts forward for NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/moe_mxfp4.h`` (ctypes, argument
+marshalling only).  Every step of the forward runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback: if the library is missing or a
+call fails, an exception is raised.
+
+    import torch, mixture_experts_mxfp4_gb300 as moe
+    m = moe.MoeMXFP4(T, d_model, d_inter, E, topk)        # owns its workspace
+    out = m.forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_mxfp4.so")
+
+STATUS = {
+    0: "MOE_OK",
+    1: "MOE_ERR_INVALID_ARG",
+    2: "MOE_ERR_UNSUPPORTED_SHAPE",
+    3: "MOE_ERR_MISALIGNED",
+    4: "MOE_ERR_WORKSPACE",
+    5: "MOE_ERR_CUDA",
+    6: "MOE_ERR_DEVICE_TIMEOUT",
+}
+MOE_OK = 0
+
+REGIONS = ["status", "counters", "sorted_ids", "sorted_w", "block_expert", "seg_start",
+           "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "partial"]
+
+# Exported C symbols (kept in step with include/moe_mxfp4.h).
+EXPORTS = [
+    "moe_mxfp4_workspace_size",
+    "moe_mxfp4_set_workspace",
+    "moe_mxfp4_forward",
+    "moe_mxfp4_status_string",
+    "moe_mxfp4_last_device_status",
+    "moe_mxfp4_get_plan",
+    "moe_mxfp4_version",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [
+        ("block_m", ctypes.c_int),
+        ("tile_rows", ctypes.c_int),
+        ("cap", ctypes.c_int),
+        ("a1s_stride", ctypes.c_int),
+        ("a2s_stride", ctypes.c_int),
+        ("stage1_splits", ctypes.c_int),
+        ("max_tiles", ctypes.c_int),
+        ("reserved", ctypes.c_int),
+        ("offset", ctypes.c_size_t * len(REGIONS)),
+        ("bytes", ctypes.c_size_t * len(REGIONS)),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+    def region(self, name: str):
+        i = REGIONS.index(name)
+        return int(self.offset[i]), int(self.bytes[i])
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libmoe_mxfp4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} not found: build it with mixture_experts_mxfp4_gb300/build.py")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i = ctypes.c_int
+    lib.moe_mxfp4_workspace_size.restype = ctypes.c_size_t
+    lib.moe_mxfp4_workspace_size.argtypes = [i, i, i, i, i]
+    lib.moe_mxfp4_set_workspace.restype = i
+    lib.moe_mxfp4_set_workspace.argtypes = [P, ctypes.c_size_t]
+    lib.moe_mxfp4_forward.restype = i
+    lib.moe_mxfp4_forward.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P]
+    lib.moe_mxfp4_status_string.restype = ctypes.c_char_p
+    lib.moe_mxfp4_status_string.argtypes = [i]
+    lib.moe_mxfp4_last_device_status.restype = i
+    lib.moe_mxfp4_last_device_status.argtypes = [P]
+    lib.moe_mxfp4_get_plan.restype = i
+    lib.moe_mxfp4_get_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+    lib.moe_mxfp4_version.restype = ctypes.c_char_p
+    lib.moe_mxfp4_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(code: int, where: str):
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+def workspace_size(T, d_model, d_inter, E, topk) -> int:
+    return int(load_library().moe_mxfp4_workspace_size(T, d_model, d_inter, E, topk))
+
+
+def get_plan(T, d_model, d_inter, E, topk) -> Plan:
+    pl = Plan()
+    _check(load_library().moe_mxfp4_get_plan(T, d_model, d_inter, E, topk, ctypes.byref(pl)),
+           "moe_mxfp4_get_plan")
+    return pl
+
+
+def set_workspace(ptr: int, nbytes: int):
+    _check(load_library().moe_mxfp4_set_workspace(ctypes.c_void_p(ptr), nbytes),
+           "moe_mxfp4_set_workspace")
+
+
+def forward_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out,
+                T, d_model, d_inter, E, topk, stream: int = 0) -> int:
+    """Raw-pointer call of moe_mxfp4_forward; returns the status code."""
+    return int(load_library().moe_mxfp4_forward(
+        ctypes.c_void_p(hidden), ctypes.c_void_p(w13), ctypes.c_void_p(w13_scale),
+        ctypes.c_void_p(w2), ctypes.c_void_p(w2_scale), ctypes.c_void_p(topk_ids),
+        ctypes.c_void_p(topk_weights), ctypes.c_void_p(out), T, d_model, d_inter, E, topk,
+        ctypes.c_void_p(stream)))
+
+
+def last_device_status(stream: int = 0) -> int:
+    return int(load_library().moe_mxfp4_last_device_status(ctypes.c_void_p(stream)))
+
+
+def version() -> str:
+    return load_library().moe_mxfp4_version().decode()
+
+
+class MoeMXFP4:
+    """One MoE layer shape with its own device workspace (a torch uint8 tensor).
+
+    The workspace is registered for the current device on every call, so several
+    instances can coexist as long as their calls are ordered on the GPU.
+    """
+
+    def __init__(self, T, d_model, d_inter, E, topk, device="cuda"):
+        import torch
+
+        self.shape = (T, d_model, d_inter, E, topk)
+        self.plan = get_plan(T, d_model, d_inter, E, topk)
+        n = max(int(self.plan.workspace_bytes), 256)
+        self.workspace = torch.empty(n + 256, dtype=torch.uint8, device=device)
+        base = self.workspace.data_ptr()
+        self.ws_ptr = (base + 255) // 256 * 256
+        self.ws_bytes = n
+
+    def region(self, name: str, dtype, shape):
+        """A torch view of one workspace region (for inspection in tests)."""
+        import torch
+
+        off, nbytes = self.plan.region(name)
+        start = self.ws_ptr - self.workspace.data_ptr() + off
+        elem = torch.empty((), dtype=dtype).element_size()
+        count = 1
+        for s in shape:
+            count *= s
+        assert count * elem <= nbytes or nbytes == 0
+        return self.workspace[start:start + count * elem].view(dtype).view(*shape)
+
+    def forward(self, hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out=None,
+                stream=None):
+        import torch
+
+        T, D, I, E, K = self.shape
+        if out is None:
+            out = torch.empty((T, D), dtype=torch.bfloat16, device=hidden.device)
+        for t in (hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("all tensors must be contiguous CUDA tensors")
+        if hidden.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+            raise ValueError("hidden and out must be bfloat16")
+        if topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
+            raise ValueError("topk_ids must be int32 and topk_weights float32")
+        if stream is None:
+            stream = torch.cuda.current_stream(hidden.device).cuda_stream
+        set_workspace(self.ws_ptr, self.ws_bytes)
+        code = forward_ptr(hidden.data_ptr(), w13.data_ptr(), w13_scale.data_ptr(), w2.data_ptr(),
+                           w2_scale.data_ptr(), topk_ids.data_ptr(), topk_weights.data_ptr(),
+                           out.data_ptr(), T, D, I, E, K, stream)
+        _check(code, "moe_mxfp4_forward")
+        return out
+
+    def device_status(self, stream=None) -> int:
+        import torch
+
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        set_workspace(self.ws_ptr, self.ws_bytes)
+        return last_device_status(stream)

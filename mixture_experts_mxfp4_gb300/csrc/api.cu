@@ -1,0 +1,342 @@
+// Host side of the C ABI (include/moe_mxfp4.h): argument validation, workspace
+// planning, TMA descriptor encoding and the launch sequence
+//   route -> quant -> stage-1 GEMM -> stage-2 GEMM -> top-k sum
+// on the caller's stream.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_mxfp4.h"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 256;
+
+struct WorkspaceReg {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+
+std::mutex g_mu;
+WorkspaceReg g_ws[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool supported_k(int k) { return k == 128 || k == 256 || (k > 0 && k % 512 == 0); }
+
+moe_status_t validate_shape(int T, int D, int I, int E, int K) {
+    if (T < 0 || E < 1 || E > 1024 || K < 1 || K > 16) return MOE_ERR_INVALID_ARG;
+    if (D <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (!supported_k(D) || !supported_k(I)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)T * K > (1LL << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+// Maximum routes per GEMM tile: small tiles when experts see few routes
+// (decode), full 128-row tiles when they see many (prefill, dense shards).
+int choose_tile_rows(int T, int E, int K) {
+    const double per_expert = (double)T * K / (double)E;
+    if (per_expert > 48.0) return 128;
+    if (per_expert > 24.0) return 64;
+    if (per_expert > 8.0) return 32;
+    return 16;
+}
+
+void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
+    memset(pl, 0, sizeof(*pl));
+    const long long R = (long long)T * K;
+    const long long used = R < E ? R : E;
+    long long cap = R + used * (kBlockM - 1);
+    cap = (cap + kBlockM - 1) / kBlockM * kBlockM;
+    pl->block_m = kBlockM;
+    pl->tile_rows = choose_tile_rows(T, E, K);
+    pl->cap = (int)cap;
+    pl->a1s_stride = (int)round_up((size_t)(D / 32), 16);
+    pl->a2s_stride = (int)round_up((size_t)(I / 32), 16);
+    pl->stage1_splits = 1;
+    pl->max_tiles = (int)(cap / kBlockM);
+    const size_t n_counters = (size_t)pl->max_tiles * (size_t)(I / 64);
+    size_t b[MOE_WS_NUM_REGIONS];
+    b[MOE_WS_STATUS] = 16 * sizeof(uint32_t);
+    b[MOE_WS_COUNTERS] = n_counters * sizeof(uint32_t);
+    b[MOE_WS_SORTED_IDS] = (size_t)cap * 4;
+    b[MOE_WS_SORTED_W] = (size_t)cap * 4;
+    b[MOE_WS_BLOCK_EXPERT] = (size_t)(cap / kBlockM) * 4;
+    b[MOE_WS_SEG_START] = (size_t)(E + 1) * 4;
+    b[MOE_WS_ROUTE_POS] = (size_t)R * 4;
+    b[MOE_WS_NUM_VALID] = 4 * 4;
+    b[MOE_WS_TILES] = (size_t)pl->max_tiles * 16;
+    b[MOE_WS_A1Q] = (size_t)cap * (D / 2);
+    b[MOE_WS_A1S] = (size_t)cap * pl->a1s_stride;
+    b[MOE_WS_A2Q] = (size_t)cap * (I / 2);
+    b[MOE_WS_A2S] = (size_t)cap * pl->a2s_stride;
+    b[MOE_WS_P] = (size_t)R * D * 4;
+    b[MOE_WS_PARTIAL] = 0;
+    size_t off = 0;
+    for (int i = 0; i < MOE_WS_NUM_REGIONS; ++i) {
+        pl->offset[i] = off;
+        pl->bytes[i] = b[i];
+        off = round_up(off + b[i], kAlign);
+    }
+    pl->workspace_bytes = off;
+}
+
+WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl) {
+    uint8_t* b = static_cast<uint8_t*>(base);
+    WsPtrs w;
+    w.status = reinterpret_cast<uint32_t*>(b + pl.offset[MOE_WS_STATUS]);
+    w.counters = reinterpret_cast<uint32_t*>(b + pl.offset[MOE_WS_COUNTERS]);
+    w.sorted_ids = reinterpret_cast<int32_t*>(b + pl.offset[MOE_WS_SORTED_IDS]);
+    w.sorted_w = reinterpret_cast<float*>(b + pl.offset[MOE_WS_SORTED_W]);
+    w.block_expert = reinterpret_cast<int32_t*>(b + pl.offset[MOE_WS_BLOCK_EXPERT]);
+    w.seg_start = reinterpret_cast<int32_t*>(b + pl.offset[MOE_WS_SEG_START]);
+    w.route_pos = reinterpret_cast<int32_t*>(b + pl.offset[MOE_WS_ROUTE_POS]);
+    w.num_valid = reinterpret_cast<int32_t*>(b + pl.offset[MOE_WS_NUM_VALID]);
+    w.tiles = reinterpret_cast<int4*>(b + pl.offset[MOE_WS_TILES]);
+    w.a1q = b + pl.offset[MOE_WS_A1Q];
+    w.a1s = b + pl.offset[MOE_WS_A1S];
+    w.a2q = b + pl.offset[MOE_WS_A2Q];
+    w.a2s = b + pl.offset[MOE_WS_A2S];
+    w.P = reinterpret_cast<float*>(b + pl.offset[MOE_WS_P]);
+    w.partial = reinterpret_cast<float*>(b + pl.offset[MOE_WS_PARTIAL]);
+    return w;
+}
+
+// ------------------------------------------------------------------ TMA maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D u8 tensor [rows][inner] with row stride `stride` bytes, box {bx, by}.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
+              uint32_t bx, uint32_t by, CUtensorMapSwizzle swz) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {stride};
+    cuuint32_t box[2] = {bx, by};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Weight-scale map: [rows][S] e8m0 bytes; S >= 16 read 16 bytes per stage, S < 16
+// read through a [rows*S/16][16] view so that one box holds box_rows whole rows.
+bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int box_rows) {
+    if (S >= 16)
+        return make_map(m, base, (uint64_t)S, rows, (uint64_t)S, 16, (uint32_t)box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    return make_map(m, base, 16, rows * S / 16, 16, 16, (uint32_t)(box_rows * S / 16),
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Pipeline geometry of one GEMM stage for contraction length Kc.
+void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1) {
+    g.kstage_elems = Kc >= 512 ? 512 : Kc;
+    g.kstages = Kc / g.kstage_elems;
+    g.kb = g.kstage_elems >= 256 ? 128 : 64;
+    g.nkt = (g.kstage_elems / 2) / g.kb;
+    g.natoms = g.kstage_elems / 128;
+    const int S = Kc / 32;
+    g.a_scale_small = S < 16 ? 1 : 0;
+    g.sr_a = S < 16 ? S : 16;
+    g.b_scale_x = S >= 16 ? 1 : 0;
+    g.tile_rows = tile_rows;
+    const uint32_t a_bytes = 128u * (g.kstage_elems / 2);
+    const uint32_t b_bytes = (uint32_t)tile_rows * (g.kstage_elems / 2);
+    g.off_b = a_bytes;
+    g.off_sa = g.off_b + b_bytes;
+    g.off_sb = g.off_sa + 2048;
+    g.stage_bytes = (uint32_t)round_up(g.off_sb + 2048, 1024);
+    const uint32_t fixed = 1024 /*align slack*/ + 256 /*barriers*/ + (stage1 ? 4096u : 0u);
+    const uint32_t budget = 227u * 1024u - fixed;
+    int ns = (int)(budget / g.stage_bytes);
+    if (ns > kMaxStages) ns = kMaxStages;
+    g.num_stages = ns;
+    g.off_bar = (uint32_t)ns * g.stage_bytes;
+    g.off_xchg = g.off_bar + 256;
+    g.smem_bytes = g.off_xchg + (stage1 ? 4096u : 0u) + 1024u;
+    const uint32_t cols = 2u * tile_rows + (uint32_t)ns * 8u * g.natoms;
+    uint32_t alloc = 32;
+    while (alloc < cols) alloc <<= 1;
+    g.tmem_cols = alloc;
+    g.sf_col0 = 2u * tile_rows;
+}
+
+int num_sms(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return 148;
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_num_sms[dev] = n > 0 ? n : 148;
+    }
+    return g_num_sms[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_mxfp4_version(void) { return "moe_mxfp4 0.1 (sm_103a, tcgen05 mxf4)"; }
+
+const char* moe_mxfp4_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+moe_status_t moe_mxfp4_get_plan(int T, int d_model, int d_inter, int E, int topk,
+                                moe_mxfp4_plan_t* plan) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = validate_shape(T, d_model, d_inter, E, topk);
+    if (st != MOE_OK) return st;
+    fill_plan(T, d_model, d_inter, E, topk, plan);
+    return MOE_OK;
+}
+
+size_t moe_mxfp4_workspace_size(int T, int d_model, int d_inter, int E, int topk) {
+    moe_mxfp4_plan_t pl;
+    if (moe_mxfp4_get_plan(T, d_model, d_inter, E, topk, &pl) != MOE_OK) return 0;
+    return pl.workspace_bytes;
+}
+
+moe_status_t moe_mxfp4_set_workspace(void* dev_ptr, size_t bytes) {
+    if (dev_ptr && (reinterpret_cast<uintptr_t>(dev_ptr) % kAlign) != 0) return MOE_ERR_MISALIGNED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_ws[dev].ptr = dev_ptr;
+    g_ws[dev].bytes = dev_ptr ? bytes : 0;
+    return MOE_OK;
+}
+
+moe_status_t moe_mxfp4_last_device_status(cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void* base;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        base = g_ws[dev].ptr;
+    }
+    if (!base) return MOE_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t word = 0;
+    // status is region 0 at offset 0 of every plan
+    if (cudaMemcpy(&word, base, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return word ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* w13_scale,
+                               const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                               const float* topk_weights, void* out, int T, int d_model,
+                               int d_inter, int E, int topk, cudaStream_t stream) {
+    const int D = d_model, I = d_inter, K = topk;
+    moe_status_t st = validate_shape(T, D, I, E, K);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (!hidden || !w13 || !w13_scale || !w2 || !w2_scale || !topk_ids || !topk_weights || !out)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_scale) || !aligned16(w2) ||
+        !aligned16(w2_scale) || !aligned16(topk_ids) || !aligned16(topk_weights) || !aligned16(out))
+        return MOE_ERR_MISALIGNED;
+
+    moe_mxfp4_plan_t pl;
+    fill_plan(T, D, I, E, K, &pl);
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void* base;
+    size_t ws_bytes;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        base = g_ws[dev].ptr;
+        ws_bytes = g_ws[dev].bytes;
+    }
+    if (!base || ws_bytes < pl.workspace_bytes) return MOE_ERR_WORKSPACE;
+    const WsPtrs ws = ws_ptrs(base, pl);
+    const int R = T * K;
+
+    // ---------------------------------------------------------- GEMM params
+    GemmParams g1;
+    memset(&g1, 0, sizeof(g1));
+    g1.ws = ws;
+    g1.D = D; g1.I = I; g1.E = E; g1.K = K; g1.R = R;
+    g1.a1s_stride = pl.a1s_stride;
+    g1.a2s_stride = pl.a2s_stride;
+    gemm_geometry(g1, D, pl.tile_rows, true);
+    g1.n_ftiles = I / 64;
+    g1.ksplits = pl.stage1_splits;
+
+    GemmParams g2 = g1;
+    gemm_geometry(g2, I, pl.tile_rows, false);
+    g2.n_ftiles = D / 128;
+    g2.ksplits = 1;
+
+    // ---------------------------------------------------------- TMA maps
+    CUtensorMap mA1, mSA1, mB1, mSB1, mA2, mSA2, mB2, mSB2;
+    const CUtensorMapSwizzle sw1 = g1.kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle sw2 = g2.kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    bool ok = true;
+    ok = ok && make_map(&mA1, w13, D / 2, (uint64_t)E * 2 * I, D / 2, g1.kb, 64, sw1);
+    ok = ok && make_scale_map(&mSA1, w13_scale, (uint64_t)E * 2 * I, D / 32, 64);
+    ok = ok && make_map(&mB1, ws.a1q, D / 2, pl.cap, D / 2, g1.kb, 16, sw1);
+    ok = ok && make_map(&mSB1, ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, 16,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && make_map(&mA2, w2, I / 2, (uint64_t)E * D, I / 2, g2.kb, 128, sw2);
+    ok = ok && make_scale_map(&mSA2, w2_scale, (uint64_t)E * D, I / 32, 128);
+    ok = ok && make_map(&mB2, ws.a2q, I / 2, pl.cap, I / 2, g2.kb, 16, sw2);
+    ok = ok && make_map(&mSB2, ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, 16,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return MOE_ERR_CUDA;
+
+    // ---------------------------------------------------------- launches
+    const int sms = num_sms(dev);
+    const int n_counters = pl.max_tiles * (I / 64);
+    if (launch_route(topk_ids, topk_weights, T, K, E, pl.tile_rows, pl.cap, n_counters, ws,
+                     stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm(1, mA1, mSA1, mB1, mSB1, g1, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm(2, mA2, mSA2, mB2, mSB2, g2, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_reduce(topk_ids, T, K, E, D, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,390 @@
+// Grouped block-scaled MXFP4 GEMMs of the MoE forward on tcgen05 tensor cores.
+//
+// Operand roles (weights on the MMA M side, routes on the N side): for one work
+// item the CTA computes
+//     acc[m, j] = sum_k (Wtile[m, k] * sW) * (Act[slot_j, k] * sA)      (fp32, TMEM)
+// with Wtile 128 weight rows and j over up to `tile_rows` sorted route slots of
+// one expert.  M = 128 fixed, N = rows of the route tile (16..128).
+//
+// Stage 1 (kernelbot-amd-moe-mxfp4-723815, solution.py, kernel_stage1 and
+// _reference_forward: gate rows [0, I), up rows [I, 2I) of w13; SwiGLU
+// silu(g) * u; bf16 intermediate as in kernelbot-amd-moe-mxfp4-754773,
+// flower_moe.py, custom_kernel): the 128 A rows are 64 gate rows followed by
+// the 64 matching up rows, so TMEM lanes 0..63 hold gate and 64..127 up
+// accumulators of 64 features.  The epilogue forms bf16(silu(g) * u) and
+// requantises each 32-feature block to MXFP4 in place of the bf16 a2 buffer.
+//
+// Stage 2 (solution.py, kernel_stage2: down projection, weight applied to the
+// output; flower_moe.py passes sorted_weights to stage 2): A = 128 rows of w2,
+// the epilogue writes w[route] * y into P[route, :] for the per-token sum.
+//
+// Pipeline (one CTA per SM, persistent over work items):
+//   warp 0  TMA producer: weight tile, route tile, raw scale tiles -> smem ring
+//   warp 1  MMA warp: rearranges the scale tiles into the tcgen05 scale-factor
+//           layout, copies them to TMEM (tcgen05.cp) and issues tcgen05.mma
+//   warp 2  allocates / frees TMEM
+//   warps 4-7  epilogue: tcgen05.ld from the double-buffered accumulator
+// All waits are bounded (ptx.cuh).
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+struct Item {
+    int e, row0, nrows, f, ks0, ks1, unit, split;
+};
+
+__device__ __forceinline__ Item decode_item(const GemmParams& p, int it) {
+    Item x;
+    const int per_tile = p.n_ftiles * p.ksplits;
+    const int tile = it / per_tile;
+    const int rem = it - tile * per_tile;
+    x.f = rem / p.ksplits;
+    x.split = rem - x.f * p.ksplits;
+    const int4 t = p.ws.tiles[tile];
+    x.e = t.x;
+    x.row0 = t.y;
+    x.nrows = t.z;
+    const int per = p.kstages / p.ksplits;
+    x.ks0 = x.split * per;
+    x.ks1 = x.ks0 + per;
+    x.unit = tile * p.n_ftiles + x.f;
+    return x;
+}
+
+// Rearrange a raw scale tile (row m at m*sr bytes, 4-byte chunk c = scales of
+// K elements [128c, 128c+128)) into natoms scale-factor atoms in place: atom c
+// holds 128 rows as [m % 32][m / 32][4 bytes], the layout tcgen05.cp .32x128b
+// .warpx4 expects.  Whole warp; rows >= 128 are not touched.
+__device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, uint32_t lane) {
+    uint32_t v[4][4];
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1) {
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(buf + (m1 * 32 + lane) * sr);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[m1][c] = (c < natoms) ? row[c] : 0u;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c < natoms) {
+            uint4 w = make_uint4(v[0][c], v[1][c], v[2][c], v[3][c]);
+            *reinterpret_cast<uint4*>(buf + c * 512 + lane * 16) = w;
+        }
+    }
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmSA,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmSB,
+                    const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+    const int NS = p.num_stages;
+
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* tfull = empty + kMaxStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* xchg = reinterpret_cast<float*>(smem + p.off_xchg);
+    uint32_t* status = p.ws.status;
+
+    const int num_tiles = p.ws.num_valid[2];
+    const int num_items = num_tiles * p.n_ftiles * p.ksplits;
+    if ((int)blockIdx.x >= num_items) return;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, p.tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int kbytes_stage = p.kstage_elems / 2;  // bytes of one row per stage
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            uint32_t issued = 0;   // bit s: stage s has been filled at least once
+            uint32_t last_ph = 0;  // bit s: parity of the last fill of stage s
+            for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+                const Item x = decode_item(p, it);
+                for (int ks = x.ks0; ks < x.ks1; ++ks) {
+                    if (!mbar_wait(&empty[s], ph ^ 1u, status, kErrTimeoutEmpty, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + (size_t)s * p.stage_bytes;
+                    const uint32_t tx = (uint32_t)(128 + x.nrows) * kbytes_stage +
+                                        128u * p.sr_a + (uint32_t)x.nrows * 16u;
+                    mbar_arrive_expect_tx(&full[s], tx);
+                    for (int kt = 0; kt < p.nkt; ++kt) {
+                        const int kx = ks * kbytes_stage + kt * p.kb;
+                        uint8_t* a_dst = st + kt * 128 * p.kb;
+                        if (STAGE == 1) {
+                            const int rg = x.e * 2 * p.I + x.f * 64;
+                            tma_load_2d_hint(a_dst, &tmA, kx, rg, &full[s], pol_w);
+                            tma_load_2d_hint(a_dst + 64 * p.kb, &tmA, kx, rg + p.I, &full[s], pol_w);
+                        } else {
+                            tma_load_2d_hint(a_dst, &tmA, kx, x.e * p.D + x.f * 128, &full[s], pol_w);
+                        }
+                        uint8_t* b_dst = st + p.off_b + kt * p.tile_rows * p.kb;
+                        for (int b = 0; b < x.nrows / 16; ++b)
+                            tma_load_2d(b_dst + b * 16 * p.kb, &tmB, kx, x.row0 + 16 * b, &full[s]);
+                    }
+                    // raw weight scales: 128 rows of sr_a bytes
+                    uint8_t* sa = st + p.off_sa;
+                    if (STAGE == 1) {
+                        const int rg = x.e * 2 * p.I + x.f * 64;
+                        if (p.a_scale_small) {
+                            const int q = 16 / p.sr_a;  // rows per 16-byte view row
+                            tma_load_2d(sa, &tmSA, 0, rg / q, &full[s]);
+                            tma_load_2d(sa + 64 * p.sr_a, &tmSA, 0, (rg + p.I) / q, &full[s]);
+                        } else {
+                            tma_load_2d(sa, &tmSA, ks * 16, rg, &full[s]);
+                            tma_load_2d(sa + 64 * 16, &tmSA, ks * 16, rg + p.I, &full[s]);
+                        }
+                    } else {
+                        const int rg = x.e * p.D + x.f * 128;
+                        if (p.a_scale_small)
+                            tma_load_2d(sa, &tmSA, 0, rg / (16 / p.sr_a), &full[s]);
+                        else
+                            tma_load_2d(sa, &tmSA, ks * 16, rg, &full[s]);
+                    }
+                    // raw activation scales: nrows rows of 16 bytes
+                    uint8_t* sb = st + p.off_sb;
+                    for (int b = 0; b < x.nrows / 16; ++b)
+                        tma_load_2d(sb + b * 256, &tmSB, p.b_scale_x ? ks * 16 : 0, x.row0 + 16 * b,
+                                    &full[s]);
+                    issued |= 1u << s;
+                    last_ph = (last_ph & ~(1u << s)) | (ph << s);
+                    if (++s == NS) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA exits: the
+                // last fill of stage i completes the phase with parity last_ph[i].
+                for (int i = 0; i < NS; ++i) {
+                    if (!((issued >> i) & 1u)) continue;
+                    const uint32_t par = (last_ph >> i) & 1u;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(smem_u32(&full[i]), par)) {
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            atomicOr(status, kErrTimeoutDrain);
+                            break;
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        int s = 0;
+        uint32_t ph = 0;
+        int local = 0;
+        bool ok = true;
+        const uint32_t layout = (p.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
+        const uint32_t sbo = 8u * p.kb;
+        const int ksteps = p.kstage_elems / 64;
+        const int steps_per_box = p.kb / 32;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++local) {
+            const Item x = decode_item(p, it);
+            const int a = local & 1;
+            const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+            if (!mbar_wait(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(a * p.tile_rows);
+            const uint32_t N = (uint32_t)x.nrows;
+            for (int ks = x.ks0; ks < x.ks1; ++ks) {
+                if (!mbar_wait(&full[s], ph, status, kErrTimeoutFull, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + (size_t)s * p.stage_bytes;
+                sf_to_atoms(st + p.off_sa, p.sr_a, p.natoms, lane);
+                sf_to_atoms(st + p.off_sb, 16, p.natoms, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t sfa = tmem_base + p.sf_col0 + (uint32_t)(s * 8 * p.natoms);
+                    const uint32_t sfb = sfa + 4u * p.natoms;
+                    for (int c = 0; c < p.natoms; ++c) {
+                        tmem_cp_sf(sfa + 4u * c, smem_desc(smem_u32(st + p.off_sa + 512 * c), 0, 128, 0));
+                        tmem_cp_sf(sfb + 4u * c, smem_desc(smem_u32(st + p.off_sb + 512 * c), 0, 128, 0));
+                    }
+                    const uint32_t a_base = smem_u32(st);
+                    const uint32_t b_base = smem_u32(st + p.off_b);
+                    for (int j = 0; j < ksteps; ++j) {
+                        const int kt = j / steps_per_box;
+                        const uint32_t koff = (uint32_t)(j % steps_per_box) * 32u;
+                        const uint64_t ad = smem_desc(a_base + kt * 128 * p.kb + koff, 16, sbo, layout);
+                        const uint64_t bd =
+                            smem_desc(b_base + kt * p.tile_rows * p.kb + koff, 16, sbo, layout);
+                        const uint32_t sid = (uint32_t)(j & 1) * 2u;
+                        const uint32_t idesc = mxf4_idesc(128, N, sid, sid);
+                        mma_mxf4(d_tmem, ad, bd, idesc, sfa + 4u * (j >> 1), sfb + 4u * (j >> 1),
+                                 (ks > x.ks0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[s]);
+                }
+                __syncwarp();
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(&tfull[a]);
+            __syncwarp();
+        }
+        if (!ok && lane == 0) {
+            // Wait for every MMA/copy already issued before TMEM is freed.
+            tc_commit(drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(drain), 0)) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(status, kErrTimeoutDrain);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t q = warp & 3u;  // TMEM lane quadrant of this warp
+        const int R = p.R;
+        int local = 0;
+        for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++local) {
+            const Item x = decode_item(p, it);
+            const int a = local & 1;
+            const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+            if (!mbar_wait(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + ((q * 32u) << 16) + (uint32_t)(a * p.tile_rows);
+            const int nchunks = x.nrows / 16;
+            if (STAGE == 1) {
+                const int n0 = x.f * 64;  // first feature of the tile
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[16];
+                    tmem_ld16(tacc + 16u * c, v);
+                    tmem_ld_wait();
+                    if (q >= 2) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) xchg[((q - 2) * 16 + i) * 32 + lane] = v[i];
+                    }
+                    named_bar_sync(1, 128);
+                    if (q < 2) {
+                        const int slot_l = x.row0 + 16 * c + (int)(lane & 15);
+                        const int rid_l = __ldg(p.ws.sorted_ids + slot_l);
+                        const int feat = n0 + 32 * (int)q;  // first feature of this warp's block
+#pragma unroll 1
+                        for (int i = 0; i < 16; ++i) {
+                            const int rid = __shfl_sync(0xffffffffu, rid_l, i);
+                            if (rid >= R) continue;  // padding slot (warp-uniform)
+                            const float g = v[i];
+                            const float u = xchg[(q * 16 + i) * 32 + lane];
+                            const float sg = g / (1.0f + expf(-g));
+                            const float hv = __bfloat162float(__float2bfloat16_rn(sg * u));
+                            const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
+                            const uint32_t amax = __reduce_max_sync(0xffffffffu, hb);
+                            const uint32_t sbyte = mx_scale_byte(amax);
+                            const uint32_t code = e2m1_code(hv, sbyte, mx_inv_scale(sbyte == 255u ? 0u : sbyte));
+                            const uint32_t nb = __shfl_down_sync(0xffffffffu, code, 1);
+                            const uint32_t byte = (code | (nb << 4)) & 0xffu;
+                            const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
+                            const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
+                            const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
+                            const int slot = x.row0 + 16 * c + i;
+                            if ((lane & 7u) == 0) {
+                                const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                                *reinterpret_cast<uint32_t*>(p.ws.a2q + (size_t)slot * (p.I / 2) +
+                                                             feat / 2 + lane / 2) = word;
+                            }
+                            if (lane == 0)
+                                p.ws.a2s[(size_t)slot * p.a2s_stride + feat / 32] = (uint8_t)sbyte;
+                        }
+                    }
+                    named_bar_sync(1, 128);
+                }
+            } else {
+                const int n = x.f * 128 + 32 * (int)q + (int)lane;  // output feature of this lane
+                for (int c = 0; c < nchunks; ++c) {
+                    float v[16];
+                    tmem_ld16(tacc + 16u * c, v);
+                    tmem_ld_wait();
+                    const int slot_l = x.row0 + 16 * c + (int)(lane & 15);
+                    const int rid_l = __ldg(p.ws.sorted_ids + slot_l);
+                    const float w_l = __ldg(p.ws.sorted_w + slot_l);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int rid = __shfl_sync(0xffffffffu, rid_l, i);
+                        const float wv = __shfl_sync(0xffffffffu, w_l, i);
+                        if (rid < R) p.ws.P[(size_t)rid * p.D + n] = wv * v[i];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[a]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem_base, p.tmem_cols);
+}
+
+cudaError_t launch_gemm(int stage, const CUtensorMap& tmA, const CUtensorMap& tmSA,
+                        const CUtensorMap& tmB, const CUtensorMap& tmSB, const GemmParams& p,
+                        int grid, cudaStream_t stream) {
+    auto kern = (stage == 1) ? moe_gemm_kernel<1> : moe_gemm_kernel<2>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, kGemmThreads, p.smem_bytes, stream>>>(tmA, tmSA, tmB, tmSB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

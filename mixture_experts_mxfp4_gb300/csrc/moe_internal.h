@@ -1,0 +1,71 @@
+// Internal declarations shared by the library's translation units: the
+// workspace pointer set, the GEMM launch parameters and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Device pointers into the caller's workspace (see moe_mxfp4_plan_t).
+struct WsPtrs {
+    uint32_t* status;      // [16]
+    uint32_t* counters;    // split-K arrival counters
+    int32_t* sorted_ids;   // [cap]
+    float* sorted_w;       // [cap]
+    int32_t* block_expert; // [cap / block_m]
+    int32_t* seg_start;    // [E + 1]
+    int32_t* route_pos;    // [R]
+    int32_t* num_valid;    // [4]
+    int4* tiles;           // [max_tiles]: {expert, first slot, rows, 0}
+    uint8_t* a1q;          // [cap][D/2]
+    uint8_t* a1s;          // [cap][a1s_stride]
+    uint8_t* a2q;          // [cap][I/2]
+    uint8_t* a2s;          // [cap][a2s_stride]
+    float* P;              // [R][D]
+    float* partial;        // split-K partial accumulators
+};
+
+// Parameters of one grouped block-scaled GEMM launch (stage 1 or stage 2).
+struct GemmParams {
+    WsPtrs ws;
+    int D, I, E, K, R;
+    int tile_rows;      // maximum MMA N (routes per tile), multiple of 16, <= 128
+    int n_ftiles;       // stage 1: I / 64 feature tiles; stage 2: D / 128 output tiles
+    int ksplits;        // stage-1 K splits (1 = none)
+    int kstages;        // K / kstage_elems
+    int kstage_elems;   // K elements per pipeline stage: 128, 256 or 512
+    int kb;             // bytes per row of one TMA box along K: 64 or 128
+    int nkt;            // TMA boxes along K per stage (kstage_elems / 2 / kb)
+    int natoms;         // 128-element scale chunks per stage (kstage_elems / 128)
+    int sr_a;           // bytes per raw weight-scale row in shared memory: 4, 8 or 16
+    int a_scale_small;  // weight scales read through a [rows*S/16, 16] view
+    int b_scale_x;      // 1 when activation scales advance 16 bytes per stage
+    int num_stages;     // shared-memory pipeline depth
+    uint32_t tmem_cols; // TMEM columns allocated
+    uint32_t sf_col0;   // first TMEM column of the per-stage scale-factor regions
+    uint32_t stage_bytes, off_b, off_sa, off_sb; // per-stage layout (A at 0)
+    uint32_t off_bar, off_xchg;                  // barriers, epilogue exchange buffer
+    uint32_t smem_bytes;                         // dynamic shared memory requested
+    int a2s_stride;
+    int a1s_stride;
+};
+
+constexpr int kBlockM = 16;          // slots per padded block
+constexpr int kGemmThreads = 256;    // 8 warps: producer, MMA, TMEM owner, spare, 4 epilogue
+constexpr int kMaxStages = 8;
+
+cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, int K, int E,
+                         int tile_rows, int cap, int n_counters, const WsPtrs& ws,
+                         cudaStream_t stream);
+cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride,
+                         const WsPtrs& ws, cudaStream_t stream);
+cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
+                          const WsPtrs& ws, cudaStream_t stream);
+cudaError_t launch_gemm(int stage, const CUtensorMap& tmA, const CUtensorMap& tmSA,
+                        const CUtensorMap& tmB, const CUtensorMap& tmSB, const GemmParams& p,
+                        int grid, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,281 @@
+// Routing (counting sort of routes by expert), dynamic MXFP4 quantisation of
+// the hidden states with the scatter into sorted order, and the per-token
+// deterministic top-k sum.
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+// ============================================================== routing
+//
+// One CTA of 1024 threads.  Structure from kernelbot-amd-moe-mxfp4-723815
+// (solution.py: kernel_count_tokens -> kernel_prefix_sum -> kernel_scatter_tokens)
+// with block_m padding per expert and per-block expert ids as in
+// kernelbot-amd-moe-mxfp4-754773 (flower_moe.py: moe_sorting_fwd buffers), the
+// route id t*topk+k and sentinel T*topk of b12x moe/fused/w4a16/kernel.py
+// (_read_moe_block_data).  Deterministic: each warp owns a contiguous chunk of
+// routes; a per-warp, per-expert histogram and its prefix over warps give every
+// route its rank, so routes appear in ascending route id within an expert.
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+// Inclusive scan over the 1024 threads of two values at once.
+__device__ __forceinline__ void block_scan2(int& a, int& b, int* wsum_a, int* wsum_b) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ta = __shfl_up_sync(0xffffffffu, a, o);
+        const int tb = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) {
+            a += ta;
+            b += tb;
+        }
+    }
+    if (lane == 31) {
+        wsum_a[warp] = a;
+        wsum_b[warp] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int xa = wsum_a[lane], xb = wsum_b[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, xa, o);
+            const int tb = __shfl_up_sync(0xffffffffu, xb, o);
+            if (lane >= o) {
+                xa += ta;
+                xb += tb;
+            }
+        }
+        wsum_a[lane] = xa;
+        wsum_b[lane] = xb;
+    }
+    __syncthreads();
+    if (warp > 0) {
+        a += wsum_a[warp - 1];
+        b += wsum_b[warp - 1];
+    }
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    moe_route_kernel(const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w,
+                     int T, int K, int E, int tile_rows, int cap, int n_counters, WsPtrs ws) {
+    extern __shared__ int route_smem[];
+    int* hist = route_smem;                 // [32][E]: per-warp counts, then prefixes
+    int* seg = hist + kRouteWarps * E;      // [E + 1]
+    int* wsum = seg + (E + 1);              // [64]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = T * K;
+    const int bm = kBlockM;
+
+    for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
+    for (int i = tid; i < n_counters; i += kRouteThreads) ws.counters[i] = 0;
+    if (tid < 16) ws.status[tid] = 0;
+    __syncthreads();
+
+    const int chunk = (R + kRouteWarps - 1) / kRouteWarps;
+    const int r_begin = min(warp * chunk, R);
+    const int r_end = min(r_begin + chunk, R);
+
+    // Pass 1: per-warp histogram (one leader per distinct expert in a batch).
+    for (int base = r_begin; base < r_end; base += 32) {
+        const int r = base + lane;
+        const int e = (r < r_end) ? topk_ids[r] : -1;
+        const bool valid = (r < r_end) && e >= 0 && e < E;
+        const int key = valid ? e : -1;
+        const uint32_t m = __match_any_sync(0xffffffffu, key);
+        if (valid && lane == __ffs(m) - 1) hist[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // Per expert: prefix over warps, padded length, tiles.
+    int cnt = 0, padded = 0, ntiles = 0;
+    if (tid < E) {
+        int run = 0;
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int c = hist[w * E + tid];
+            hist[w * E + tid] = run;
+            run += c;
+        }
+        cnt = run;
+        padded = (cnt + bm - 1) / bm * bm;
+        ntiles = (padded + tile_rows - 1) / tile_rows;
+    }
+    int seg_incl = padded, tile_incl = ntiles;
+    block_scan2(seg_incl, tile_incl, wsum, wsum + 32);
+    const int seg_e = seg_incl - padded, tile_e = tile_incl - ntiles;
+    if (tid < E) seg[tid] = seg_e;
+    if (tid == kRouteThreads - 1) seg[E] = seg_incl;  // total padded length
+    __shared__ int s_totals[2];
+    if (tid == kRouteThreads - 1) {
+        s_totals[0] = seg_incl;
+        s_totals[1] = tile_incl;
+    }
+    int valid_incl = cnt, dummy = 0;
+    __syncthreads();
+    block_scan2(valid_incl, dummy, wsum, wsum + 32);
+    const int total_padded = s_totals[0], total_tiles = s_totals[1];
+
+    if (tid <= E) ws.seg_start[tid] = seg[tid];
+    if (tid < E && cnt > 0) {
+        for (int j = 0; j < ntiles; ++j) {
+            const int rows = min(tile_rows, padded - j * tile_rows);
+            ws.tiles[tile_e + j] = make_int4(tid, seg_e + j * tile_rows, rows, 0);
+        }
+        for (int b = seg_e / bm; b < (seg_e + padded) / bm; ++b) ws.block_expert[b] = tid;
+        for (int p = seg_e + cnt; p < seg_e + padded; ++p) {
+            ws.sorted_ids[p] = R;
+            ws.sorted_w[p] = 0.0f;
+        }
+    }
+    for (int p = total_padded + tid; p < cap; p += kRouteThreads) {
+        ws.sorted_ids[p] = R;
+        ws.sorted_w[p] = 0.0f;
+    }
+    for (int b = total_padded / bm + tid; b < cap / bm; b += kRouteThreads) ws.block_expert[b] = -1;
+    if (tid == kRouteThreads - 1) {
+        ws.num_valid[0] = total_padded;
+        ws.num_valid[1] = valid_incl;
+        ws.num_valid[2] = total_tiles;
+        ws.num_valid[3] = 0;
+    }
+
+    // Pass 2: scatter in the same order; rank = warp prefix + rank in batch.
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int base = r_begin; base < r_end; base += 32) {
+        const int r = base + lane;
+        const int e = (r < r_end) ? topk_ids[r] : -1;
+        const bool valid = (r < r_end) && e >= 0 && e < E;
+        const int key = valid ? e : -1;
+        const uint32_t m = __match_any_sync(0xffffffffu, key);
+        if (valid) {
+            const int pos = seg[e] + hist[warp * E + e] + __popc(m & lt_mask);
+            ws.sorted_ids[pos] = r;
+            ws.sorted_w[pos] = topk_w[r];
+            ws.route_pos[r] = pos;
+        } else if (r < r_end) {
+            ws.route_pos[r] = -1;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(m) - 1) hist[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, int K, int E,
+                         int tile_rows, int cap, int n_counters, const WsPtrs& ws,
+                         cudaStream_t stream) {
+    const size_t smem = sizeof(int) * ((size_t)kRouteWarps * E + (E + 1) + 64);
+    cudaError_t err = cudaFuncSetAttribute(moe_route_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    moe_route_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, topk_w, T, K, E, tile_rows,
+                                                         cap, n_counters, ws);
+    return cudaGetLastError();
+}
+
+// ============================================================== quant + scatter
+//
+// One warp per token.  Lane g quantises 32-element block g (64 bytes of bf16,
+// four 16-byte loads) once, then writes its 16 code bytes and scale byte to
+// the sorted slot of every valid route of the token (the token's activation is
+// quantised once per token, as flower_moe.py does with topk=1 for hidden).
+
+constexpr int kQuantWarps = 8;
+
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    moe_quant_kernel(const __nv_bfloat16* __restrict__ hidden, int T, int K, int D,
+                     int a1s_stride, WsPtrs ws) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int pos[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pos[k] = (k < K) ? ws.route_pos[t * K + k] : -1;
+    const int nblk = D / 32;
+    const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)t * D);
+    for (int g = lane; g < nblk; g += 32) {
+        uint4 raw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + g * 4 + i);
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+        const uint32_t s = mx_scale_byte(amax);
+        const float inv = mx_inv_scale(s == 255u ? 0u : s);
+        uint32_t packed[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) packed[i / 8] |= e2m1_code(v[i], s, inv) << (4 * (i % 8));
+        const uint4 codes = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (pos[k] >= 0) {
+                *reinterpret_cast<uint4*>(ws.a1q + (size_t)pos[k] * (D / 2) + g * 16) = codes;
+                ws.a1s[(size_t)pos[k] * a1s_stride + g] = (uint8_t)s;
+            }
+        }
+    }
+}
+
+cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride,
+                         const WsPtrs& ws, cudaStream_t stream) {
+    const int grid = (T + kQuantWarps - 1) / kQuantWarps;
+    moe_quant_kernel<<<grid, kQuantWarps * 32, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(hidden), T, K, D, a1s_stride, ws);
+    return cudaGetLastError();
+}
+
+// ============================================================== top-k sum
+//
+// out[t, n] = bf16( sum over k ascending of P[t*K + k, n] ), skipping routes
+// whose id is outside [0, E).  P already holds w[t,k] * y (stage-2 epilogue).
+// Deterministic: one thread owns four outputs and adds in a fixed order.
+
+__global__ void __launch_bounds__(256)
+    moe_reduce_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int D,
+                      const float* __restrict__ P, __nv_bfloat16* __restrict__ out) {
+    const int n4 = D / 4;
+    const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long)T * n4) return;
+    const int t = (int)(idx / n4);
+    const int c = (int)(idx % n4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < K; ++k) {
+        const int e = __ldg(topk_ids + t * K + k);
+        if (e < 0 || e >= E) continue;
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(P + ((size_t)t * K + k) * D) + c);
+        acc.x = acc.x + v.x;
+        acc.y = acc.y + v.y;
+        acc.z = acc.z + v.z;
+        acc.w = acc.w + v.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + (size_t)t * D + 4 * c) = pk;
+}
+
+cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
+                          const WsPtrs& ws, cudaStream_t stream) {
+    const long total = (long)T * (D / 4);
+    const int grid = (int)((total + 255) / 256);
+    moe_reduce_kernel<<<grid, 256, 0, stream>>>(topk_ids, T, K, E, D, ws.P,
+                                                reinterpret_cast<__nv_bfloat16*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,115 @@
+"""Host-side tests of the C ABI that need no GPU: the library builds and loads,
+exports every entry point include/moe_mxfp4.h declares, plans workspaces
+consistently, and rejects bad arguments with the documented status codes before
+touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_mxfp4_gb300 import build
+
+    build.build()
+    import mixture_experts_mxfp4_gb300 as moe
+
+    return moe.load_library()
+
+
+def _declared_symbols():
+    syms = set()
+    inc = os.path.join(ROOT, "include")
+    for name in os.listdir(inc):
+        if not name.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, name)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(moe_mxfp4_\w+)\s*\(", text):
+            syms.add(m.group(1))
+    return sorted(syms)
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert "moe_mxfp4_forward" in declared
+    for s in declared:
+        assert hasattr(lib, s), f"{s} declared in include/ but not exported"
+    import mixture_experts_mxfp4_gb300 as moe
+
+    assert sorted(moe.EXPORTS) == sorted(declared)
+
+
+def test_status_strings(lib):
+    import mixture_experts_mxfp4_gb300 as moe
+
+    for code in moe.STATUS:
+        assert lib.moe_mxfp4_status_string(code)
+    assert b"sm_103a" in lib.moe_mxfp4_version()
+
+
+@pytest.mark.parametrize("shape", [(16, 256, 128, 9, 3), (16, 7168, 256, 257, 9),
+                                   (128, 7168, 256, 257, 9), (512, 7168, 2048, 33, 9),
+                                   (4096, 7168, 256, 257, 9), (1, 128, 128, 1, 1)])
+def test_plan_layout(lib, shape):
+    import mixture_experts_mxfp4_gb300 as moe
+    import oracle
+
+    T, D, I, E, K = shape
+    pl = moe.get_plan(*shape)
+    assert pl.block_m == 16
+    assert pl.cap == oracle.route_capacity(T, K, E, 16)
+    assert pl.tile_rows % 16 == 0 and 16 <= pl.tile_rows <= 128
+    assert pl.a1s_stride % 16 == 0 and pl.a1s_stride >= D // 32
+    assert pl.a2s_stride % 16 == 0 and pl.a2s_stride >= I // 32
+    R = T * K
+    expect = {"sorted_ids": pl.cap * 4, "sorted_w": pl.cap * 4, "route_pos": R * 4,
+              "a1q": pl.cap * D // 2, "a2q": pl.cap * I // 2, "P": R * D * 4,
+              "seg_start": (E + 1) * 4}
+    prev_end = 0
+    for i, name in enumerate(moe.REGIONS):
+        off, nb = pl.region(name)
+        assert off % 256 == 0
+        assert off >= prev_end
+        prev_end = off + nb
+        if name in expect:
+            assert nb == expect[name], name
+    assert pl.workspace_bytes >= prev_end
+    assert moe.workspace_size(*shape) == pl.workspace_bytes
+
+
+def test_validation_codes_without_device(lib):
+    import mixture_experts_mxfp4_gb300 as moe
+
+    good = 1 << 20  # a fake, 16-byte aligned address; never dereferenced on these paths
+    args = [good] * 8
+
+    def call(T=16, D=256, I=128, E=9, K=3, ptrs=None):
+        p = ptrs or args
+        return moe.forward_ptr(*p, T, D, I, E, K, 0)
+
+    assert call(T=-1) == 1
+    assert call(E=0) == 1
+    assert call(E=1025) == 1
+    assert call(K=0) == 1
+    assert call(K=17) == 1
+    assert call(D=0) == 1
+    assert call(D=384) == 2      # not 128, 256 or a multiple of 512
+    assert call(I=192) == 2
+    assert call(D=1000) == 2
+    assert call(T=0) == 0        # empty input: nothing to do
+    nulls = list(args)
+    nulls[3] = 0
+    assert call(ptrs=nulls) == 1
+    mis = list(args)
+    mis[0] = good + 8
+    assert call(ptrs=mis) == 3
+    assert moe.workspace_size(16, 384, 128, 9, 3) == 0
+    with pytest.raises(moe.MoeError):
+        moe.get_plan(16, 256, 100, 9, 3)
+    # workspace registration checks alignment before any device call
+    assert lib.moe_mxfp4_set_workspace(ctypes.c_void_p(good + 64), 1024) == 3

@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA library (called through the C ABI) against the CPU oracle.
+
+Bars (from the method's acceptance criteria):
+  * routing arrays, tile list and the quantised hidden rows: bit-exact;
+  * requantised intermediate (a2 codes/scales): at most 0.1% of elements differ,
+    each by at most one e2m1 step (fp32 accumulation order can flip a rounding);
+  * output: for every token row, max |gpu - oracle| <= 2e-2 * rms(oracle row),
+    and exactly zero where the oracle row is zero.
+Full-size workloads compare every token the oracle can afford and sample tokens
+otherwise; all inputs are seeded synthetic tensors (workloads module).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+ROW_TOL = 2e-2
+CODE_FRAC = 1e-3
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_mxfp4_gb300 import build
+
+    build.build()
+    import mixture_experts_mxfp4_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def _threads():
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def _unpack(p):
+    p = np.asarray(p, np.uint8)
+    return np.stack([p & 15, p >> 4], axis=-1).reshape(*p.shape[:-1], p.shape[-1] * 2)
+
+
+_E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6])
+
+
+def _deq(codes, scales, n):
+    v = _E2M1[_unpack(codes)]
+    return v * np.repeat(np.ldexp(1.0, scales[..., : n // 32].astype(np.int64) - 127), 32, axis=-1)
+
+
+def run_gpu(moe, inp, w):
+    dev = torch.device("cuda")
+    m = moe.MoeMXFP4(w.T, w.D, w.I, w.E, w.K)
+    t = {k: v.to(dev) for k, v in inp.items()}
+    out = m.forward(t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"],
+                    t["topk_ids"], t["topk_weights"])
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    return m, t, out
+
+
+def ws_arrays(m, w):
+    pl = m.plan
+    R = w.R
+    cap = pl.cap
+    get = lambda name, dt, shape: m.region(name, dt, shape).cpu().numpy()
+    return {
+        "sorted_ids": get("sorted_ids", torch.int32, (cap,)),
+        "sorted_w": get("sorted_w", torch.float32, (cap,)),
+        "block_expert": get("block_expert", torch.int32, (cap // 16,)),
+        "seg_start": get("seg_start", torch.int32, (w.E + 1,)),
+        "route_pos": get("route_pos", torch.int32, (R,)),
+        "num_valid": get("num_valid", torch.int32, (4,)),
+        "tiles": get("tiles", torch.int32, (pl.max_tiles, 4)),
+        "a1q": get("a1q", torch.uint8, (cap, w.D // 2)),
+        "a1s": get("a1s", torch.uint8, (cap, pl.a1s_stride)),
+        "a2q": get("a2q", torch.uint8, (cap, w.I // 2)),
+        "a2s": get("a2s", torch.uint8, (cap, pl.a2s_stride)),
+    }
+
+
+def check_routing(ws, ref, w, tile_rows):
+    n = int(ref["num_valid"][0])
+    np.testing.assert_array_equal(ws["num_valid"][:2], ref["num_valid"])
+    np.testing.assert_array_equal(ws["sorted_ids"], ref["sorted_ids"])
+    np.testing.assert_array_equal(ws["sorted_w"].view(np.uint32), ref["sorted_w"].view(np.uint32))
+    np.testing.assert_array_equal(ws["block_expert"], ref["block_expert"])
+    np.testing.assert_array_equal(ws["seg_start"], ref["seg_start"])
+    np.testing.assert_array_equal(ws["route_pos"], ref["route_pos"])
+    # tile list: each expert's padded segment cut into tile_rows pieces, in order
+    tiles = []
+    ss = ref["seg_start"]
+    for e in range(w.E):
+        for off in range(0, ss[e + 1] - ss[e], tile_rows):
+            tiles.append((e, ss[e] + off, min(tile_rows, ss[e + 1] - ss[e] - off), 0))
+    assert ws["num_valid"][2] == len(tiles)
+    np.testing.assert_array_equal(ws["tiles"][: len(tiles)], np.array(tiles, np.int32).reshape(-1, 4))
+    return n
+
+
+def check_a1(ws, ref_fw, routing, w, tokens=None):
+    R = w.R
+    sel = set(range(w.T)) if tokens is None else set(int(t) for t in tokens)
+    for p in range(int(routing["num_valid"][0])):
+        r = int(routing["sorted_ids"][p])
+        if r >= R or (r // w.K) not in sel:
+            continue
+        t = r // w.K
+        np.testing.assert_array_equal(ws["a1q"][p], ref_fw["a1q"][t], err_msg=f"a1q slot {p}")
+        np.testing.assert_array_equal(ws["a1s"][p, : w.D // 32], ref_fw["a1s"][t],
+                                      err_msg=f"a1s slot {p}")
+
+
+def check_a2(ws, ref_fw, routing, w, tokens=None):
+    R = w.R
+    sel = set(range(w.T)) if tokens is None else set(int(t) for t in tokens)
+    total = 0
+    diff = 0
+    for p in range(int(routing["num_valid"][0])):
+        r = int(routing["sorted_ids"][p])
+        if r >= R or (r // w.K) not in sel:
+            continue
+        gq, gs = ws["a2q"][p], ws["a2s"][p, : w.I // 32]
+        oq, os_ = ref_fw["a2q"][r], ref_fw["a2s"][r]
+        total += w.I
+        if np.array_equal(gq, oq) and np.array_equal(gs, os_):
+            continue
+        dg = _deq(gq[None], gs[None], w.I)[0]
+        do = _deq(oq[None], os_[None], w.I)[0]
+        bad = (_unpack(gq[None])[0] != _unpack(oq[None])[0]) | np.repeat(gs != os_, 32)
+        diff += int(bad.sum())
+        # one e2m1 step: adjacent grid values differ by at most x2 (or 0 <-> 0.5 * 2^X)
+        unit = np.repeat(np.ldexp(1.0, np.maximum(gs, os_).astype(np.int64) - 127), 32)
+        ok = np.abs(dg - do) <= 0.5 * np.maximum(np.abs(dg), np.abs(do)) + 0.5 * unit
+        assert ok.all(), f"a2 slot {p} route {r}: more than one step"
+        assert (np.abs(gs.astype(int) - os_.astype(int)) <= 1).all()
+    assert total > 0
+    assert diff <= CODE_FRAC * total, f"{diff} of {total} a2 codes differ"
+    return diff, total
+
+
+def check_out(out_gpu, ref_fw, tokens=None):
+    g = out_gpu.float().cpu().numpy()
+    o = oracle.bf16_bits_to_f32(ref_fw["out_bf16"])
+    rows = range(g.shape[0]) if tokens is None else tokens
+    worst = 0.0
+    for t in rows:
+        rms = float(np.sqrt(np.mean(o[t].astype(np.float64) ** 2)))
+        err = float(np.max(np.abs(g[t].astype(np.float64) - o[t])))
+        if rms == 0.0:
+            assert err == 0.0, f"row {t}: oracle row is zero, gpu max |x| = {err}"
+            continue
+        worst = max(worst, err / rms)
+        assert err <= ROW_TOL * rms, f"row {t}: max err {err} > {ROW_TOL} * rms {rms}"
+    return worst
+
+
+def full_check(moe, w, inp, tokens=None):
+    m, t, out = run_gpu(moe, inp, w)
+    npi = workloads.to_numpy(inp)
+    routing = oracle.route(npi["topk_ids"], npi["topk_weights"], w.E, 16, cap=m.plan.cap)
+    ref = oracle.forward(**npi, tokens=tokens, threads=_threads(), want_h=False)
+    ws = ws_arrays(m, w)
+    check_routing(ws, routing, w, m.plan.tile_rows)
+    check_a1(ws, ref, routing, w, tokens)
+    check_a2(ws, ref, routing, w, tokens)
+    worst = check_out(out, ref, tokens)
+    return m, t, out, worst
+
+
+# ------------------------------------------------------------------ workloads
+
+def test_tiny_workload(moe):
+    w = workloads.WORKLOADS[workloads.TINY]
+    full_check(moe, w, workloads.make_inputs(w))
+
+
+def test_decode_t16_full(moe):
+    w = workloads.WORKLOADS[workloads.DECODE_T16]
+    full_check(moe, w, workloads.make_inputs(w))
+
+
+def test_decode_t128_full(moe):
+    w = workloads.WORKLOADS["decode_T128_D7168_I256_E257_K9"]
+    full_check(moe, w, workloads.make_inputs(w))
+
+
+def test_dense_shard_t512_sampled(moe):
+    w = workloads.WORKLOADS["dense_T512_D7168_I2048_E33_K9"]
+    toks = [0, 1, 77, 255, 256, 400, 510, 511]
+    full_check(moe, w, workloads.make_inputs(w), tokens=toks)
+
+
+def test_prefill_zipf_t4096_sampled(moe):
+    w = workloads.WORKLOADS["prefill_zipf_T4096_D7168_I256_E257_K9"]
+    toks = [0, 1, 2, 1000, 2047, 2048, 3333, 4094, 4095]
+    full_check(moe, w, workloads.make_inputs(w), tokens=toks)
+
+
+# ------------------------------------------------------------------ edge cases
+
+def _small(T=16, D=256, I=128, E=9, K=3, seed=0):
+    w = workloads.custom(T, D, I, E, K)
+    return w, workloads.make_inputs(w, seed=seed)
+
+
+def test_single_token(moe):
+    w, inp = _small(T=1)
+    full_check(moe, w, inp)
+
+
+def test_all_routes_on_one_expert(moe):
+    w, inp = _small(T=40, E=9, K=1)
+    inp["topk_ids"][:] = 4
+    full_check(moe, w, inp)
+
+
+def test_exactly_full_blocks_and_duplicates(moe):
+    # expert 2 receives exactly 32 routes (two full blocks); token 0 repeats an expert
+    w, inp = _small(T=32, E=5, K=2)
+    ids = inp["topk_ids"]
+    ids[:, 0] = 2
+    ids[:, 1] = torch.arange(32, dtype=torch.int32) % 4 + 1
+    ids[0, 1] = 2
+    ids[1, 1] = 2
+    ids[1, 0] = 3
+    full_check(moe, w, inp)
+
+
+def test_invalid_ids_and_empty_rows(moe):
+    w, inp = _small(T=20, E=9, K=3)
+    ids = inp["topk_ids"]
+    ids[0, :] = -1            # a token with no valid route -> exact zero row
+    ids[3, 1] = 9             # == E: out of range
+    ids[5, 0] = 1000
+    ids[7, 2] = -7
+    full_check(moe, w, inp)
+
+
+def test_dense_shape_small(moe):
+    # K = 512-multiple contraction with several pipeline stages, 128-row tiles
+    w, inp = _small(T=64, D=1024, I=512, E=3, K=2)
+    full_check(moe, w, inp)
+
+
+def test_large_tiles_mid_shape(moe):
+    w, inp = _small(T=256, D=512, I=256, E=5, K=3)
+    full_check(moe, w, inp)
+
+
+def test_empty_batch(moe):
+    m = moe.MoeMXFP4(0, 256, 128, 9, 3)
+    e = torch.empty(0, device="cuda")
+    code = moe.forward_ptr(e.data_ptr(), 16, 16, 16, 16, 16, 16, 16, 0, 256, 128, 9, 3, 0)
+    assert code == 0
+    del m
+
+
+def test_closed_form_bit_exact(moe):
+    """All-ones case from tests/golden/closed_form.txt: exact in every step."""
+    D, I, E, K, T = 256, 128, 1, 1, 1
+    hidden = torch.ones(T, D, dtype=torch.bfloat16)
+    inp = {
+        "hidden": hidden,
+        "w13": torch.full((E, 2 * I, D // 2), 0x22, dtype=torch.uint8),
+        "w13_scale": torch.full((E, 2 * I, D // 32), 127, dtype=torch.uint8),
+        "w2": torch.full((E, D, I // 2), 0x22, dtype=torch.uint8),
+        "w2_scale": torch.full((E, D, I // 32), 127, dtype=torch.uint8),
+        "topk_ids": torch.zeros(T, K, dtype=torch.int32),
+        "topk_weights": torch.full((T, K), 0.375, dtype=torch.float32),
+    }
+    w = workloads.custom(T, D, I, E, K)
+    _, _, out = run_gpu(moe, inp, w)
+    assert (out.float().cpu() == 3145728.0).all()
+
+
+def test_deterministic_repeat(moe):
+    w = workloads.WORKLOADS[workloads.TINY]
+    inp = workloads.make_inputs(w)
+    m, t, out = run_gpu(moe, inp, w)
+    ref = out.clone()
+    for _ in range(5):
+        o2 = m.forward(t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"],
+                       t["topk_ids"], t["topk_weights"])
+        torch.cuda.synchronize()
+        assert torch.equal(o2.view(torch.int16), ref.view(torch.int16))
