@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MXFP4 MoE forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one moe_mxfp4_forward call (route -> quant -> stage-1 GEMM ->
+stage-2 GEMM -> top-k sum) over one batch of synthetic inputs already resident
+in HBM.  Between steps the L2 is flushed (a 256 MiB write), so every step reads
+the expert weights from HBM.  Step time is the device time between CUDA events
+the library records on its stream before its first and after its last kernel.
+
+Multi-GPU (torchrun, one process per GPU): replicas only -- each rank runs an
+independent forward on its own batch (the op has no exchange step); the value
+is the tokens of all ranks divided by the slowest rank's time (weak scaling).
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on a
+bounded sample of the same workload; under torchrun only rank 0 runs it.
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused MoE µs/call and tokens/s; achieved HBM TB/s or MXFP4 TFLOPS vs roofline"
+DEFAULT_WORKLOAD = "decode_T16_D7168_I256_E257_K9"
+# Published number for this workload on the pages (MI355X, aiter): 152.7 us/call
+# for (T=16, E=257, d_inter=256, topk=9); context only.
+PUBLISHED_US = {"decode_T16_D7168_I256_E257_K9": 152.7,
+                "decode_T128_D7168_I256_E257_K9": 239.0,
+                "dense_T512_D7168_I2048_E33_K9": 380.4}
+HBM_FALLBACK_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_stage1_decode_T16_D7168_I256_E257_K9.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_mxfp4_gb300", "csrc", f)
+                  for f in ("gemm.cu", "ptx.cuh", "mx.cuh", "moe_internal.h", "api.cu")]
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units processed by all ranks / slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per stage-1 launch from the committed ncu summary, or None when
+    the summary is missing or the kernel sources changed since it was taken."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def alg_bytes(w, ids):
+    """Algorithmic bytes of one forward call and of its stage-1 GEMM."""
+    import workloads
+
+    E_t = workloads.touched_experts(ids, w.E)
+    per_expert_w13 = 2 * w.I * w.D * 17 // 32      # w13 + its e8m0 scales
+    per_expert_w2 = w.D * w.I * 17 // 32           # w2 + scales
+    act = w.T * w.D * 2                            # bf16 hidden in
+    out = w.T * w.D * 2                            # bf16 out
+    route = w.T * w.K * 8                          # ids + weights
+    total = E_t * (per_expert_w13 + per_expert_w2) + act + out + route
+    n_valid = int(((ids >= 0) & (ids < w.E)).sum())
+    stage1 = E_t * per_expert_w13 + w.T * w.D * 17 // 32 + n_valid * w.I * 17 // 32
+    return total, stage1, E_t
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, w):
+    """Time the CPU oracle (as it stands) on a bounded sample of the workload."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    inp = workloads.to_numpy(workloads.make_inputs(w))
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ntok = min(w.T, max(1, args.ref_tokens))
+    toks = np.arange(ntok, dtype=np.int32)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle.forward(**inp, tokens=toks, threads=threads, want_h=False)
+    times = []
+    for _ in range(max(1, args.steps)):
+        t0 = time.perf_counter()
+        oracle.forward(**inp, tokens=toks, threads=threads, want_h=False)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = ntok * len(times) / tot
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": len(times),
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_inter": w.I, "E": w.E,
+                   "topk": w.K, "sample_tokens": ntok},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{ntok} of {w.T} tokens per step, full routing"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline(w, budget_s: float):
+    """Oracle on the host cores over whole batches of the workload, ~budget_s seconds."""
+    import numpy as np
+
+    import oracle
+    import workloads
+
+    inp = workloads.to_numpy(workloads.make_inputs(w))
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ntok = w.T
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.forward(**inp, threads=threads, want_h=False)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": ntok * reps / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} full batches of {ntok} tokens ({w.name}), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w, world, rank, local):
+    import numpy as np
+    import torch
+
+    import mixture_experts_mxfp4_gb300 as moe
+    import workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    moe.load_library()
+    inp = workloads.make_inputs(w, seed=args.seed + rank)
+    t = {k: v.to(dev) for k, v in inp.items()}
+    m = moe.MoeMXFP4(w.T, w.D, w.I, w.E, w.K, device=dev)
+    out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fargs = (t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"], t["topk_ids"],
+             t["topk_weights"])
+
+    moe.set_kernel_timing(True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        m.forward(*fargs, out=out)
+    torch.cuda.synchronize(dev)
+    if m.device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+
+    names = moe.KERNEL_NAMES
+    per_kernel = {n: 0.0 for n in names}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)  # let the sampler start before the timed region
+    total_ms = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        m.forward(*fargs, out=out)
+        kt = moe.kernel_times()
+        for n in names:
+            per_kernel[n] += kt[n]
+        total_ms += sum(kt.values())
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = clocks.stop()
+    if m.device_status() != 0:
+        raise RuntimeError("device status after timed region")
+    moe.set_kernel_timing(False)
+
+    max_s = max_over_ranks(total_ms / 1e3, world, dev if world > 1 else None)
+    value = aggregate_value(w.T * args.steps, world, max_s)
+    us_call = 1e3 * total_ms / args.steps
+
+    # ---- end to end through the public API: pinned host in, host out
+    h_hidden = inp["hidden"].pin_memory()
+    h_ids = inp["topk_ids"].pin_memory()
+    h_w = inp["topk_weights"].pin_memory()
+    h_out = torch.empty(w.T, w.D, dtype=torch.bfloat16).pin_memory()
+    d_hidden = torch.empty_like(t["hidden"])
+    d_ids = torch.empty_like(t["topk_ids"])
+    d_w = torch.empty_like(t["topk_weights"])
+    e2e_steps = max(1, min(args.steps, 200))
+    for _ in range(3):
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        m.forward(d_hidden, *fargs[1:5], d_ids, d_w, out=out)
+        h_out.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_ids.copy_(h_ids, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        m.forward(d_hidden, *fargs[1:5], d_ids, d_w, out=out)
+        h_out.copy_(out, non_blocking=True)
+        s1.record(stream)
+        s1.synchronize()
+        e2e_ms += s0.elapsed_time(s1)
+    e2e_max = max_over_ranks(e2e_ms / 1e3, world, dev if world > 1 else None)
+    e2e_value = aggregate_value(w.T * e2e_steps, world, e2e_max)
+    h2d = h_hidden.numel() * 2 + h_ids.numel() * 4 + h_w.numel() * 4
+    d2h = h_out.numel() * 2
+
+    # ---- roofline of the dominant kernel (stage-1 GEMM), measured live above
+    ids_np = inp["topk_ids"].numpy()
+    b_total, b_stage1, e_touched = alg_bytes(w, ids_np)
+    peak, peak_kind = measured_peaks()
+    dom = max(per_kernel, key=per_kernel.get)
+    s1_ms = per_kernel["gemm_stage1"] / args.steps
+    achieved = b_stage1 / (s1_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "gemm_stage1", "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "traffic": profiled_traffic(),
+                "alg_bytes_per_launch": b_stage1, "peak_kind": peak_kind}
+    fwd_gbs = b_total / (us_call * 1e-6) / 1e9
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 (e2m1 x e2m1, fp32 accumulate)",
+        "data": "synthetic (seeded; DeepSeek-R1-shaped, random weights)",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_inter": w.I, "E": w.E,
+                   "topk": w.K, "touched_experts": e_touched,
+                   "l2": "flushed before every step (256 MiB write, untimed)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": us_call,
+        "per_kernel_us": {n: 1e3 * v / args.steps for n, v in per_kernel.items()},
+        "dominant_kernel": dom,
+        "roofline": roofline,
+        "roofline_forward": {"bound": "hbm", "alg_bytes": b_total, "achieved": fwd_gbs,
+                             "peak": peak, "unit": "GB/s", "frac": fwd_gbs / peak},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": moe.load_library().moe_mxfp4_num_kernels() * args.steps,
+        "clocks": clk,
+    }
+    if w.name in PUBLISHED_US:
+        res["vs_baseline"] = value / (w.T / (PUBLISHED_US[w.name] * 1e-6))
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res = run_gpu(args, w, world, rank, local)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w, args.cpu_baseline_s)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

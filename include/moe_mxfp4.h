@@ -147,6 +147,24 @@ moe_status_t moe_mxfp4_get_plan(int T, int d_model, int d_inter, int E, int topk
 /* Version string of the library build. */
 const char* moe_mxfp4_version(void);
 
+/* ------------------------------------------------------------------ timing */
+
+/* Number of kernels one forward call launches (route, quant, stage-1 GEMM,
+ * stage-2 GEMM, top-k sum). */
+int moe_mxfp4_num_kernels(void);
+
+/*
+ * Optional instrumentation for benchmarks.  With enable != 0 the forward call
+ * records a CUDA event on its stream before each kernel and after the last one
+ * (events created once per device, on first enable; no device memory is
+ * allocated).  moe_mxfp4_kernel_times waits for the last recorded event and
+ * writes the duration of each kernel of the most recent call on the current
+ * device, in milliseconds, to ms[0 .. min(n, num_kernels) - 1]; it returns the
+ * number written, or -1 when timing is off or no call was recorded.
+ */
+moe_status_t moe_mxfp4_set_kernel_timing(int enable);
+int moe_mxfp4_kernel_times(float* ms, int n);
+
 #ifdef __cplusplus
 }
 #endif

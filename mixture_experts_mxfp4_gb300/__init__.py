@@ -40,7 +40,12 @@ EXPORTS = [
     "moe_mxfp4_last_device_status",
     "moe_mxfp4_get_plan",
     "moe_mxfp4_version",
+    "moe_mxfp4_num_kernels",
+    "moe_mxfp4_set_kernel_timing",
+    "moe_mxfp4_kernel_times",
 ]
+
+KERNEL_NAMES = ["route", "quant", "gemm_stage1", "gemm_stage2", "topk_sum"]
 
 
 class MoeError(RuntimeError):
@@ -96,6 +101,12 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_get_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
     lib.moe_mxfp4_version.restype = ctypes.c_char_p
     lib.moe_mxfp4_version.argtypes = []
+    lib.moe_mxfp4_num_kernels.restype = i
+    lib.moe_mxfp4_num_kernels.argtypes = []
+    lib.moe_mxfp4_set_kernel_timing.restype = i
+    lib.moe_mxfp4_set_kernel_timing.argtypes = [i]
+    lib.moe_mxfp4_kernel_times.restype = i
+    lib.moe_mxfp4_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), i]
     _lib = lib
     return lib
 
@@ -133,6 +144,22 @@ def forward_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, ou
 
 def last_device_status(stream: int = 0) -> int:
     return int(load_library().moe_mxfp4_last_device_status(ctypes.c_void_p(stream)))
+
+
+def set_kernel_timing(enable: bool):
+    _check(load_library().moe_mxfp4_set_kernel_timing(1 if enable else 0),
+           "moe_mxfp4_set_kernel_timing")
+
+
+def kernel_times():
+    """Per-kernel durations (ms) of the last forward call on this device, by name."""
+    lib = load_library()
+    n = lib.moe_mxfp4_num_kernels()
+    buf = (ctypes.c_float * n)()
+    got = lib.moe_mxfp4_kernel_times(buf, n)
+    if got < 0:
+        raise MoeError(5, "moe_mxfp4_kernel_times")
+    return {KERNEL_NAMES[i]: float(buf[i]) for i in range(got)}
 
 
 def version() -> str:

@@ -23,9 +23,19 @@ struct WorkspaceReg {
     size_t bytes = 0;
 };
 
+constexpr int kNumKernels = 5;
+
+struct Timing {
+    bool enabled = false;
+    bool created = false;
+    bool recorded = false;
+    cudaEvent_t ev[kNumKernels + 1];
+};
+
 std::mutex g_mu;
 WorkspaceReg g_ws[kMaxDevices];
 int g_num_sms[kMaxDevices];
+Timing g_timing[kMaxDevices];
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -60,8 +70,18 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     pl->cap = (int)cap;
     pl->a1s_stride = (int)round_up((size_t)(D / 32), 16);
     pl->a2s_stride = (int)round_up((size_t)(I / 32), 16);
-    pl->stage1_splits = 1;
     pl->max_tiles = (int)(cap / kBlockM);
+    // Stage-1 K splits: decode batches have few (expert, feature-tile) units per
+    // SM, so the contraction over d_model is split and summed by the last CTA.
+    {
+        const int kst = D >= 512 ? D / 512 : 1;
+        const double units = (double)(used < E ? used : E) * (I / 64);
+        int want = (int)(4.0 * 304.0 / (units > 1 ? units : 1));
+        int best = 1;
+        for (int s = 1; s <= kst && s <= 8; ++s)
+            if (kst % s == 0 && s <= (want > 1 ? want : 1)) best = s;
+        pl->stage1_splits = pl->tile_rows <= 64 ? best : 1;
+    }
     const size_t n_counters = (size_t)pl->max_tiles * (size_t)(I / 64);
     size_t b[MOE_WS_NUM_REGIONS];
     b[MOE_WS_STATUS] = 16 * sizeof(uint32_t);
@@ -78,7 +98,9 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     b[MOE_WS_A2Q] = (size_t)cap * (I / 2);
     b[MOE_WS_A2S] = (size_t)cap * pl->a2s_stride;
     b[MOE_WS_P] = (size_t)R * D * 4;
-    b[MOE_WS_PARTIAL] = 0;
+    b[MOE_WS_PARTIAL] = pl->stage1_splits > 1
+                            ? n_counters * (size_t)pl->stage1_splits * pl->tile_rows * 128 * 4
+                            : 0;
     size_t off = 0;
     for (int i = 0; i < MOE_WS_NUM_REGIONS; ++i) {
         pl->offset[i] = off;
@@ -132,33 +154,81 @@ EncodeTiledFn get_encode() {
     return fn;
 }
 
+// Tiled u8 tensor map of rank r: dims innermost first, strides (bytes) of dims
+// 1..r-1, box extents.  The dimensions may overlap in memory (a K-box dimension
+// with a stride smaller than the row stride), which lets one box gather the
+// K-tiles of a stage or the gate and up halves of w13.
+bool make_map_nd(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swz) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t d[5];
+    cuuint64_t st[4];
+    cuuint32_t b[5];
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), d,
+                     st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 2-D u8 tensor [rows][inner] with row stride `stride` bytes, box {bx, by}.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t stride,
               uint32_t bx, uint32_t by, CUtensorMapSwizzle swz) {
-    EncodeTiledFn enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {stride};
-    cuuint32_t box[2] = {bx, by};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    const uint64_t dims[2] = {inner, rows};
+    const uint64_t strides[1] = {stride};
+    const uint32_t box[2] = {bx, by};
+    return make_map_nd(m, base, 2, dims, strides, box, swz);
+}
+
+// Packed-e2m1 operand [rows][Kc/2 bytes] seen as {kb bytes, rows, Kc/2/kb K-boxes}
+// (optionally with a second row dimension of `halves` at `half_stride` bytes):
+// one box brings box_rows rows x nkt K-boxes, laid out [kbox][half][row][kb].
+bool make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, int Kc, int kb, int nkt,
+                      int box_rows, int halves, uint64_t half_stride) {
+    const uint64_t row_bytes = (uint64_t)Kc / 2;
+    const CUtensorMapSwizzle swz = kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (halves > 1) {
+        const uint64_t dims[4] = {(uint64_t)kb, rows, (uint64_t)halves, row_bytes / kb};
+        const uint64_t strides[3] = {row_bytes, half_stride, (uint64_t)kb};
+        const uint32_t box[4] = {(uint32_t)kb, (uint32_t)box_rows, (uint32_t)halves, (uint32_t)nkt};
+        return make_map_nd(m, base, 4, dims, strides, box, swz);
+    }
+    const uint64_t dims[3] = {(uint64_t)kb, rows, row_bytes / kb};
+    const uint64_t strides[2] = {row_bytes, (uint64_t)kb};
+    const uint32_t box[3] = {(uint32_t)kb, (uint32_t)box_rows, (uint32_t)nkt};
+    return make_map_nd(m, base, 3, dims, strides, box, swz);
 }
 
 // Weight-scale map: [rows][S] e8m0 bytes; S >= 16 read 16 bytes per stage, S < 16
 // read through a [rows*S/16][16] view so that one box holds box_rows whole rows.
-bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int box_rows) {
-    if (S >= 16)
-        return make_map(m, base, (uint64_t)S, rows, (uint64_t)S, 16, (uint32_t)box_rows,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-    return make_map(m, base, 16, rows * S / 16, 16, 16, (uint32_t)(box_rows * S / 16),
-                    CU_TENSOR_MAP_SWIZZLE_NONE);
+// With halves = 2 a third dimension adds the rows `half_rows` further (w13 up rows).
+bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int box_rows,
+                    int halves, uint64_t half_rows) {
+    const bool small = S < 16;
+    const uint64_t inner = small ? 16 : (uint64_t)S;
+    const uint64_t vrows = small ? rows * S / 16 : rows;
+    const uint64_t stride = small ? 16 : (uint64_t)S;
+    const uint32_t brows = small ? (uint32_t)(box_rows * S / 16) : (uint32_t)box_rows;
+    if (halves > 1) {
+        const uint64_t dims[3] = {inner, vrows, (uint64_t)halves};
+        const uint64_t strides[2] = {stride, half_rows * (uint64_t)S};
+        const uint32_t box[3] = {16, brows, (uint32_t)halves};
+        return make_map_nd(m, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    return make_map(m, base, inner, vrows, stride, 16, brows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Pipeline geometry of one GEMM stage for contraction length Kc.
+// Pipeline geometry of one GEMM stage for contraction length Kc.  Narrow route
+// tiles (decode) run two CTAs per SM: a single stream of scale-factor copies and
+// MMAs leaves the tensor pipe idle between them, and a second CTA fills it.
 void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1) {
+    g.ctas_per_sm = tile_rows <= 64 ? 2 : 1;
     g.kstage_elems = Kc >= 512 ? 512 : Kc;
     g.kstages = Kc / g.kstage_elems;
     g.kb = g.kstage_elems >= 256 ? 128 : 64;
@@ -175,19 +245,30 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1) {
     g.off_sa = g.off_b + b_bytes;
     g.off_sb = g.off_sa + 2048;
     g.stage_bytes = (uint32_t)round_up(g.off_sb + 2048, 1024);
-    const uint32_t fixed = 1024 /*align slack*/ + 256 /*barriers*/ + (stage1 ? 4096u : 0u);
-    const uint32_t budget = 227u * 1024u - fixed;
+    const uint32_t fixed = 1024 /*align slack*/ + 256 /*barriers*/ + (stage1 ? 4352u : 0u);
+    // 227 KB of shared memory per SM, split between the CTAs of an SM
+    const uint32_t budget = (g.ctas_per_sm == 2 ? 113u * 1024u : 227u * 1024u) - fixed;
     int ns = (int)(budget / g.stage_bytes);
     if (ns > kMaxStages) ns = kMaxStages;
+    // One accumulator per buffer: narrow MMAs into the same accumulator measured
+    // no slower than into separate ones.
+    const int nacc = 1;
+    const uint32_t tmem_limit = 512u / (uint32_t)g.ctas_per_sm;
+    // TMEM: 2 accumulator buffers of nacc * N columns + per-stage scale factors.
+    while (ns > 1 && 2u * nacc * tile_rows + (uint32_t)ns * 8u * g.natoms > tmem_limit) --ns;
+    g.nacc = nacc;
     g.num_stages = ns;
     g.off_bar = (uint32_t)ns * g.stage_bytes;
     g.off_xchg = g.off_bar + 256;
-    g.smem_bytes = g.off_xchg + (stage1 ? 4096u : 0u) + 1024u;
-    const uint32_t cols = 2u * tile_rows + (uint32_t)ns * 8u * g.natoms;
+    g.smem_bytes = g.off_xchg + (stage1 ? 4352u : 0u) + 1024u;
+    // with one CTA per SM, ask for more than half the SM's shared memory so that
+    // two CTAs never share an SM (and its TMEM)
+    if (g.ctas_per_sm == 1 && g.smem_bytes < 118u * 1024u) g.smem_bytes = 118u * 1024u;
+    const uint32_t cols = 2u * nacc * tile_rows + (uint32_t)ns * 8u * g.natoms;
     uint32_t alloc = 32;
     while (alloc < cols) alloc <<= 1;
     g.tmem_cols = alloc;
-    g.sf_col0 = 2u * tile_rows;
+    g.sf_col0 = 2u * nacc * tile_rows;
 }
 
 int num_sms(int dev) {
@@ -311,32 +392,80 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
 
     // ---------------------------------------------------------- TMA maps
     CUtensorMap mA1, mSA1, mB1, mSB1, mA2, mSA2, mB2, mSB2;
-    const CUtensorMapSwizzle sw1 = g1.kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    const CUtensorMapSwizzle sw2 = g2.kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const int tr = pl.tile_rows;
     bool ok = true;
-    ok = ok && make_map(&mA1, w13, D / 2, (uint64_t)E * 2 * I, D / 2, g1.kb, 64, sw1);
-    ok = ok && make_scale_map(&mSA1, w13_scale, (uint64_t)E * 2 * I, D / 32, 64);
-    ok = ok && make_map(&mB1, ws.a1q, D / 2, pl.cap, D / 2, g1.kb, 16, sw1);
-    ok = ok && make_map(&mSB1, ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, 16,
+    // stage 1: A = 64 gate rows + the 64 up rows I rows further, both K-boxes of a stage
+    ok = ok && make_operand_map(&mA1, w13, (uint64_t)E * 2 * I, D, g1.kb, g1.nkt, 64, 2,
+                                (uint64_t)I * (D / 2));
+    ok = ok && make_scale_map(&mSA1, w13_scale, (uint64_t)E * 2 * I, D / 32, 64, 2, (uint64_t)I);
+    ok = ok && make_operand_map(&mB1, ws.a1q, pl.cap, D, g1.kb, g1.nkt, tr, 1, 0);
+    ok = ok && make_map(&mSB1, ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok = ok && make_map(&mA2, w2, I / 2, (uint64_t)E * D, I / 2, g2.kb, 128, sw2);
-    ok = ok && make_scale_map(&mSA2, w2_scale, (uint64_t)E * D, I / 32, 128);
-    ok = ok && make_map(&mB2, ws.a2q, I / 2, pl.cap, I / 2, g2.kb, 16, sw2);
-    ok = ok && make_map(&mSB2, ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, 16,
+    // stage 2: A = 128 rows of w2
+    ok = ok && make_operand_map(&mA2, w2, (uint64_t)E * D, I, g2.kb, g2.nkt, 128, 1, 0);
+    ok = ok && make_scale_map(&mSA2, w2_scale, (uint64_t)E * D, I / 32, 128, 1, 0);
+    ok = ok && make_operand_map(&mB2, ws.a2q, pl.cap, I, g2.kb, g2.nkt, tr, 1, 0);
+    ok = ok && make_map(&mSB2, ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return MOE_ERR_CUDA;
 
     // ---------------------------------------------------------- launches
     const int sms = num_sms(dev);
     const int n_counters = pl.max_tiles * (I / 64);
+    Timing& tm = g_timing[dev];
+    const bool timed = tm.enabled && tm.created;
+    auto mark = [&](int i) {
+        if (timed) cudaEventRecord(tm.ev[i], stream);
+    };
+    mark(0);
     if (launch_route(topk_ids, topk_weights, T, K, E, pl.tile_rows, pl.cap, n_counters, ws,
                      stream) != cudaSuccess)
         return MOE_ERR_CUDA;
+    mark(1);
     if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_gemm(1, mA1, mSA1, mB1, mSB1, g1, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_gemm(2, mA2, mSA2, mB2, mSB2, g2, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(2);
+    if (launch_gemm(1, mA1, mSA1, mB1, mSB1, g1, sms * g1.ctas_per_sm, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark(3);
+    if (launch_gemm(2, mA2, mSA2, mB2, mSB2, g2, sms * g2.ctas_per_sm, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark(4);
     if (launch_reduce(topk_ids, T, K, E, D, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(5);
+    if (timed) tm.recorded = true;
     return MOE_OK;
+}
+
+int moe_mxfp4_num_kernels(void) { return kNumKernels; }
+
+moe_status_t moe_mxfp4_set_kernel_timing(int enable) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Timing& tm = g_timing[dev];
+    if (enable && !tm.created) {
+        for (int i = 0; i <= kNumKernels; ++i)
+            if (cudaEventCreate(&tm.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
+        tm.created = true;
+    }
+    tm.enabled = enable != 0;
+    tm.recorded = false;
+    return MOE_OK;
+}
+
+int moe_mxfp4_kernel_times(float* ms, int n) {
+    int dev = 0;
+    if (!ms || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    Timing& tm = g_timing[dev];
+    if (!tm.enabled || !tm.recorded) return -1;
+    if (cudaEventSynchronize(tm.ev[kNumKernels]) != cudaSuccess) return -1;
+    const int m = n < kNumKernels ? n : kNumKernels;
+    for (int i = 0; i < m; ++i) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, tm.ev[i], tm.ev[i + 1]) != cudaSuccess) return -1;
+        ms[i] = t;
+    }
+    return m;
 }
 
 }  // extern "C"

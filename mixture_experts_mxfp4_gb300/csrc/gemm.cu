@@ -19,11 +19,16 @@
 // the epilogue writes w[route] * y into P[route, :] for the per-token sum.
 //
 // Pipeline (one CTA per SM, persistent over work items):
-//   warp 0  TMA producer: weight tile, route tile, raw scale tiles -> smem ring
-//   warp 1  MMA warp: rearranges the scale tiles into the tcgen05 scale-factor
-//           layout, copies them to TMEM (tcgen05.cp) and issues tcgen05.mma
+//   warp 0  TMA producer: one box each for the weight tile, the route tile and
+//           the two raw scale tiles per stage -> smem ring
+//   warp 1  MMA warp: copies the stage's scale factors to TMEM (tcgen05.cp) and
+//           issues tcgen05.mma; consecutive K-steps go to `nacc` independent
+//           accumulators so that narrow (small-N) MMAs do not wait on each other
 //   warp 2  allocates / frees TMEM
-//   warps 4-7  epilogue: tcgen05.ld from the double-buffered accumulator
+//   warp 3  rearranges each stage's raw scale tiles into the tcgen05
+//           scale-factor layout one stage ahead of the MMA warp
+//   warps 4-7  epilogue: tcgen05.ld of the double-buffered accumulators, summed
+//           over the nacc partial accumulators in a fixed order
 // All waits are bounded (ptx.cuh).
 #include <cuda_bf16.h>
 
@@ -78,7 +83,7 @@ __device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, ui
 }
 
 template <int STAGE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 2)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmSA,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmSB,
                     const GemmParams p) {
@@ -91,12 +96,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* empty = full + kMaxStages;
-    uint64_t* tfull = empty + kMaxStages;
+    uint64_t* sfready = empty + kMaxStages;
+    uint64_t* tfull = sfready + kMaxStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float* xchg = reinterpret_cast<float*>(smem + p.off_xchg);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + p.off_xchg + 4096);
     uint32_t* status = p.ws.status;
 
     const int num_tiles = p.ws.num_valid[2];
@@ -107,6 +114,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sfready[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -150,47 +158,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                    const uint32_t tx = (uint32_t)(128 + x.nrows) * kbytes_stage +
-                                        128u * p.sr_a + (uint32_t)x.nrows * 16u;
+                    const uint32_t tx = (uint32_t)(128 + p.tile_rows) * kbytes_stage +
+                                        128u * p.sr_a + (uint32_t)p.tile_rows * 16u;
                     mbar_arrive_expect_tx(&full[s], tx);
-                    for (int kt = 0; kt < p.nkt; ++kt) {
-                        const int kx = ks * kbytes_stage + kt * p.kb;
-                        uint8_t* a_dst = st + kt * 128 * p.kb;
-                        if (STAGE == 1) {
-                            const int rg = x.e * 2 * p.I + x.f * 64;
-                            tma_load_2d_hint(a_dst, &tmA, kx, rg, &full[s], pol_w);
-                            tma_load_2d_hint(a_dst + 64 * p.kb, &tmA, kx, rg + p.I, &full[s], pol_w);
-                        } else {
-                            tma_load_2d_hint(a_dst, &tmA, kx, x.e * p.D + x.f * 128, &full[s], pol_w);
-                        }
-                        uint8_t* b_dst = st + p.off_b + kt * p.tile_rows * p.kb;
-                        for (int b = 0; b < x.nrows / 16; ++b)
-                            tma_load_2d(b_dst + b * 16 * p.kb, &tmB, kx, x.row0 + 16 * b, &full[s]);
-                    }
-                    // raw weight scales: 128 rows of sr_a bytes
-                    uint8_t* sa = st + p.off_sa;
+                    const int kt0 = ks * p.nkt;  // first K box of the stage
                     if (STAGE == 1) {
+                        // 64 gate rows and the 64 matching up rows (I rows further) in one box
                         const int rg = x.e * 2 * p.I + x.f * 64;
-                        if (p.a_scale_small) {
-                            const int q = 16 / p.sr_a;  // rows per 16-byte view row
-                            tma_load_2d(sa, &tmSA, 0, rg / q, &full[s]);
-                            tma_load_2d(sa + 64 * p.sr_a, &tmSA, 0, (rg + p.I) / q, &full[s]);
-                        } else {
-                            tma_load_2d(sa, &tmSA, ks * 16, rg, &full[s]);
-                            tma_load_2d(sa + 64 * 16, &tmSA, ks * 16, rg + p.I, &full[s]);
-                        }
+                        tma_load_4d_hint(st, &tmA, 0, rg, 0, kt0, &full[s], pol_w);
+                        if (p.a_scale_small)
+                            tma_load_3d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), 0, &full[s]);
+                        else
+                            tma_load_3d(st + p.off_sa, &tmSA, ks * 16, rg, 0, &full[s]);
                     } else {
                         const int rg = x.e * p.D + x.f * 128;
+                        tma_load_3d_hint(st, &tmA, 0, rg, kt0, &full[s], pol_w);
                         if (p.a_scale_small)
-                            tma_load_2d(sa, &tmSA, 0, rg / (16 / p.sr_a), &full[s]);
+                            tma_load_2d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), &full[s]);
                         else
-                            tma_load_2d(sa, &tmSA, ks * 16, rg, &full[s]);
+                            tma_load_2d(st + p.off_sa, &tmSA, ks * 16, rg, &full[s]);
                     }
-                    // raw activation scales: nrows rows of 16 bytes
-                    uint8_t* sb = st + p.off_sb;
-                    for (int b = 0; b < x.nrows / 16; ++b)
-                        tma_load_2d(sb + b * 256, &tmSB, p.b_scale_x ? ks * 16 : 0, x.row0 + 16 * b,
-                                    &full[s]);
+                    // route tile: tile_rows sorted slots from row0 (rows past the tile's
+                    // own are read but never used; past the end they are zero-filled)
+                    tma_load_3d(st + p.off_b, &tmB, 0, x.row0, kt0, &full[s]);
+                    tma_load_2d(st + p.off_sb, &tmSB, p.b_scale_x ? ks * 16 : 0, x.row0, &full[s]);
                     issued |= 1u << s;
                     last_ph = (last_ph & ~(1u << s)) | (ph << s);
                     if (++s == NS) {
@@ -225,27 +216,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t sbo = 8u * p.kb;
         const int ksteps = p.kstage_elems / 64;
         const int steps_per_box = p.kb / 32;
+        const uint32_t acc_cols = (uint32_t)(p.nacc * p.tile_rows);
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++local) {
             const Item x = decode_item(p, it);
             const int a = local & 1;
             const uint32_t aph = (uint32_t)(local >> 1) & 1u;
-            if (!mbar_wait(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
+            if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(a * p.tile_rows);
+            const uint32_t d_base = tmem_base + (uint32_t)a * acc_cols;
             const uint32_t N = (uint32_t)x.nrows;
             for (int ks = x.ks0; ks < x.ks1; ++ks) {
-                if (!mbar_wait(&full[s], ph, status, kErrTimeoutFull, abort_flag)) {
+                if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
+                    !mbar_wait_warp(&sfready[s], ph, status, kErrTimeoutFull, abort_flag)) {
                     ok = false;
                     break;
                 }
                 uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                sf_to_atoms(st + p.off_sa, p.sr_a, p.natoms, lane);
-                sf_to_atoms(st + p.off_sb, 16, p.natoms, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
                 if (lane == 0) {
                     tc_fence_after();
                     const uint32_t sfa = tmem_base + p.sf_col0 + (uint32_t)(s * 8 * p.natoms);
@@ -256,6 +245,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     const uint32_t a_base = smem_u32(st);
                     const uint32_t b_base = smem_u32(st + p.off_b);
+                    const int kg0 = (ks - x.ks0) * ksteps;  // K-step index within the item
                     for (int j = 0; j < ksteps; ++j) {
                         const int kt = j / steps_per_box;
                         const uint32_t koff = (uint32_t)(j % steps_per_box) * 32u;
@@ -264,8 +254,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             smem_desc(b_base + kt * p.tile_rows * p.kb + koff, 16, sbo, layout);
                         const uint32_t sid = (uint32_t)(j & 1) * 2u;
                         const uint32_t idesc = mxf4_idesc(128, N, sid, sid);
-                        mma_mxf4(d_tmem, ad, bd, idesc, sfa + 4u * (j >> 1), sfb + 4u * (j >> 1),
-                                 (ks > x.ks0 || j > 0) ? 1u : 0u);
+                        const int kg = kg0 + j;
+                        const uint32_t d = d_base + (uint32_t)((kg % p.nacc) * p.tile_rows);
+                        mma_mxf4(d, ad, bd, idesc, sfa + 4u * (j >> 1), sfb + 4u * (j >> 1),
+                                 kg >= p.nacc ? 1u : 0u);
                     }
                     tc_commit(&empty[s]);
                 }
@@ -291,6 +283,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
         __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ scale layout
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            const Item x = decode_item(p, it);
+            for (int ks = x.ks0; ks < x.ks1; ++ks) {
+                if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + (size_t)s * p.stage_bytes;
+                sf_to_atoms(st + p.off_sa, p.sr_a, p.natoms, lane);
+                sf_to_atoms(st + p.off_sb, 16, p.natoms, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfready[s]);
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const uint32_t q = warp & 3u;  // TMEM lane quadrant of this warp
@@ -300,60 +316,113 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const Item x = decode_item(p, it);
             const int a = local & 1;
             const uint32_t aph = (uint32_t)(local >> 1) & 1u;
-            if (!mbar_wait(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) break;
+            if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag, 256)) break;
             tc_fence_after();
-            const uint32_t tacc = tmem_base + ((q * 32u) << 16) + (uint32_t)(a * p.tile_rows);
+            const uint32_t tacc =
+                tmem_base + ((q * 32u) << 16) + (uint32_t)(a * p.nacc * p.tile_rows);
             const int nchunks = x.nrows / 16;
+            // v = sum over the nacc partial accumulators, in ascending order
+            auto load_acc = [&](int c, float (&v)[16]) {
+                tmem_ld16(tacc + 16u * c, v);
+                for (int i = 1; i < p.nacc; ++i) {
+                    float t[16];
+                    tmem_ld16(tacc + (uint32_t)(i * p.tile_rows) + 16u * c, t);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = v[k] + t[k];
+                }
+                tmem_ld_wait();
+            };
+            bool released = false;
             if (STAGE == 1) {
                 const int n0 = x.f * 64;  // first feature of the tile
-                for (int c = 0; c < nchunks; ++c) {
-                    float v[16];
-                    tmem_ld16(tacc + 16u * c, v);
-                    tmem_ld_wait();
-                    if (q >= 2) {
+                bool have = true;
+                if (p.ksplits > 1) {
+                    // Split-K: publish this split's partial sums, then the CTA that
+                    // completes the unit's count sums splits 0..S-1 in that order.
+                    float* part = p.ws.partial + (size_t)x.unit * p.ksplits * p.tile_rows * 128;
+                    for (int c = 0; c < nchunks; ++c) {
+                        float v[16];
+                        load_acc(c, v);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) xchg[((q - 2) * 16 + i) * 32 + lane] = v[i];
+                        for (int i = 0; i < 16; ++i)
+                            part[((size_t)x.split * p.tile_rows + 16 * c + i) * 128 + 32 * q + lane] = v[i];
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&tempty[a]);
+                    released = true;
+                    __threadfence();
+                    named_bar_sync(1, 128);
+                    if (q == 0 && lane == 0) {
+                        const uint32_t prev = atomicAdd(p.ws.counters + x.unit, 1u);
+                        *last_flag = (prev == (uint32_t)(p.ksplits - 1)) ? 1 : 0;
                     }
                     named_bar_sync(1, 128);
-                    if (q < 2) {
-                        const int slot_l = x.row0 + 16 * c + (int)(lane & 15);
-                        const int rid_l = __ldg(p.ws.sorted_ids + slot_l);
-                        const int feat = n0 + 32 * (int)q;  // first feature of this warp's block
-#pragma unroll 1
-                        for (int i = 0; i < 16; ++i) {
-                            const int rid = __shfl_sync(0xffffffffu, rid_l, i);
-                            if (rid >= R) continue;  // padding slot (warp-uniform)
-                            const float g = v[i];
-                            const float u = xchg[(q * 16 + i) * 32 + lane];
-                            const float sg = g / (1.0f + expf(-g));
-                            const float hv = __bfloat162float(__float2bfloat16_rn(sg * u));
-                            const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
-                            const uint32_t amax = __reduce_max_sync(0xffffffffu, hb);
-                            const uint32_t sbyte = mx_scale_byte(amax);
-                            const uint32_t code = e2m1_code(hv, sbyte, mx_inv_scale(sbyte == 255u ? 0u : sbyte));
-                            const uint32_t nb = __shfl_down_sync(0xffffffffu, code, 1);
-                            const uint32_t byte = (code | (nb << 4)) & 0xffu;
-                            const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
-                            const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
-                            const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
-                            const int slot = x.row0 + 16 * c + i;
-                            if ((lane & 7u) == 0) {
-                                const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                                *reinterpret_cast<uint32_t*>(p.ws.a2q + (size_t)slot * (p.I / 2) +
-                                                             feat / 2 + lane / 2) = word;
+                    have = *last_flag != 0;
+                    if (have) __threadfence();
+                }
+                if (have) {
+                    const float* part = p.ws.partial + (size_t)x.unit * p.ksplits * p.tile_rows * 128;
+                    for (int c = 0; c < nchunks; ++c) {
+                        float v[16];
+                        if (p.ksplits > 1) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[i] = __ldcg(part + ((size_t)(16 * c + i)) * 128 + 32 * q + lane);
+                            for (int sp = 1; sp < p.ksplits; ++sp) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[i] = v[i] + __ldcg(part + ((size_t)sp * p.tile_rows + 16 * c + i) * 128 +
+                                                         32 * q + lane);
                             }
-                            if (lane == 0)
-                                p.ws.a2s[(size_t)slot * p.a2s_stride + feat / 32] = (uint8_t)sbyte;
+                        } else {
+                            load_acc(c, v);
                         }
+                        if (q >= 2) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) xchg[((q - 2) * 16 + i) * 32 + lane] = v[i];
+                        }
+                        named_bar_sync(1, 128);
+                        if (q < 2) {
+                            const int slot_l = x.row0 + 16 * c + (int)(lane & 15);
+                            const int rid_l = __ldg(p.ws.sorted_ids + slot_l);
+                            const int feat = n0 + 32 * (int)q;  // first feature of this warp's block
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int rid = __shfl_sync(0xffffffffu, rid_l, i);
+                                if (rid >= R) continue;  // padding slot (warp-uniform)
+                                const float g = v[i];
+                                const float u = xchg[(q * 16 + i) * 32 + lane];
+                                const float sg = g / (1.0f + expf(-g));
+                                const float hv = __bfloat162float(__float2bfloat16_rn(sg * u));
+                                const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
+                                const uint32_t amax = __reduce_max_sync(0xffffffffu, hb);
+                                const uint32_t sbyte = mx_scale_byte(amax);
+                                const uint32_t code =
+                                    e2m1_code(hv, sbyte, mx_inv_scale(sbyte == 255u ? 0u : sbyte));
+                                const uint32_t nb = __shfl_down_sync(0xffffffffu, code, 1);
+                                const uint32_t byte = (code | (nb << 4)) & 0xffu;
+                                const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
+                                const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
+                                const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
+                                const int slot = x.row0 + 16 * c + i;
+                                if ((lane & 7u) == 0) {
+                                    const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                                    *reinterpret_cast<uint32_t*>(p.ws.a2q + (size_t)slot * (p.I / 2) +
+                                                                 feat / 2 + lane / 2) = word;
+                                }
+                                if (lane == 0)
+                                    p.ws.a2s[(size_t)slot * p.a2s_stride + feat / 32] = (uint8_t)sbyte;
+                            }
+                        }
+                        named_bar_sync(1, 128);
                     }
-                    named_bar_sync(1, 128);
                 }
             } else {
                 const int n = x.f * 128 + 32 * (int)q + (int)lane;  // output feature of this lane
                 for (int c = 0; c < nchunks; ++c) {
                     float v[16];
-                    tmem_ld16(tacc + 16u * c, v);
-                    tmem_ld_wait();
+                    load_acc(c, v);
                     const int slot_l = x.row0 + 16 * c + (int)(lane & 15);
                     const int rid_l = __ldg(p.ws.sorted_ids + slot_l);
                     const float w_l = __ldg(p.ws.sorted_w + slot_l);
@@ -365,8 +434,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&tempty[a]);
+            if (!released) {
+                tc_fence_before();
+                mbar_arrive(&tempty[a]);
+            }
         }
     }
 

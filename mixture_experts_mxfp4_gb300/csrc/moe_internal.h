@@ -44,6 +44,8 @@ struct GemmParams {
     int a_scale_small;  // weight scales read through a [rows*S/16, 16] view
     int b_scale_x;      // 1 when activation scales advance 16 bytes per stage
     int num_stages;     // shared-memory pipeline depth
+    int nacc;           // independent accumulators; MMA k-step j accumulates into j % nacc
+    int ctas_per_sm;    // 1, or 2 for narrow tiles (two MMA issue streams per SM)
     uint32_t tmem_cols; // TMEM columns allocated
     uint32_t sf_col0;   // first TMEM column of the per-stage scale-factor regions
     uint32_t stage_bytes, off_b, off_sa, off_sb; // per-stage layout (A at 0)

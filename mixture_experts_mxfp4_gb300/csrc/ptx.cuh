@@ -89,6 +89,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     }
 }
 
+// Warp-level wait: lane 0 polls, the other lanes wait at the shuffle.  With
+// backoff_ns > 0 the poller sleeps between polls (for long waits off the
+// critical path).  Must be called by all 32 lanes.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                               uint32_t err_bit, volatile int* abort_flag,
+                                               uint32_t backoff_ns = 0) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        const uint32_t a = smem_u32(bar);
+        if (!mbar_try_wait(a, parity)) {
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t it = 1;; ++it) {
+                if (backoff_ns) __nanosleep(backoff_ns);
+                if (mbar_try_wait(a, parity)) break;
+                if ((it & 15u) == 0) {
+                    if (*abort_flag) {
+                        ok = 0;
+                        break;
+                    }
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        atomicOr(status, err_bit);
+                        *abort_flag = 1;
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -113,6 +145,38 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D and 4-D tiled loads (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1,
+                                            int32_t c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, uint64_t* bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
+        "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m, int32_t c0,
+                                                 int32_t c1, int32_t c2, uint64_t* bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+        "l"(policy)
         : "memory");
 }
 
