@@ -154,16 +154,22 @@ const char* moe_mxfp4_version(void);
 int moe_mxfp4_num_kernels(void);
 
 /*
- * Optional instrumentation for benchmarks.  With enable != 0 the forward call
- * records a CUDA event on its stream before each kernel and after the last one
- * (events created once per device, on first enable; no device memory is
- * allocated).  moe_mxfp4_kernel_times waits for the last recorded event and
- * writes the duration of each kernel of the most recent call on the current
- * device, in milliseconds, to ms[0 .. min(n, num_kernels) - 1]; it returns the
- * number written, or -1 when timing is off or no call was recorded.
+ * Optional instrumentation for benchmarks (events created once per device on
+ * first use; no device memory is allocated).
+ *   mode 0: off.
+ *   mode 1: the forward call records a CUDA event on its stream before each
+ *           kernel and after the last one.  Events between kernels serialise
+ *           them (the dependent-launch overlap is lost), so use it for the
+ *           per-kernel breakdown.
+ *   mode 2: events only before the first and after the last kernel.
+ * moe_mxfp4_kernel_times (mode 1) waits for the last event and writes each
+ * kernel's duration of the most recent call, in ms, to ms[0 .. min(n, num_kernels)-1]
+ * and returns the count, or -1.  moe_mxfp4_last_call_ms (modes 1 and 2) returns
+ * the device time of the most recent call in ms, or a negative value.
  */
-moe_status_t moe_mxfp4_set_kernel_timing(int enable);
+moe_status_t moe_mxfp4_set_kernel_timing(int mode);
 int moe_mxfp4_kernel_times(float* ms, int n);
+float moe_mxfp4_last_call_ms(void);
 
 #ifdef __cplusplus
 }

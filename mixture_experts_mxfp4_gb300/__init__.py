@@ -43,6 +43,7 @@ EXPORTS = [
     "moe_mxfp4_num_kernels",
     "moe_mxfp4_set_kernel_timing",
     "moe_mxfp4_kernel_times",
+    "moe_mxfp4_last_call_ms",
 ]
 
 KERNEL_NAMES = ["route", "quant", "gemm_stage1", "gemm_stage2", "topk_sum"]
@@ -107,6 +108,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_set_kernel_timing.argtypes = [i]
     lib.moe_mxfp4_kernel_times.restype = i
     lib.moe_mxfp4_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), i]
+    lib.moe_mxfp4_last_call_ms.restype = ctypes.c_float
+    lib.moe_mxfp4_last_call_ms.argtypes = []
     _lib = lib
     return lib
 
@@ -146,9 +149,17 @@ def last_device_status(stream: int = 0) -> int:
     return int(load_library().moe_mxfp4_last_device_status(ctypes.c_void_p(stream)))
 
 
-def set_kernel_timing(enable: bool):
-    _check(load_library().moe_mxfp4_set_kernel_timing(1 if enable else 0),
-           "moe_mxfp4_set_kernel_timing")
+def set_kernel_timing(mode):
+    """0 off, 1 events around every kernel, 2 events around the whole call only."""
+    _check(load_library().moe_mxfp4_set_kernel_timing(int(mode)), "moe_mxfp4_set_kernel_timing")
+
+
+def last_call_ms() -> float:
+    """Device time (ms) of the last forward call on this device (timing mode 1 or 2)."""
+    t = float(load_library().moe_mxfp4_last_call_ms())
+    if t < 0:
+        raise MoeError(5, "moe_mxfp4_last_call_ms")
+    return t
 
 
 def kernel_times():

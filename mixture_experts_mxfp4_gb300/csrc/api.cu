@@ -26,6 +26,7 @@ struct WorkspaceReg {
 constexpr int kNumKernels = 5;
 
 struct Timing {
+    int mode = 0;
     bool enabled = false;
     bool created = false;
     bool recorded = false;
@@ -415,7 +416,7 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
     Timing& tm = g_timing[dev];
     const bool timed = tm.enabled && tm.created;
     auto mark = [&](int i) {
-        if (timed) cudaEventRecord(tm.ev[i], stream);
+        if (timed && (tm.mode == 1 || i == 0 || i == kNumKernels)) cudaEventRecord(tm.ev[i], stream);
     };
     mark(0);
     if (launch_route(topk_ids, topk_weights, T, K, E, pl.tile_rows, pl.cap, n_counters, ws,
@@ -438,26 +439,39 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
 
 int moe_mxfp4_num_kernels(void) { return kNumKernels; }
 
-moe_status_t moe_mxfp4_set_kernel_timing(int enable) {
+moe_status_t moe_mxfp4_set_kernel_timing(int mode) {
+    if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     Timing& tm = g_timing[dev];
-    if (enable && !tm.created) {
+    if (mode && !tm.created) {
         for (int i = 0; i <= kNumKernels; ++i)
             if (cudaEventCreate(&tm.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
         tm.created = true;
     }
-    tm.enabled = enable != 0;
+    tm.mode = mode;
+    tm.enabled = mode != 0;
     tm.recorded = false;
     return MOE_OK;
+}
+
+float moe_mxfp4_last_call_ms(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1.f;
+    Timing& tm = g_timing[dev];
+    if (!tm.enabled || !tm.recorded) return -1.f;
+    if (cudaEventSynchronize(tm.ev[kNumKernels]) != cudaSuccess) return -1.f;
+    float t = -1.f;
+    if (cudaEventElapsedTime(&t, tm.ev[0], tm.ev[kNumKernels]) != cudaSuccess) return -1.f;
+    return t;
 }
 
 int moe_mxfp4_kernel_times(float* ms, int n) {
     int dev = 0;
     if (!ms || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
     Timing& tm = g_timing[dev];
-    if (!tm.enabled || !tm.recorded) return -1;
+    if (!tm.enabled || !tm.recorded || tm.mode != 1) return -1;
     if (cudaEventSynchronize(tm.ev[kNumKernels]) != cudaSuccess) return -1;
     const int m = n < kNumKernels ? n : kNumKernels;
     for (int i = 0; i < m; ++i) {

@@ -106,10 +106,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + p.off_xchg + 4096);
     uint32_t* status = p.ws.status;
 
-    const int num_tiles = p.ws.num_valid[2];
-    const int num_items = num_tiles * p.n_ftiles * p.ksplits;
-    if ((int)blockIdx.x >= num_items) return;
-
+    grid_dep_launch();
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
@@ -124,15 +121,21 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 2) {
-        tmem_alloc(tmem_slot, p.tmem_cols);
-        tmem_relinquish();
-    }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmSB);
+    }
+    // Everything above overlaps the previous kernel; from here on the kernel
+    // reads what earlier kernels wrote, and TMEM is free once they have exited.
+    grid_dep_wait();
+    const int num_tiles = p.ws.num_valid[2];
+    const int num_items = num_tiles * p.n_ftiles * p.ksplits;
+    if ((int)blockIdx.x >= num_items) return;
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, p.tmem_cols);
+        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -454,8 +457,17 @@ cudaError_t launch_gemm(int stage, const CUtensorMap& tmA, const CUtensorMap& tm
     cudaError_t err =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
     if (err != cudaSuccess) return err;
-    kern<<<grid, kGemmThreads, p.smem_bytes, stream>>>(tmA, tmSA, tmB, tmSB, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmSA, tmB, tmSB, p);
 }
 
 }  // namespace moe

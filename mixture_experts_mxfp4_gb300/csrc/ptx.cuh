@@ -309,6 +309,20 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor finishes; grid_dep_wait()
+// blocks until the predecessor grid has completed and its writes are visible.
+// grid_dep_launch() lets the successor start launching.
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ misc
 
 __device__ __forceinline__ uint32_t lane_id() {

@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int R = T * K;
     const int bm = kBlockM;
+    grid_dep_launch();
 
     for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
     for (int i = tid; i < n_counters; i += kRouteThreads) ws.counters[i] = 0;
@@ -181,28 +182,31 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
 
 // ============================================================== quant + scatter
 //
-// One warp per token.  Lane g quantises 32-element block g (64 bytes of bf16,
-// four 16-byte loads) once, then writes its 16 code bytes and scale byte to
-// the sorted slot of every valid route of the token (the token's activation is
-// quantised once per token, as flower_moe.py does with topk=1 for hidden).
+// One thread per (token, 32-element block): the block (64 bytes of bf16, four
+// 16-byte loads) is quantised once, then its 16 code bytes and scale byte are
+// written to the sorted slot of every valid route of the token (the token's
+// activation is quantised once per token, as flower_moe.py does with topk=1
+// for the hidden states).  The loads and the quantisation run before the
+// routing kernel has finished (dependent launch); only the scatter waits.
 
-constexpr int kQuantWarps = 8;
+constexpr int kQuantThreads = 256;
 
-__global__ void __launch_bounds__(kQuantWarps * 32)
+__global__ void __launch_bounds__(kQuantThreads)
     moe_quant_kernel(const __nv_bfloat16* __restrict__ hidden, int T, int K, int D,
                      int a1s_stride, WsPtrs ws) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kQuantWarps + (threadIdx.x >> 5);
-    if (t >= T) return;
-    int pos[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) pos[k] = (k < K) ? ws.route_pos[t * K + k] : -1;
+    grid_dep_launch();
     const int nblk = D / 32;
-    const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)t * D);
-    for (int g = lane; g < nblk; g += 32) {
+    const long gid = (long)blockIdx.x * kQuantThreads + threadIdx.x;
+    const bool active = gid < (long)T * nblk;
+    const int t = active ? (int)(gid / nblk) : 0;
+    const int g = active ? (int)(gid - (long)t * nblk) : 0;
+    uint4 codes = make_uint4(0, 0, 0, 0);
+    uint32_t s = 0;
+    if (active) {
+        const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)t * D) + g * 4;
         uint4 raw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + g * 4 + i);
+        for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
         const uint32_t* w = reinterpret_cast<const uint32_t*>(raw);
         float v[32];
 #pragma unroll
@@ -213,28 +217,39 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         uint32_t amax = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
-        const uint32_t s = mx_scale_byte(amax);
+        s = mx_scale_byte(amax);
         const float inv = mx_inv_scale(s == 255u ? 0u : s);
         uint32_t packed[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int i = 0; i < 32; ++i) packed[i / 8] |= e2m1_code(v[i], s, inv) << (4 * (i % 8));
-        const uint4 codes = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (pos[k] >= 0) {
-                *reinterpret_cast<uint4*>(ws.a1q + (size_t)pos[k] * (D / 2) + g * 16) = codes;
-                ws.a1s[(size_t)pos[k] * a1s_stride + g] = (uint8_t)s;
-            }
+        codes = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    }
+    grid_dep_wait();  // route_pos comes from the routing kernel
+    if (!active) return;
+    for (int k = 0; k < K; ++k) {
+        const int pos = ws.route_pos[t * K + k];
+        if (pos >= 0) {
+            *reinterpret_cast<uint4*>(ws.a1q + (size_t)pos * (D / 2) + g * 16) = codes;
+            ws.a1s[(size_t)pos * a1s_stride + g] = (uint8_t)s;
         }
     }
 }
 
 cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride,
                          const WsPtrs& ws, cudaStream_t stream) {
-    const int grid = (T + kQuantWarps - 1) / kQuantWarps;
-    moe_quant_kernel<<<grid, kQuantWarps * 32, 0, stream>>>(
-        reinterpret_cast<const __nv_bfloat16*>(hidden), T, K, D, a1s_stride, ws);
-    return cudaGetLastError();
+    const long total = (long)T * (D / 32);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((total + kQuantThreads - 1) / kQuantThreads));
+    cfg.blockDim = dim3(kQuantThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_quant_kernel,
+                              reinterpret_cast<const __nv_bfloat16*>(hidden), T, K, D, a1s_stride,
+                              ws);
 }
 
 // ============================================================== top-k sum
@@ -246,6 +261,8 @@ cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride
 __global__ void __launch_bounds__(256)
     moe_reduce_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int D,
                       const float* __restrict__ P, __nv_bfloat16* __restrict__ out) {
+    grid_dep_launch();
+    grid_dep_wait();  // P comes from the stage-2 GEMM
     const int n4 = D / 4;
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)T * n4) return;
@@ -272,10 +289,17 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
                           const WsPtrs& ws, cudaStream_t stream) {
     const long total = (long)T * (D / 4);
-    const int grid = (int)((total + 255) / 256);
-    moe_reduce_kernel<<<grid, 256, 0, stream>>>(topk_ids, T, K, E, D, ws.P,
-                                                reinterpret_cast<__nv_bfloat16*>(out));
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((total + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_reduce_kernel, topk_ids, T, K, E, D,
+                              static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace moe
