@@ -60,6 +60,11 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int it) {
     return x;
 }
 
+// Scale factors in TMEM: tcgen05.cp .32x128b.warpx4 copies 32 rows x 16 bytes
+// and replicates them into the four 32-lane quadrants; one 128-element chunk of
+// 128 rows occupies an "atom" of 4 columns, and the MMA's scale-factor address
+// must be the first (4-aligned) column of an atom.
+//
 // Rearrange a raw scale tile (row m at m*sr bytes, 4-byte chunk c = scales of
 // K elements [128c, 128c+128)) into natoms scale-factor atoms in place: atom c
 // holds 128 rows as [m % 32][m / 32][4 bytes], the layout tcgen05.cp .32x128b
@@ -79,6 +84,25 @@ __device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, ui
             uint4 w = make_uint4(v[0][c], v[1][c], v[2][c], v[3][c]);
             *reinterpret_cast<uint4*>(buf + c * 512 + lane * 16) = w;
         }
+    }
+}
+
+// Issue one stage's MMAs (one thread).  KSTEPS = K-steps of 64 in the stage,
+// SPB = K-steps per TMA box row (4 for 128-byte rows, 2 for 64-byte rows).
+// Descriptors advance by constant offsets: +32 bytes per K-step inside a
+// swizzled row, + one box per SPB steps.
+template <int KSTEPS, int SPB>
+__device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, uint64_t bdesc0,
+                                                 uint32_t a_box, uint32_t b_box, uint32_t idesc_even,
+                                                 uint32_t idesc_odd, uint32_t sfa, uint32_t sfb,
+                                                 bool accumulate) {
+#pragma unroll
+    for (int j = 0; j < KSTEPS; ++j) {
+        const uint32_t kt = (uint32_t)(j / SPB), kk = (uint32_t)(j % SPB);
+        const uint64_t ad = adesc0 + (uint64_t)(kt * a_box + kk * 2u);
+        const uint64_t bd = bdesc0 + (uint64_t)(kt * b_box + kk * 2u);
+        mma_mxf4(d, ad, bd, (j & 1) ? idesc_odd : idesc_even, sfa + 4u * (j >> 1),
+                 sfb + 4u * (j >> 1), (accumulate || j > 0) ? 1u : 0u);
     }
 }
 
@@ -211,68 +235,116 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        int s = 0;
-        uint32_t ph = 0;
-        int local = 0;
-        bool ok = true;
+        // Walks this CTA's (item, k-stage) sequence.  When the next stage is
+        // already resident, its scale factors are copied to TMEM before this
+        // stage's MMAs are issued, so the MMAs never wait on fresh copies.
         const uint32_t layout = (p.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
         const uint32_t sbo = 8u * p.kb;
         const int ksteps = p.kstage_elems / 64;
-        const int steps_per_box = p.kb / 32;
+        const uint32_t a_box = (128u * p.kb) >> 4;              // descriptor units (16 B)
+        const uint32_t b_box = ((uint32_t)p.tile_rows * p.kb) >> 4;
         const uint32_t acc_cols = (uint32_t)(p.nacc * p.tile_rows);
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++local) {
-            const Item x = decode_item(p, it);
-            const int a = local & 1;
-            const uint32_t aph = (uint32_t)(local >> 1) & 1u;
-            if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
-                ok = false;
-                break;
+        auto sf_cols = [&](int ss) { return tmem_base + p.sf_col0 + (uint32_t)(ss * 8 * p.natoms); };
+        auto copy_scales = [&](int ss) {  // lane 0 only
+            uint8_t* st = smem + (size_t)ss * p.stage_bytes;
+            const uint32_t sfa = sf_cols(ss), sfb = sfa + 4u * p.natoms;
+            const uint64_t da = smem_desc(smem_u32(st + p.off_sa), 0, 128, 0);
+            const uint64_t db = smem_desc(smem_u32(st + p.off_sb), 0, 128, 0);
+            for (int c = 0; c < p.natoms; ++c) {
+                tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
+                tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
             }
-            tc_fence_after();
-            const uint32_t d_base = tmem_base + (uint32_t)a * acc_cols;
-            const uint32_t N = (uint32_t)x.nrows;
-            for (int ks = x.ks0; ks < x.ks1; ++ks) {
+        };
+        int it = blockIdx.x, local = 0, s = 0, pre = -1;
+        uint32_t ph = 0;
+        Item x = decode_item(p, it);
+        int ks = x.ks0;
+        bool ok = true;
+        uint32_t idesc_even = mxf4_idesc(128, (uint32_t)x.nrows, 0, 0);
+        uint32_t idesc_odd = mxf4_idesc(128, (uint32_t)x.nrows, 2, 2);
+        while (ok) {
+            const int a = local & 1;
+            if (ks == x.ks0) {
+                const uint32_t aph = (uint32_t)(local >> 1) & 1u;
+                if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (pre != s) {
                 if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
                     !mbar_wait_warp(&sfready[s], ph, status, kErrTimeoutFull, abort_flag)) {
                     ok = false;
                     break;
                 }
-                uint8_t* st = smem + (size_t)s * p.stage_bytes;
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t sfa = tmem_base + p.sf_col0 + (uint32_t)(s * 8 * p.natoms);
-                    const uint32_t sfb = sfa + 4u * p.natoms;
-                    for (int c = 0; c < p.natoms; ++c) {
-                        tmem_cp_sf(sfa + 4u * c, smem_desc(smem_u32(st + p.off_sa + 512 * c), 0, 128, 0));
-                        tmem_cp_sf(sfb + 4u * c, smem_desc(smem_u32(st + p.off_sb + 512 * c), 0, 128, 0));
-                    }
-                    const uint32_t a_base = smem_u32(st);
-                    const uint32_t b_base = smem_u32(st + p.off_b);
-                    const int kg0 = (ks - x.ks0) * ksteps;  // K-step index within the item
-                    for (int j = 0; j < ksteps; ++j) {
-                        const int kt = j / steps_per_box;
-                        const uint32_t koff = (uint32_t)(j % steps_per_box) * 32u;
-                        const uint64_t ad = smem_desc(a_base + kt * 128 * p.kb + koff, 16, sbo, layout);
-                        const uint64_t bd =
-                            smem_desc(b_base + kt * p.tile_rows * p.kb + koff, 16, sbo, layout);
-                        const uint32_t sid = (uint32_t)(j & 1) * 2u;
-                        const uint32_t idesc = mxf4_idesc(128, N, sid, sid);
-                        const int kg = kg0 + j;
-                        const uint32_t d = d_base + (uint32_t)((kg % p.nacc) * p.tile_rows);
-                        mma_mxf4(d, ad, bd, idesc, sfa + 4u * (j >> 1), sfb + 4u * (j >> 1),
-                                 kg >= p.nacc ? 1u : 0u);
-                    }
-                    tc_commit(&empty[s]);
-                }
-                __syncwarp();
-                if (++s == NS) {
-                    s = 0;
-                    ph ^= 1u;
+                    copy_scales(s);
                 }
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(&tfull[a]);
+            // next position in the sequence
+            int nit = it, nks = ks + 1, nlocal = local;
+            Item nx = x;
+            if (nks == x.ks1) {
+                nit += gridDim.x;
+                ++nlocal;
+                if (nit < num_items) {
+                    nx = decode_item(p, nit);
+                    nks = nx.ks0;
+                }
+            }
+            const bool nhave = nit < num_items;
+            int sn = s + 1;
+            uint32_t phn = ph;
+            if (sn == NS) {
+                sn = 0;
+                phn ^= 1u;
+            }
+            pre = -1;
+            if (nhave) {
+                int ready = 0;
+                if (lane == 0) ready = (mbar_test(&full[sn], phn) && mbar_test(&sfready[sn], phn)) ? 1 : 0;
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready) {
+                    if (lane == 0) {
+                        tc_fence_after();
+                        copy_scales(sn);
+                    }
+                    pre = sn;
+                }
+            }
+            if (lane == 0) {
+                uint8_t* st = smem + (size_t)s * p.stage_bytes;
+                const uint64_t ad0 = smem_desc(smem_u32(st), 16, sbo, layout);
+                const uint64_t bd0 = smem_desc(smem_u32(st + p.off_b), 16, sbo, layout);
+                const uint32_t sfa = sf_cols(s), sfb = sfa + 4u * p.natoms;
+                const uint32_t d = tmem_base + (uint32_t)a * acc_cols;
+                const bool acc = ks > x.ks0;
+                if (ksteps == 8)
+                    issue_stage_mmas<8, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa, sfb,
+                                           acc);
+                else if (ksteps == 4)
+                    issue_stage_mmas<4, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa, sfb,
+                                           acc);
+                else
+                    issue_stage_mmas<2, 2>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa, sfb,
+                                           acc);
+                tc_commit(&empty[s]);
+                if (ks + 1 == x.ks1) tc_commit(&tfull[a]);
+            }
             __syncwarp();
+            if (!nhave) break;
+            if (nlocal != local) {
+                idesc_even = mxf4_idesc(128, (uint32_t)nx.nrows, 0, 0);
+                idesc_odd = mxf4_idesc(128, (uint32_t)nx.nrows, 2, 2);
+            }
+            it = nit;
+            ks = nks;
+            x = nx;
+            local = nlocal;
+            s = sn;
+            ph = phn;
         }
         if (!ok && lane == 0) {
             // Wait for every MMA/copy already issued before TMEM is freed.
