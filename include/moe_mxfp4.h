@@ -92,6 +92,37 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
                                const float* topk_weights, void* out, int T, int d_model,
                                int d_inter, int E, int topk, cudaStream_t stream);
 
+/*
+ * Forward without any device allocation, for callers that cannot allocate.
+ * (This entry point has no counterpart in the pages; it is a deployment aid.)
+ *
+ * Some callers cannot call cudaMalloc when they run this layer: a serving
+ * runtime that has handed all free device memory to its own pool (cudaMalloc
+ * then fails), a plugin host that forbids plugins to allocate, or a latency-
+ * critical loop that must avoid cudaMalloc's implicit synchronisation.  They
+ * cannot own the workspace moe_mxfp4_forward needs either.  This call takes the
+ * same arguments and computes the same result, but its scratch is a static
+ * device array of MOE_MXFP4_STATIC_WORKSPACE_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits.  Nothing is
+ * allocated by the call: no cudaMalloc, no allocating library routine.
+ *   - Shapes whose workspace (moe_mxfp4_workspace_size) exceeds the array are
+ *     rejected with MOE_ERR_WORKSPACE; other errors as for moe_mxfp4_forward.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) for that device; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the array and leaves its contents behind;
+ *     the parts that must start at zero are cleared by each call.  Calls that
+ *     overlap on the GPU (unordered streams) race on the array.
+ *   - moe_mxfp4_last_device_status reports on the registered workspace, not on
+ *     this array.
+ */
+#define MOE_MXFP4_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+moe_status_t moe_mxfp4_forward_noalloc(const void* hidden, const void* w13, const void* w13_scale,
+                                       const void* w2, const void* w2_scale,
+                                       const int32_t* topk_ids, const float* topk_weights,
+                                       void* out, int T, int d_model, int d_inter, int E,
+                                       int topk, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_mxfp4_status_string(moe_status_t status);
 

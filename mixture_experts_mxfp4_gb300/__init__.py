@@ -44,7 +44,11 @@ EXPORTS = [
     "moe_mxfp4_set_kernel_timing",
     "moe_mxfp4_kernel_times",
     "moe_mxfp4_last_call_ms",
+    "moe_mxfp4_forward_noalloc",
 ]
+
+# Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
+STATIC_WORKSPACE_BYTES = 64 << 20
 
 KERNEL_NAMES = ["route", "quant", "gemm_stage1", "gemm_stage2", "topk_sum"]
 
@@ -110,6 +114,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), i]
     lib.moe_mxfp4_last_call_ms.restype = ctypes.c_float
     lib.moe_mxfp4_last_call_ms.argtypes = []
+    lib.moe_mxfp4_forward_noalloc.restype = i
+    lib.moe_mxfp4_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P]
     _lib = lib
     return lib
 
@@ -139,6 +145,18 @@ def forward_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, ou
                 T, d_model, d_inter, E, topk, stream: int = 0) -> int:
     """Raw-pointer call of moe_mxfp4_forward; returns the status code."""
     return int(load_library().moe_mxfp4_forward(
+        ctypes.c_void_p(hidden), ctypes.c_void_p(w13), ctypes.c_void_p(w13_scale),
+        ctypes.c_void_p(w2), ctypes.c_void_p(w2_scale), ctypes.c_void_p(topk_ids),
+        ctypes.c_void_p(topk_weights), ctypes.c_void_p(out), T, d_model, d_inter, E, topk,
+        ctypes.c_void_p(stream)))
+
+
+def forward_noalloc_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out,
+                        T, d_model, d_inter, E, topk, stream: int = 0) -> int:
+    """Raw-pointer call of moe_mxfp4_forward_noalloc (no workspace, nothing
+    allocated: the scratch is a static array inside the library); returns the
+    status code."""
+    return int(load_library().moe_mxfp4_forward_noalloc(
         ctypes.c_void_p(hidden), ctypes.c_void_p(w13), ctypes.c_void_p(w13_scale),
         ctypes.c_void_p(w2), ctypes.c_void_p(w2_scale), ctypes.c_void_p(topk_ids),
         ctypes.c_void_p(topk_weights), ctypes.c_void_p(out), T, d_model, d_inter, E, topk,

@@ -345,11 +345,14 @@ moe_status_t moe_mxfp4_last_device_status(cudaStream_t stream) {
     return word ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
 }
 
-moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* w13_scale,
-                               const void* w2, const void* w2_scale, const int32_t* topk_ids,
-                               const float* topk_weights, void* out, int T, int d_model,
-                               int d_inter, int E, int topk, cudaStream_t stream) {
-    const int D = d_model, I = d_inter, K = topk;
+}  // extern "C"
+
+namespace moe {
+
+moe_status_t validate_forward(const void* hidden, const void* w13, const void* w13_scale,
+                              const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                              const float* topk_weights, const void* out, int T, int D, int I,
+                              int E, int K) {
     moe_status_t st = validate_shape(T, D, I, E, K);
     if (st != MOE_OK) return st;
     if (T == 0) return MOE_OK;
@@ -358,20 +361,17 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
     if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_scale) || !aligned16(w2) ||
         !aligned16(w2_scale) || !aligned16(topk_ids) || !aligned16(topk_weights) || !aligned16(out))
         return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
 
+// The launch sequence of one forward call on the workspace at `base` (at least
+// workspace_bytes of the shape's plan, 256-byte aligned); arguments validated.
+moe_status_t forward_on_workspace(const void* hidden, const void* w13, const void* w13_scale,
+                                  const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                                  const float* topk_weights, void* out, int T, int D, int I, int E,
+                                  int K, void* base, int dev, cudaStream_t stream) {
     moe_mxfp4_plan_t pl;
     fill_plan(T, D, I, E, K, &pl);
-
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-    void* base;
-    size_t ws_bytes;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        base = g_ws[dev].ptr;
-        ws_bytes = g_ws[dev].bytes;
-    }
-    if (!base || ws_bytes < pl.workspace_bytes) return MOE_ERR_WORKSPACE;
     const WsPtrs ws = ws_ptrs(base, pl);
     const int R = T * K;
 
@@ -435,6 +435,39 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
     mark(5);
     if (timed) tm.recorded = true;
     return MOE_OK;
+}
+
+size_t plan_workspace_bytes(int T, int D, int I, int E, int K) {
+    moe_mxfp4_plan_t pl;
+    fill_plan(T, D, I, E, K, &pl);
+    return pl.workspace_bytes;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* w13_scale,
+                               const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                               const float* topk_weights, void* out, int T, int d_model,
+                               int d_inter, int E, int topk, cudaStream_t stream) {
+    const int D = d_model, I = d_inter, K = topk;
+    moe_status_t st = validate_forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
+                                       topk_weights, out, T, D, I, E, K);
+    if (st != MOE_OK || T == 0) return st;
+    const size_t need = plan_workspace_bytes(T, D, I, E, K);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void* base;
+    size_t ws_bytes;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        base = g_ws[dev].ptr;
+        ws_bytes = g_ws[dev].bytes;
+    }
+    if (!base || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    return forward_on_workspace(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out,
+                                T, D, I, E, K, base, dev, stream);
 }
 
 int moe_mxfp4_num_kernels(void) { return kNumKernels; }

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/moe_mxfp4.h"
+
 namespace moe {
 
 // Device pointers into the caller's workspace (see moe_mxfp4_plan_t).
@@ -58,6 +60,17 @@ struct GemmParams {
 constexpr int kBlockM = 16;          // slots per padded block
 constexpr int kGemmThreads = 256;    // 8 warps: producer, MMA, TMEM owner, spare, 4 epilogue
 constexpr int kMaxStages = 8;
+
+// Host-side pieces of the forward call shared by its entry points (api.cu).
+moe_status_t validate_forward(const void* hidden, const void* w13, const void* w13_scale,
+                              const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                              const float* topk_weights, const void* out, int T, int D, int I,
+                              int E, int K);
+size_t plan_workspace_bytes(int T, int D, int I, int E, int K);
+moe_status_t forward_on_workspace(const void* hidden, const void* w13, const void* w13_scale,
+                                  const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                                  const float* topk_weights, void* out, int T, int D, int I, int E,
+                                  int K, void* base, int dev, cudaStream_t stream);
 
 cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, int K, int E,
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,

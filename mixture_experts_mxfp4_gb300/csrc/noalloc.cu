@@ -1,0 +1,67 @@
+// moe_mxfp4_forward_noalloc: the forward call for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocating routine) at the point
+// where they run the MoE layer: a serving runtime that hands all free device
+// memory to its own pool at start-up (so a later cudaMalloc fails), a plugin
+// host that does not let plugins allocate, or a latency-critical loop that must
+// not hit cudaMalloc's implicit device synchronisation.  Such a caller also
+// cannot own a workspace for moe_mxfp4_set_workspace.  This entry point instead
+// uses a scratch buffer that lives in the library itself: a file-scope
+// __device__ array of kStaticWorkspaceBytes, which every GPU that loads the
+// library holds until the process exits.  Shapes whose workspace does not fit
+// are rejected with MOE_ERR_WORKSPACE.
+//
+// The array is shared by every call on a device and keeps the previous call's
+// contents; the parts that must start at zero (split-K arrival counters and the
+// device status word) are cleared by the routing kernel at the start of every
+// call.  Calls that overlap on the GPU (different streams without ordering)
+// race on the array.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = MOE_MXFP4_STATIC_WORKSPACE_BYTES;
+constexpr int kMaxDev = 64;
+
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDev];
+
+// Device address of g_static_workspace on the current device: looked up once
+// per device (the name is only a host-side stand-in for the device array).
+void* static_workspace(int dev) {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess) return nullptr;
+        g_static_ptr[dev] = ptr;
+    }
+    return g_static_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_mxfp4_forward_noalloc(const void* hidden, const void* w13,
+                                                  const void* w13_scale, const void* w2,
+                                                  const void* w2_scale, const int32_t* topk_ids,
+                                                  const float* topk_weights, void* out, int T,
+                                                  int d_model, int d_inter, int E, int topk,
+                                                  cudaStream_t stream) {
+    const moe_status_t st = moe::validate_forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
+                                                  topk_weights, out, T, d_model, d_inter, E, topk);
+    if (st != MOE_OK || T == 0) return st;
+    if (moe::plan_workspace_bytes(T, d_model, d_inter, E, topk) > kStaticWorkspaceBytes)
+        return MOE_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MOE_ERR_CUDA;
+    void* base = static_workspace(dev);
+    if (!base) return MOE_ERR_CUDA;
+    return moe::forward_on_workspace(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights,
+                                     out, T, d_model, d_inter, E, topk, base, dev, stream);
+}
