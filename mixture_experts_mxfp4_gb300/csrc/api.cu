@@ -226,10 +226,15 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int 
 }
 
 // Pipeline geometry of one GEMM stage for contraction length Kc.  Narrow route
-// tiles (decode) run two CTAs per SM: a single stream of scale-factor copies and
-// MMAs leaves the tensor pipe idle between them, and a second CTA fills it.
+// tiles (decode) use two MMA-issuing warps: a single stream of scale-factor
+// copies and narrow MMAs leaves the tensor pipe idle between instructions, and a
+// second stream fills it (measured ~2x per SM), while one CTA per SM keeps a
+// deep shared-memory ring to hide the TMA latency.
 void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1) {
-    g.ctas_per_sm = tile_rows <= 64 ? 2 : 1;
+    // Single-stage items (short contraction, e.g. stage 2 at d_inter <= 512):
+    // per-item work (tile lookup, barrier round trips) dominates, so two CTAs
+    // share each SM.
+    g.ctas_per_sm = (!stage1 && Kc <= 512 && tile_rows <= 64) ? 2 : 1;
     g.kstage_elems = Kc >= 512 ? 512 : Kc;
     g.kstages = Kc / g.kstage_elems;
     g.kb = g.kstage_elems >= 256 ? 128 : 64;
@@ -246,30 +251,47 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1) {
     g.off_sa = g.off_b + b_bytes;
     g.off_sb = g.off_sa + 2048;
     g.stage_bytes = (uint32_t)round_up(g.off_sb + 2048, 1024);
-    const uint32_t fixed = 1024 /*align slack*/ + 256 /*barriers*/ + (stage1 ? 4352u : 0u);
+    const uint32_t xchg = stage1 ? (uint32_t)(kEpiGroups * kXchgBytes) : 0u;
+    const uint32_t fixed = 1024 /*align slack*/ + 512 /*barriers*/ + xchg;
     // 227 KB of shared memory per SM, split between the CTAs of an SM
     const uint32_t budget = (g.ctas_per_sm == 2 ? 113u * 1024u : 227u * 1024u) - fixed;
     int ns = (int)(budget / g.stage_bytes);
     if (ns > kMaxStages) ns = kMaxStages;
-    // One accumulator per buffer: narrow MMAs into the same accumulator measured
-    // no slower than into separate ones.
-    const int nacc = 1;
     const uint32_t tmem_limit = 512u / (uint32_t)g.ctas_per_sm;
-    // TMEM: 2 accumulator buffers of nacc * N columns + per-stage scale factors.
-    while (ns > 1 && 2u * nacc * tile_rows + (uint32_t)ns * 8u * g.natoms > tmem_limit) --ns;
-    g.nacc = nacc;
+    // TMEM: acc_bufs accumulator buffers x one accumulator of N columns per MMA
+    // warp, plus the per-stage scale factors.  Single-stage items (short K) keep
+    // more items in flight between the MMA warps and the epilogue.
+    int nb = g.kstages == 1 ? 4 : 2;
+    int mw = tile_rows <= 64 ? 2 : 1;
+    auto cols_for = [&](int b, int m, int n) {
+        return (uint32_t)(b * m * tile_rows) + (uint32_t)n * 8u * g.natoms;
+    };
+    if (cols_for(nb, mw, ns) > tmem_limit) nb = 2;
+    if (cols_for(nb, mw, ns) > tmem_limit) mw = 1;
+    while (ns > 1 && cols_for(nb, mw, ns) > tmem_limit) --ns;
+    // The MMA warps' look-ahead tests slot (g + mw) % ns by parity; that is only
+    // unambiguous when the slot's previous stage (g + mw - ns) belonged to the
+    // same warp, i.e. when ns is a multiple of mw.
+    if (mw == 2 && ns % 2 == 1) {
+        if (ns > 2)
+            --ns;
+        else
+            mw = 1;
+    }
+    g.mma_warps = mw;
+    g.acc_bufs = nb;
     g.num_stages = ns;
     g.off_bar = (uint32_t)ns * g.stage_bytes;
-    g.off_xchg = g.off_bar + 256;
-    g.smem_bytes = g.off_xchg + (stage1 ? 4352u : 0u) + 1024u;
+    g.off_xchg = g.off_bar + 512;  // barriers, TMEM slot and abort flag fit in 512 bytes
+    g.smem_bytes = g.off_xchg + xchg + 1024u;
     // with one CTA per SM, ask for more than half the SM's shared memory so that
     // two CTAs never share an SM (and its TMEM)
     if (g.ctas_per_sm == 1 && g.smem_bytes < 118u * 1024u) g.smem_bytes = 118u * 1024u;
-    const uint32_t cols = 2u * nacc * tile_rows + (uint32_t)ns * 8u * g.natoms;
+    const uint32_t cols = cols_for(nb, mw, ns);
     uint32_t alloc = 32;
     while (alloc < cols) alloc <<= 1;
     g.tmem_cols = alloc;
-    g.sf_col0 = 2u * nacc * tile_rows;
+    g.sf_col0 = (uint32_t)(nb * mw * tile_rows);
 }
 
 int num_sms(int dev) {

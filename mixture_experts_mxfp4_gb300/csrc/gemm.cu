@@ -21,14 +21,16 @@
 // Pipeline (one CTA per SM, persistent over work items):
 //   warp 0  TMA producer: one box each for the weight tile, the route tile and
 //           the two raw scale tiles per stage -> smem ring
-//   warp 1  MMA warp: copies the stage's scale factors to TMEM (tcgen05.cp) and
-//           issues tcgen05.mma; consecutive K-steps go to `nacc` independent
-//           accumulators so that narrow (small-N) MMAs do not wait on each other
-//   warp 2  allocates / frees TMEM
+//   warp 1  MMA warp: copies a stage's scale factors to TMEM (tcgen05.cp) and
+//           issues tcgen05.mma.  With mma_warps = 2, warp 2 is a second MMA warp:
+//           the CTA's stages alternate between the two (each into its own
+//           accumulator), so two instruction streams keep the tensor pipe busy
+//           with narrow (small-N) MMAs
+//   warp 2  also allocates / frees TMEM
 //   warp 3  rearranges each stage's raw scale tiles into the tcgen05
-//           scale-factor layout one stage ahead of the MMA warp
-//   warps 4-7  epilogue: tcgen05.ld of the double-buffered accumulators, summed
-//           over the nacc partial accumulators in a fixed order
+//           scale-factor layout ahead of the MMA warps
+//   warps 4-7  epilogue: tcgen05.ld of the double-buffered accumulators; the two
+//           MMA warps' partial accumulators are summed in a fixed order
 // All waits are bounded (ptx.cuh).
 #include <cuda_bf16.h>
 
@@ -71,11 +73,22 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int it) {
 // .warpx4 expects.  Whole warp; rows >= 128 are not touched.
 __device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, uint32_t lane) {
     uint32_t v[4][4];
+    if (sr == 16) {  // whole 16-byte rows: conflict-free vector loads
 #pragma unroll
-    for (int m1 = 0; m1 < 4; ++m1) {
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(buf + (m1 * 32 + lane) * sr);
+        for (int m1 = 0; m1 < 4; ++m1) {
+            const uint4 r = *reinterpret_cast<const uint4*>(buf + (m1 * 32 + lane) * 16);
+            v[m1][0] = r.x;
+            v[m1][1] = r.y;
+            v[m1][2] = r.z;
+            v[m1][3] = r.w;
+        }
+    } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) v[m1][c] = (c < natoms) ? row[c] : 0u;
+        for (int m1 = 0; m1 < 4; ++m1) {
+            const uint32_t* row = reinterpret_cast<const uint32_t*>(buf + (m1 * 32 + lane) * sr);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[m1][c] = (c < natoms) ? row[c] : 0u;
+        }
     }
     __syncwarp();
 #pragma unroll
@@ -107,7 +120,7 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, ui
 }
 
 template <int STAGE>
-__global__ void __launch_bounds__(kGemmThreads, 2)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmSA,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmSB,
                     const GemmParams p) {
@@ -122,10 +135,11 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     uint64_t* empty = full + kMaxStages;
     uint64_t* sfready = empty + kMaxStages;
     uint64_t* tfull = sfready + kMaxStages;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
+    uint64_t* tempty = tfull + kMaxAccBufs;
+    uint64_t* drain = tempty + kMaxAccBufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // per epilogue group: 4 KB exchange buffer, then a flag word
     float* xchg = reinterpret_cast<float*>(smem + p.off_xchg);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + p.off_xchg + 4096);
     uint32_t* status = p.ws.status;
@@ -137,8 +151,8 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             mbar_init(&empty[s], 1);
             mbar_init(&sfready[s], 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&tfull[a], 1);
+        for (int a = 0; a < p.acc_bufs; ++a) {
+            mbar_init(&tfull[a], (uint32_t)p.mma_warps);
             mbar_init(&tempty[a], 128);
         }
         mbar_init(drain, 1);
@@ -233,17 +247,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 }
             }
         }
-    } else if (warp == 1) {
+    }
+    if (warp == 1 || (warp == 2 && p.mma_warps == 2)) {
         // ------------------------------------------------------------ MMA
-        // Walks this CTA's (item, k-stage) sequence.  When the next stage is
-        // already resident, its scale factors are copied to TMEM before this
-        // stage's MMAs are issued, so the MMAs never wait on fresh copies.
+        // The CTA's stages are numbered g = 0, 1, ... in (item, k-stage) order;
+        // MMA warp w issues the stages with g % mma_warps == w into its own
+        // accumulator.  When this warp's next stage is already resident, its
+        // scale factors are copied to TMEM before this stage's MMAs are issued,
+        // so the MMAs never wait on just-issued copies.
+        const int w = (int)warp - 1;
+        const int MW = p.mma_warps;
         const uint32_t layout = (p.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
         const uint32_t sbo = 8u * p.kb;
         const int ksteps = p.kstage_elems / 64;
         const uint32_t a_box = (128u * p.kb) >> 4;              // descriptor units (16 B)
         const uint32_t b_box = ((uint32_t)p.tile_rows * p.kb) >> 4;
-        const uint32_t acc_cols = (uint32_t)(p.nacc * p.tile_rows);
+        const uint32_t acc_cols = (uint32_t)(MW * p.tile_rows);  // per accumulator buffer
         auto sf_cols = [&](int ss) { return tmem_base + p.sf_col0 + (uint32_t)(ss * 8 * p.natoms); };
         auto copy_scales = [&](int ss) {  // lane 0 only
             uint8_t* st = smem + (size_t)ss * p.stage_bytes;
@@ -255,96 +274,80 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
             }
         };
-        int it = blockIdx.x, local = 0, s = 0, pre = -1;
-        uint32_t ph = 0;
-        Item x = decode_item(p, it);
-        int ks = x.ks0;
+        auto ready = [&](long gg) -> bool {  // lane 0: stage gg resident and rearranged?
+            const int ss = (int)(gg % NS);
+            const uint32_t pp = (uint32_t)((gg / NS) & 1);
+            return mbar_test(&full[ss], pp) && mbar_test(&sfready[ss], pp);
+        };
+        long g = 0;       // flattened index of the current (item, k-stage)
+        long pre = -1;    // stage whose scale factors are already in TMEM
         bool ok = true;
-        uint32_t idesc_even = mxf4_idesc(128, (uint32_t)x.nrows, 0, 0);
-        uint32_t idesc_odd = mxf4_idesc(128, (uint32_t)x.nrows, 2, 2);
-        while (ok) {
-            const int a = local & 1;
-            if (ks == x.ks0) {
-                const uint32_t aph = (uint32_t)(local >> 1) & 1u;
-                if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+        int local = 0;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++local) {
+            const Item x = decode_item(p, it);
+            const int a = local % p.acc_bufs;
+            const uint32_t aph = (uint32_t)(local / p.acc_bufs) & 1u;
+            if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
+                ok = false;
+                break;
             }
-            if (pre != s) {
-                if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
-                    !mbar_wait_warp(&sfready[s], ph, status, kErrTimeoutFull, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    tc_fence_after();
-                    copy_scales(s);
-                }
-            }
-            // next position in the sequence
-            int nit = it, nks = ks + 1, nlocal = local;
-            Item nx = x;
-            if (nks == x.ks1) {
-                nit += gridDim.x;
-                ++nlocal;
-                if (nit < num_items) {
-                    nx = decode_item(p, nit);
-                    nks = nx.ks0;
-                }
-            }
-            const bool nhave = nit < num_items;
-            int sn = s + 1;
-            uint32_t phn = ph;
-            if (sn == NS) {
-                sn = 0;
-                phn ^= 1u;
-            }
-            pre = -1;
-            if (nhave) {
-                int ready = 0;
-                if (lane == 0) ready = (mbar_test(&full[sn], phn) && mbar_test(&sfready[sn], phn)) ? 1 : 0;
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
+            tc_fence_after();
+            const uint32_t d = tmem_base + (uint32_t)a * acc_cols + (uint32_t)(w * p.tile_rows);
+            const uint32_t idesc_even = mxf4_idesc(128, (uint32_t)x.nrows, 0, 0);
+            const uint32_t idesc_odd = mxf4_idesc(128, (uint32_t)x.nrows, 2, 2);
+            const bool more_items = it + (int)gridDim.x < num_items;
+            bool first = true;
+            for (int ks = x.ks0; ks < x.ks1; ++ks, ++g) {
+                if ((int)(g % MW) != w) continue;
+                const int s = (int)(g % NS);
+                const uint32_t ph = (uint32_t)((g / NS) & 1);
+                if (pre != g) {
+                    if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
+                        !mbar_wait_warp(&sfready[s], ph, status, kErrTimeoutFull, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     if (lane == 0) {
                         tc_fence_after();
-                        copy_scales(sn);
+                        copy_scales(s);
                     }
-                    pre = sn;
                 }
+                // this warp's next stage: in this item, or the first stage of the next
+                const long gn = g + MW;
+                const bool next_exists = (ks + MW < x.ks1) || more_items;
+                int rd = 0;
+                if (lane == 0 && next_exists) rd = ready(gn) ? 1 : 0;
+                rd = __shfl_sync(0xffffffffu, rd, 0);
+                if (rd) {
+                    if (lane == 0) {
+                        tc_fence_after();
+                        copy_scales((int)(gn % NS));
+                    }
+                    pre = gn;
+                }
+                if (lane == 0) {
+                    uint8_t* st = smem + (size_t)s * p.stage_bytes;
+                    const uint64_t ad0 = smem_desc(smem_u32(st), 16, sbo, layout);
+                    const uint64_t bd0 = smem_desc(smem_u32(st + p.off_b), 16, sbo, layout);
+                    const uint32_t sfa = sf_cols(s), sfb = sfa + 4u * p.natoms;
+                    if (ksteps == 8)
+                        issue_stage_mmas<8, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa,
+                                               sfb, !first);
+                    else if (ksteps == 4)
+                        issue_stage_mmas<4, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa,
+                                               sfb, !first);
+                    else
+                        issue_stage_mmas<2, 2>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa,
+                                               sfb, !first);
+                    tc_commit(&empty[s]);
+                }
+                __syncwarp();
+                first = false;
             }
-            if (lane == 0) {
-                uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                const uint64_t ad0 = smem_desc(smem_u32(st), 16, sbo, layout);
-                const uint64_t bd0 = smem_desc(smem_u32(st + p.off_b), 16, sbo, layout);
-                const uint32_t sfa = sf_cols(s), sfb = sfa + 4u * p.natoms;
-                const uint32_t d = tmem_base + (uint32_t)a * acc_cols;
-                const bool acc = ks > x.ks0;
-                if (ksteps == 8)
-                    issue_stage_mmas<8, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa, sfb,
-                                           acc);
-                else if (ksteps == 4)
-                    issue_stage_mmas<4, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa, sfb,
-                                           acc);
-                else
-                    issue_stage_mmas<2, 2>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa, sfb,
-                                           acc);
-                tc_commit(&empty[s]);
-                if (ks + 1 == x.ks1) tc_commit(&tfull[a]);
-            }
+            if (!ok) break;
+            // every MMA warp arrives once per item (a warp without stages in it too)
+            if (lane == 0) tc_commit(&tfull[a]);
             __syncwarp();
-            if (!nhave) break;
-            if (nlocal != local) {
-                idesc_even = mxf4_idesc(128, (uint32_t)nx.nrows, 0, 0);
-                idesc_odd = mxf4_idesc(128, (uint32_t)nx.nrows, 2, 2);
-            }
-            it = nit;
-            ks = nks;
-            x = nx;
-            local = nlocal;
-            s = sn;
-            ph = phn;
         }
         if (!ok && lane == 0) {
             // Wait for every MMA/copy already issued before TMEM is freed.
@@ -384,29 +387,57 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
-        const uint32_t q = warp & 3u;  // TMEM lane quadrant of this warp
+        // Two groups of four warps take alternate items, so one item's global
+        // traffic overlaps the next item's TMEM reads.  Each group covers the 128
+        // TMEM lanes (warp % 4 = lane quadrant).
+        const uint32_t q = warp & 3u;            // TMEM lane quadrant of this warp
+        const int grp = (int)(warp - 4) >> 2;    // epilogue group
+        const uint32_t bar_id = 1u + (uint32_t)grp;
+        float* xg = xchg + grp * (kXchgBytes / 4);
+        volatile int* flag = last_flag + grp * (kXchgBytes / 4);
         const int R = p.R;
+        const int MW = p.mma_warps;
         int local = 0;
+        int g0 = 0;  // flattened index of the item's first k-stage (as the MMA warps count)
         for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++local) {
             const Item x = decode_item(p, it);
-            const int a = local & 1;
-            const uint32_t aph = (uint32_t)(local >> 1) & 1u;
-            if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag, 256)) break;
+            const int nst = x.ks1 - x.ks0;
+            const int gbeg = g0;
+            g0 += nst;
+            if ((local & (kEpiGroups - 1)) != grp) continue;
+            // route metadata of the tile's first 16 slots, fetched before waiting
+            const int slot0 = x.row0 + (int)(lane & 15);
+            int rid_pre = __ldg(p.ws.sorted_ids + slot0);
+            float w_pre = STAGE == 2 ? __ldg(p.ws.sorted_w + slot0) : 0.0f;
+            const int a = local % p.acc_bufs;
+            const uint32_t aph = (uint32_t)(local / p.acc_bufs) & 1u;
+            if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc =
-                tmem_base + ((q * 32u) << 16) + (uint32_t)(a * p.nacc * p.tile_rows);
+                tmem_base + ((q * 32u) << 16) + (uint32_t)(a * MW * p.tile_rows);
             const int nchunks = x.nrows / 16;
-            // v = sum over the nacc partial accumulators, in ascending order
+            // MMA warp w wrote an accumulator for this item iff one of the item's
+            // stages g has g % MW == w.
+            bool has1 = false;
+            if (MW == 2) has1 = ((gbeg & 1) == 1) || nst > 1;
+            const bool has0 = (MW == 1) || ((gbeg & 1) == 0) || nst > 1;
+            // v = sum of the MMA warps' partial accumulators, warp 0's first
             auto load_acc = [&](int c, float (&v)[16]) {
-                tmem_ld16(tacc + 16u * c, v);
-                for (int i = 1; i < p.nacc; ++i) {
+                if (has0 && has1) {
                     float t[16];
-                    tmem_ld16(tacc + (uint32_t)(i * p.tile_rows) + 16u * c, t);
+                    tmem_ld16(tacc + 16u * c, v);
+                    tmem_ld16(tacc + (uint32_t)p.tile_rows + 16u * c, t);
                     tmem_ld_wait();
 #pragma unroll
                     for (int k = 0; k < 16; ++k) v[k] = v[k] + t[k];
+                } else {
+                    tmem_ld16(tacc + (has0 ? 0u : (uint32_t)p.tile_rows) + 16u * c, v);
+                    tmem_ld_wait();
                 }
-                tmem_ld_wait();
+            };
+            auto release = [&]() {
+                tc_fence_before();
+                mbar_arrive(&tempty[a]);
             };
             bool released = false;
             if (STAGE == 1) {
@@ -419,21 +450,22 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     for (int c = 0; c < nchunks; ++c) {
                         float v[16];
                         load_acc(c, v);
+                        if (c + 1 == nchunks) {
+                            release();
+                            released = true;
+                        }
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             part[((size_t)x.split * p.tile_rows + 16 * c + i) * 128 + 32 * q + lane] = v[i];
                     }
-                    tc_fence_before();
-                    mbar_arrive(&tempty[a]);
-                    released = true;
                     __threadfence();
-                    named_bar_sync(1, 128);
+                    named_bar_sync(bar_id, 128);
                     if (q == 0 && lane == 0) {
                         const uint32_t prev = atomicAdd(p.ws.counters + x.unit, 1u);
-                        *last_flag = (prev == (uint32_t)(p.ksplits - 1)) ? 1 : 0;
+                        *flag = (prev == (uint32_t)(p.ksplits - 1)) ? 1 : 0;
                     }
-                    named_bar_sync(1, 128);
-                    have = *last_flag != 0;
+                    named_bar_sync(bar_id, 128);
+                    have = *flag != 0;
                     if (have) __threadfence();
                 }
                 if (have) {
@@ -452,22 +484,26 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                             }
                         } else {
                             load_acc(c, v);
+                            if (c + 1 == nchunks) {
+                                release();
+                                released = true;
+                            }
                         }
                         if (q >= 2) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) xchg[((q - 2) * 16 + i) * 32 + lane] = v[i];
+                            for (int i = 0; i < 16; ++i) xg[((q - 2) * 16 + i) * 32 + lane] = v[i];
                         }
-                        named_bar_sync(1, 128);
+                        named_bar_sync(bar_id, 128);
                         if (q < 2) {
-                            const int slot_l = x.row0 + 16 * c + (int)(lane & 15);
-                            const int rid_l = __ldg(p.ws.sorted_ids + slot_l);
+                            const int rid_l =
+                                c == 0 ? rid_pre : __ldg(p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
                             const int feat = n0 + 32 * (int)q;  // first feature of this warp's block
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const int rid = __shfl_sync(0xffffffffu, rid_l, i);
                                 if (rid >= R) continue;  // padding slot (warp-uniform)
                                 const float g = v[i];
-                                const float u = xchg[(q * 16 + i) * 32 + lane];
+                                const float u = xg[(q * 16 + i) * 32 + lane];
                                 const float sg = g / (1.0f + expf(-g));
                                 const float hv = __bfloat162float(__float2bfloat16_rn(sg * u));
                                 const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
@@ -490,7 +526,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                                     p.ws.a2s[(size_t)slot * p.a2s_stride + feat / 32] = (uint8_t)sbyte;
                             }
                         }
-                        named_bar_sync(1, 128);
+                        named_bar_sync(bar_id, 128);
                     }
                 }
             } else {
@@ -498,9 +534,17 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 for (int c = 0; c < nchunks; ++c) {
                     float v[16];
                     load_acc(c, v);
-                    const int slot_l = x.row0 + 16 * c + (int)(lane & 15);
-                    const int rid_l = __ldg(p.ws.sorted_ids + slot_l);
-                    const float w_l = __ldg(p.ws.sorted_w + slot_l);
+                    if (c + 1 == nchunks) {
+                        release();
+                        released = true;
+                    }
+                    int rid_l = rid_pre;
+                    float w_l = w_pre;
+                    if (c > 0) {
+                        const int sl = x.row0 + 16 * c + (int)(lane & 15);
+                        rid_l = __ldg(p.ws.sorted_ids + sl);
+                        w_l = __ldg(p.ws.sorted_w + sl);
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int rid = __shfl_sync(0xffffffffu, rid_l, i);
@@ -509,10 +553,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     }
                 }
             }
-            if (!released) {
-                tc_fence_before();
-                mbar_arrive(&tempty[a]);
-            }
+            if (!released) release();
         }
     }
 

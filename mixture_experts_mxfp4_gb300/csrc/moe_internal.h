@@ -46,8 +46,9 @@ struct GemmParams {
     int a_scale_small;  // weight scales read through a [rows*S/16, 16] view
     int b_scale_x;      // 1 when activation scales advance 16 bytes per stage
     int num_stages;     // shared-memory pipeline depth
-    int nacc;           // independent accumulators; MMA k-step j accumulates into j % nacc
-    int ctas_per_sm;    // 1, or 2 for narrow tiles (two MMA issue streams per SM)
+    int mma_warps;      // MMA-issuing warps (1 or 2); warp w takes the CTA's stages g % mma_warps == w
+    int ctas_per_sm;    // CTAs per SM (1 or 2)
+    int acc_bufs;       // TMEM accumulator buffers (items in flight between MMA and epilogue)
     uint32_t tmem_cols; // TMEM columns allocated
     uint32_t sf_col0;   // first TMEM column of the per-stage scale-factor regions
     uint32_t stage_bytes, off_b, off_sa, off_sb; // per-stage layout (A at 0)
@@ -58,8 +59,12 @@ struct GemmParams {
 };
 
 constexpr int kBlockM = 16;          // slots per padded block
-constexpr int kGemmThreads = 256;    // 8 warps: producer, MMA, TMEM owner, spare, 4 epilogue
+// 12 warps: producer, MMA, second MMA / TMEM owner, scale layout, 2 x 4 epilogue
+constexpr int kGemmThreads = 384;
+constexpr int kEpiGroups = 2;
+constexpr int kXchgBytes = 4352;     // per epilogue group: 4 KB exchange + flag
 constexpr int kMaxStages = 8;
+constexpr int kMaxAccBufs = 4;
 
 // Host-side pieces of the forward call shared by its entry points (api.cu).
 moe_status_t validate_forward(const void* hidden, const void* w13, const void* w13_scale,
