@@ -74,6 +74,9 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     pl->max_tiles = (int)(cap / kBlockM);
     // Stage-1 K splits: decode batches have few (expert, feature-tile) units per
     // SM, so the contraction over d_model is split and summed by the last CTA.
+    // Stage-1 K splits: decode batches have few (expert, feature-tile) units per
+    // SM, so the contraction over d_model is split and summed by the last CTA.
+    // (Finer splits measured slower: the split-K epilogue costs per item.)
     {
         const int kst = D >= 512 ? D / 512 : 1;
         const double units = (double)(used < E ? used : E) * (I / 64);
@@ -230,7 +233,7 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int 
 // copies and narrow MMAs leaves the tensor pipe idle between instructions, and a
 // second stream fills it (measured ~2x per SM), while one CTA per SM keeps a
 // deep shared-memory ring to hide the TMA latency.
-void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1) {
+void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplits) {
     // Single-stage items (short contraction, e.g. stage 2 at d_inter <= 512):
     // per-item work (tile lookup, barrier round trips) dominates, so two CTAs
     // share each SM.
@@ -261,7 +264,7 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1) {
     // TMEM: acc_bufs accumulator buffers x one accumulator of N columns per MMA
     // warp, plus the per-stage scale factors.  Single-stage items (short K) keep
     // more items in flight between the MMA warps and the epilogue.
-    int nb = g.kstages == 1 ? 4 : 2;
+    int nb = g.kstages / ksplits <= 2 ? 4 : 2;
     int mw = tile_rows <= 64 ? 2 : 1;
     auto cols_for = [&](int b, int m, int n) {
         return (uint32_t)(b * m * tile_rows) + (uint32_t)n * 8u * g.natoms;
@@ -404,12 +407,12 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     g1.D = D; g1.I = I; g1.E = E; g1.K = K; g1.R = R;
     g1.a1s_stride = pl.a1s_stride;
     g1.a2s_stride = pl.a2s_stride;
-    gemm_geometry(g1, D, pl.tile_rows, true);
+    gemm_geometry(g1, D, pl.tile_rows, true, pl.stage1_splits);
     g1.n_ftiles = I / 64;
     g1.ksplits = pl.stage1_splits;
 
     GemmParams g2 = g1;
-    gemm_geometry(g2, I, pl.tile_rows, false);
+    gemm_geometry(g2, I, pl.tile_rows, false, 1);
     g2.n_ftiles = D / 128;
     g2.ksplits = 1;
 

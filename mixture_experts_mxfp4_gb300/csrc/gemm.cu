@@ -131,10 +131,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t lane = threadIdx.x & 31;
     const int NS = p.num_stages;
 
+    // full: weight + route tiles landed; sfull: raw scale tiles landed (they are
+    // small and arrive first, so their rearrangement overlaps the weight load);
+    // sfready: scale tiles rearranged; empty: stage consumed by the MMAs.
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* empty = full + kMaxStages;
     uint64_t* sfready = empty + kMaxStages;
-    uint64_t* tfull = sfready + kMaxStages;
+    uint64_t* sfull = sfready + kMaxStages;
+    uint64_t* tfull = sfull + kMaxStages;
     uint64_t* tempty = tfull + kMaxAccBufs;
     uint64_t* drain = tempty + kMaxAccBufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -150,6 +154,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sfready[s], 1);
+            mbar_init(&sfull[s], 1);
         }
         for (int a = 0; a < p.acc_bufs; ++a) {
             mbar_init(&tfull[a], (uint32_t)p.mma_warps);
@@ -199,30 +204,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                    const uint32_t tx = (uint32_t)(128 + p.tile_rows) * kbytes_stage +
-                                        128u * p.sr_a + (uint32_t)p.tile_rows * 16u;
-                    mbar_arrive_expect_tx(&full[s], tx);
                     const int kt0 = ks * p.nkt;  // first K box of the stage
+                    const int rg = STAGE == 1 ? x.e * 2 * p.I + x.f * 64 : x.e * p.D + x.f * 128;
+                    // raw scale tiles first, on their own barrier
+                    mbar_arrive_expect_tx(&sfull[s], 128u * p.sr_a + (uint32_t)p.tile_rows * 16u);
                     if (STAGE == 1) {
-                        // 64 gate rows and the 64 matching up rows (I rows further) in one box
-                        const int rg = x.e * 2 * p.I + x.f * 64;
-                        tma_load_4d_hint(st, &tmA, 0, rg, 0, kt0, &full[s], pol_w);
+                        // the 64 gate rows and the 64 matching up rows (I rows further)
                         if (p.a_scale_small)
-                            tma_load_3d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), 0, &full[s]);
+                            tma_load_3d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), 0, &sfull[s]);
                         else
-                            tma_load_3d(st + p.off_sa, &tmSA, ks * 16, rg, 0, &full[s]);
+                            tma_load_3d(st + p.off_sa, &tmSA, ks * 16, rg, 0, &sfull[s]);
                     } else {
-                        const int rg = x.e * p.D + x.f * 128;
-                        tma_load_3d_hint(st, &tmA, 0, rg, kt0, &full[s], pol_w);
                         if (p.a_scale_small)
-                            tma_load_2d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), &full[s]);
+                            tma_load_2d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), &sfull[s]);
                         else
-                            tma_load_2d(st + p.off_sa, &tmSA, ks * 16, rg, &full[s]);
+                            tma_load_2d(st + p.off_sa, &tmSA, ks * 16, rg, &sfull[s]);
                     }
+                    tma_load_2d(st + p.off_sb, &tmSB, p.b_scale_x ? ks * 16 : 0, x.row0, &sfull[s]);
+                    // weight tile and route tile
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(128 + p.tile_rows) * kbytes_stage);
+                    if (STAGE == 1)
+                        tma_load_4d_hint(st, &tmA, 0, rg, 0, kt0, &full[s], pol_w);
+                    else
+                        tma_load_3d_hint(st, &tmA, 0, rg, kt0, &full[s], pol_w);
                     // route tile: tile_rows sorted slots from row0 (rows past the tile's
                     // own are read but never used; past the end they are zero-filled)
                     tma_load_3d(st + p.off_b, &tmB, 0, x.row0, kt0, &full[s]);
-                    tma_load_2d(st + p.off_sb, &tmSB, p.b_scale_x ? ks * 16 : 0, x.row0, &full[s]);
                     issued |= 1u << s;
                     last_ph = (last_ph & ~(1u << s)) | (ph << s);
                     if (++s == NS) {
@@ -238,7 +245,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (!((issued >> i) & 1u)) continue;
                     const uint32_t par = (last_ph >> i) & 1u;
                     const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(smem_u32(&full[i]), par)) {
+                    while (!mbar_try_wait(smem_u32(&full[i]), par) ||
+                           !mbar_try_wait(smem_u32(&sfull[i]), par)) {
                         if (globaltimer_ns() - t0 > kWaitLimitNs) {
                             atomicOr(status, kErrTimeoutDrain);
                             break;
@@ -369,7 +377,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
             const Item x = decode_item(p, it);
             for (int ks = x.ks0; ks < x.ks1; ++ks) {
-                if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag)) {
+                if (!mbar_wait_warp(&sfull[s], ph, status, kErrTimeoutFull, abort_flag)) {
                     ok = false;
                     break;
                 }
