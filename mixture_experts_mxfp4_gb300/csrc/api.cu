@@ -142,10 +142,14 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Looked up once; guarded by its own mutex because it is called while g_mu is
+// held (launch-state construction).
+std::mutex g_encode_mu;
+
 EncodeTiledFn get_encode() {
     static EncodeTiledFn fn = nullptr;
     static bool tried = false;
-    std::lock_guard<std::mutex> lk(g_mu);
+    std::lock_guard<std::mutex> lk(g_encode_mu);
     if (!tried) {
         tried = true;
         void* p = nullptr;
@@ -391,17 +395,36 @@ moe_status_t validate_forward(const void* hidden, const void* w13, const void* w
 
 // The launch sequence of one forward call on the workspace at `base` (at least
 // workspace_bytes of the shape's plan, 256-byte aligned); arguments validated.
-moe_status_t forward_on_workspace(const void* hidden, const void* w13, const void* w13_scale,
-                                  const void* w2, const void* w2_scale, const int32_t* topk_ids,
-                                  const float* topk_weights, void* out, int T, int D, int I, int E,
-                                  int K, void* base, int dev, cudaStream_t stream) {
+}  // namespace moe
+
+namespace {
+
+// Host state of one forward configuration: the plan, both GEMMs' parameters and
+// their eight TMA descriptors.  They depend only on the shape, the weight
+// pointers and the workspace, so they are built once and reused; this keeps
+// the per-call host work to the five launches.
+struct alignas(64) LaunchState {
+    CUtensorMap mA1, mSA1, mB1, mSB1, mA2, mSA2, mB2, mSB2;
+    moe::GemmParams g1, g2;
     moe_mxfp4_plan_t pl;
+    const void* key_ptr[5];
+    int key_shape[5];
+    bool valid;
+};
+
+constexpr int kCacheWays = 4;
+LaunchState g_cache[kMaxDevices][kCacheWays];
+int g_cache_next[kMaxDevices];
+
+bool build_state(LaunchState& st, const void* w13, const void* w13_scale, const void* w2,
+                 const void* w2_scale, int T, int D, int I, int E, int K, void* base) {
+    using namespace moe;
+    moe_mxfp4_plan_t& pl = st.pl;
     fill_plan(T, D, I, E, K, &pl);
     const WsPtrs ws = ws_ptrs(base, pl);
     const int R = T * K;
 
-    // ---------------------------------------------------------- GEMM params
-    GemmParams g1;
+    GemmParams& g1 = st.g1;
     memset(&g1, 0, sizeof(g1));
     g1.ws = ws;
     g1.D = D; g1.I = I; g1.E = E; g1.K = K; g1.R = R;
@@ -411,29 +434,73 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     g1.n_ftiles = I / 64;
     g1.ksplits = pl.stage1_splits;
 
-    GemmParams g2 = g1;
+    GemmParams& g2 = st.g2;
+    g2 = g1;
     gemm_geometry(g2, I, pl.tile_rows, false, 1);
     g2.n_ftiles = D / 128;
     g2.ksplits = 1;
 
-    // ---------------------------------------------------------- TMA maps
-    CUtensorMap mA1, mSA1, mB1, mSB1, mA2, mSA2, mB2, mSB2;
     const int tr = pl.tile_rows;
     bool ok = true;
     // stage 1: A = 64 gate rows + the 64 up rows I rows further, both K-boxes of a stage
-    ok = ok && make_operand_map(&mA1, w13, (uint64_t)E * 2 * I, D, g1.kb, g1.nkt, 64, 2,
+    ok = ok && make_operand_map(&st.mA1, w13, (uint64_t)E * 2 * I, D, g1.kb, g1.nkt, 64, 2,
                                 (uint64_t)I * (D / 2));
-    ok = ok && make_scale_map(&mSA1, w13_scale, (uint64_t)E * 2 * I, D / 32, 64, 2, (uint64_t)I);
-    ok = ok && make_operand_map(&mB1, ws.a1q, pl.cap, D, g1.kb, g1.nkt, tr, 1, 0);
-    ok = ok && make_map(&mSB1, ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, tr,
+    ok = ok && make_scale_map(&st.mSA1, w13_scale, (uint64_t)E * 2 * I, D / 32, 64, 2, (uint64_t)I);
+    ok = ok && make_operand_map(&st.mB1, ws.a1q, pl.cap, D, g1.kb, g1.nkt, tr, 1, 0);
+    ok = ok && make_map(&st.mSB1, ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     // stage 2: A = 128 rows of w2
-    ok = ok && make_operand_map(&mA2, w2, (uint64_t)E * D, I, g2.kb, g2.nkt, 128, 1, 0);
-    ok = ok && make_scale_map(&mSA2, w2_scale, (uint64_t)E * D, I / 32, 128, 1, 0);
-    ok = ok && make_operand_map(&mB2, ws.a2q, pl.cap, I, g2.kb, g2.nkt, tr, 1, 0);
-    ok = ok && make_map(&mSB2, ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, tr,
+    ok = ok && make_operand_map(&st.mA2, w2, (uint64_t)E * D, I, g2.kb, g2.nkt, 128, 1, 0);
+    ok = ok && make_scale_map(&st.mSA2, w2_scale, (uint64_t)E * D, I / 32, 128, 1, 0);
+    ok = ok && make_operand_map(&st.mB2, ws.a2q, pl.cap, I, g2.kb, g2.nkt, tr, 1, 0);
+    ok = ok && make_map(&st.mSB2, ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok) return MOE_ERR_CUDA;
+    return ok;
+}
+
+// Copy of the cached state for this configuration on device `dev` (built on a
+// miss) into *out; false when a tensor map cannot be encoded.
+bool launch_state(int dev, const void* w13, const void* w13_scale, const void* w2,
+                  const void* w2_scale, int T, int D, int I, int E, int K, void* base,
+                  LaunchState* out) {
+    const void* kp[5] = {w13, w13_scale, w2, w2_scale, base};
+    const int ks[5] = {T, D, I, E, K};
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int w = 0; w < kCacheWays; ++w) {
+        const LaunchState& c = g_cache[dev][w];
+        if (c.valid && memcmp(c.key_ptr, kp, sizeof(kp)) == 0 &&
+            memcmp(c.key_shape, ks, sizeof(ks)) == 0) {
+            *out = c;
+            return true;
+        }
+    }
+    LaunchState& st = g_cache[dev][g_cache_next[dev]];
+    g_cache_next[dev] = (g_cache_next[dev] + 1) % kCacheWays;
+    st.valid = false;
+    if (!build_state(st, w13, w13_scale, w2, w2_scale, T, D, I, E, K, base)) return false;
+    memcpy(st.key_ptr, kp, sizeof(kp));
+    memcpy(st.key_shape, ks, sizeof(ks));
+    st.valid = true;
+    *out = st;
+    return true;
+}
+
+}  // namespace
+
+namespace moe {
+
+moe_status_t forward_on_workspace(const void* hidden, const void* w13, const void* w13_scale,
+                                  const void* w2, const void* w2_scale, const int32_t* topk_ids,
+                                  const float* topk_weights, void* out, int T, int D, int I, int E,
+                                  int K, void* base, int dev, cudaStream_t stream) {
+    LaunchState state;
+    if (!launch_state(dev, w13, w13_scale, w2, w2_scale, T, D, I, E, K, base, &state))
+        return MOE_ERR_CUDA;
+    const LaunchState* st = &state;
+    const moe_mxfp4_plan_t& pl = st->pl;
+    const GemmParams& g1 = st->g1;
+    const GemmParams& g2 = st->g2;
+    const WsPtrs& ws = g1.ws;
 
     // ---------------------------------------------------------- launches
     const int sms = num_sms(dev);
@@ -450,10 +517,12 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     mark(1);
     if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
-    if (launch_gemm(1, mA1, mSA1, mB1, mSB1, g1, sms * g1.ctas_per_sm, stream) != cudaSuccess)
+    if (launch_gemm(1, st->mA1, st->mSA1, st->mB1, st->mSB1, g1, sms * g1.ctas_per_sm, stream) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     mark(3);
-    if (launch_gemm(2, mA2, mSA2, mB2, mSB2, g2, sms * g2.ctas_per_sm, stream) != cudaSuccess)
+    if (launch_gemm(2, st->mA2, st->mSA2, st->mB2, st->mSB2, g2, sms * g2.ctas_per_sm, stream) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     mark(4);
     if (launch_reduce(topk_ids, T, K, E, D, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;

@@ -575,9 +575,19 @@ cudaError_t launch_gemm(int stage, const CUtensorMap& tmA, const CUtensorMap& tm
                         const CUtensorMap& tmB, const CUtensorMap& tmSB, const GemmParams& p,
                         int grid, cudaStream_t stream) {
     auto kern = (stage == 1) ? moe_gemm_kernel<1> : moe_gemm_kernel<2>;
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
+    // Raise the dynamic shared-memory limit once per device to the largest size
+    // any configuration asks for.
+    static int limit_set[2][64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (limit_set[stage - 1][dev] < (int)p.smem_bytes) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kGemmSmemLimit);
+        if (err != cudaSuccess) return err;
+        limit_set[stage - 1][dev] = kGemmSmemLimit;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kGemmThreads);

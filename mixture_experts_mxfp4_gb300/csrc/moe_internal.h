@@ -64,6 +64,7 @@ constexpr int kGemmThreads = 384;
 constexpr int kEpiGroups = 2;
 constexpr int kXchgBytes = 4352;     // per epilogue group: 4 KB exchange + flag
 constexpr int kMaxStages = 8;
+constexpr int kGemmSmemLimit = 227 * 1024;  // dynamic shared memory limit set on the GEMMs
 constexpr int kMaxAccBufs = 4;
 
 // Host-side pieces of the forward call shared by its entry points (api.cu).

@@ -172,9 +172,19 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream) {
     const size_t smem = sizeof(int) * ((size_t)kRouteWarps * E + (E + 1) + 64);
-    cudaError_t err = cudaFuncSetAttribute(moe_route_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // limit raised once per device to what E <= 1024 can need
+    static bool limit_set[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!limit_set[dev]) {
+        const int max_smem = (int)(sizeof(int) * ((size_t)kRouteWarps * 1024 + 1025 + 64));
+        err = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   max_smem);
+        if (err != cudaSuccess) return err;
+        limit_set[dev] = true;
+    }
     moe_route_kernel<<<1, kRouteThreads, smem, stream>>>(topk_ids, topk_w, T, K, E, tile_rows,
                                                          cap, n_counters, ws);
     return cudaGetLastError();
