@@ -237,7 +237,9 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int 
 // copies and narrow MMAs leaves the tensor pipe idle between instructions, and a
 // second stream fills it (measured ~2x per SM), while one CTA per SM keeps a
 // deep shared-memory ring to hide the TMA latency.
-void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplits) {
+void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplits,
+                   int mblocks) {
+    g.mblocks = mblocks;
     // Single-stage items (short contraction, e.g. stage 2 at d_inter <= 512):
     // per-item work (tile lookup, barrier round trips) dominates, so two CTAs
     // share each SM.
@@ -252,11 +254,14 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplit
     g.sr_a = S < 16 ? S : 16;
     g.b_scale_x = S >= 16 ? 1 : 0;
     g.tile_rows = tile_rows;
-    const uint32_t a_bytes = 128u * (g.kstage_elems / 2);
+    const uint32_t a_bytes = 128u * mblocks * (g.kstage_elems / 2);
     const uint32_t b_bytes = (uint32_t)tile_rows * (g.kstage_elems / 2);
+    // raw weight scales (128 * mblocks rows of sr_a bytes), rearranged in place
+    uint32_t sa_bytes = 128u * mblocks * (uint32_t)g.sr_a;
+    if (sa_bytes < 2048u) sa_bytes = 2048u;
     g.off_b = a_bytes;
     g.off_sa = g.off_b + b_bytes;
-    g.off_sb = g.off_sa + 2048;
+    g.off_sb = g.off_sa + sa_bytes;
     g.stage_bytes = (uint32_t)round_up(g.off_sb + 2048, 1024);
     const uint32_t xchg = stage1 ? (uint32_t)(kEpiGroups * kXchgBytes) : 0u;
     const uint32_t fixed = 1024 /*align slack*/ + 512 /*barriers*/ + xchg;
@@ -270,21 +275,17 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplit
     // more items in flight between the MMA warps and the epilogue.
     int nb = g.kstages / ksplits <= 2 ? 4 : 2;
     int mw = tile_rows <= 64 ? 2 : 1;
+    // per stage: mblocks + 1 scale-factor atoms (weights, route tile) per K chunk
     auto cols_for = [&](int b, int m, int n) {
-        return (uint32_t)(b * m * tile_rows) + (uint32_t)n * 8u * g.natoms;
+        return (uint32_t)(b * m * mblocks * tile_rows) + (uint32_t)n * (mblocks + 1) * 4u * g.natoms;
     };
     if (cols_for(nb, mw, ns) > tmem_limit) nb = 2;
     if (cols_for(nb, mw, ns) > tmem_limit) mw = 1;
     while (ns > 1 && cols_for(nb, mw, ns) > tmem_limit) --ns;
     // The MMA warps' look-ahead tests slot (g + mw) % ns by parity; that is only
     // unambiguous when the slot's previous stage (g + mw - ns) belonged to the
-    // same warp, i.e. when ns is a multiple of mw.
-    if (mw == 2 && ns % 2 == 1) {
-        if (ns > 2)
-            --ns;
-        else
-            mw = 1;
-    }
+    // same warp, i.e. when ns is a multiple of mw; otherwise it is switched off.
+    g.lookahead = (ns % mw == 0) ? 1 : 0;
     g.mma_warps = mw;
     g.acc_bufs = nb;
     g.num_stages = ns;
@@ -298,7 +299,7 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplit
     uint32_t alloc = 32;
     while (alloc < cols) alloc <<= 1;
     g.tmem_cols = alloc;
-    g.sf_col0 = (uint32_t)(nb * mw * tile_rows);
+    g.sf_col0 = (uint32_t)(nb * mw * mblocks * tile_rows);
 }
 
 int num_sms(int dev) {
@@ -430,14 +431,16 @@ bool build_state(LaunchState& st, const void* w13, const void* w13_scale, const 
     g1.D = D; g1.I = I; g1.E = E; g1.K = K; g1.R = R;
     g1.a1s_stride = pl.a1s_stride;
     g1.a2s_stride = pl.a2s_stride;
-    gemm_geometry(g1, D, pl.tile_rows, true, pl.stage1_splits);
+    gemm_geometry(g1, D, pl.tile_rows, true, pl.stage1_splits, 1);
     g1.n_ftiles = I / 64;
     g1.ksplits = pl.stage1_splits;
 
     GemmParams& g2 = st.g2;
     g2 = g1;
-    gemm_geometry(g2, I, pl.tile_rows, false, 1);
-    g2.n_ftiles = D / 128;
+    // stage 2 on narrow tiles: two 128-row blocks of w2 per item share the route tile
+    const int mb2 = (pl.tile_rows <= 64 && D % 256 == 0) ? 2 : 1;
+    gemm_geometry(g2, I, pl.tile_rows, false, 1, mb2);
+    g2.n_ftiles = D / (128 * mb2);
     g2.ksplits = 1;
 
     const int tr = pl.tile_rows;
@@ -450,8 +453,8 @@ bool build_state(LaunchState& st, const void* w13, const void* w13_scale, const 
     ok = ok && make_map(&st.mSB1, ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     // stage 2: A = 128 rows of w2
-    ok = ok && make_operand_map(&st.mA2, w2, (uint64_t)E * D, I, g2.kb, g2.nkt, 128, 1, 0);
-    ok = ok && make_scale_map(&st.mSA2, w2_scale, (uint64_t)E * D, I / 32, 128, 1, 0);
+    ok = ok && make_operand_map(&st.mA2, w2, (uint64_t)E * D, I, g2.kb, g2.nkt, 128 * g2.mblocks, 1, 0);
+    ok = ok && make_scale_map(&st.mSA2, w2_scale, (uint64_t)E * D, I / 32, 128 * g2.mblocks, 1, 0);
     ok = ok && make_operand_map(&st.mB2, ws.a2q, pl.cap, I, g2.kb, g2.nkt, tr, 1, 0);
     ok = ok && make_map(&st.mSB2, ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);

@@ -205,9 +205,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint8_t* st = smem + (size_t)s * p.stage_bytes;
                     const int kt0 = ks * p.nkt;  // first K box of the stage
-                    const int rg = STAGE == 1 ? x.e * 2 * p.I + x.f * 64 : x.e * p.D + x.f * 128;
+                    const int rg = STAGE == 1 ? x.e * 2 * p.I + x.f * 64
+                                              : x.e * p.D + x.f * 128 * p.mblocks;
+                    const uint32_t arows = 128u * (uint32_t)p.mblocks;
                     // raw scale tiles first, on their own barrier
-                    mbar_arrive_expect_tx(&sfull[s], 128u * p.sr_a + (uint32_t)p.tile_rows * 16u);
+                    mbar_arrive_expect_tx(&sfull[s], arows * p.sr_a + (uint32_t)p.tile_rows * 16u);
                     if (STAGE == 1) {
                         // the 64 gate rows and the 64 matching up rows (I rows further)
                         if (p.a_scale_small)
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tma_load_2d(st + p.off_sb, &tmSB, p.b_scale_x ? ks * 16 : 0, x.row0, &sfull[s]);
                     // weight tile and route tile
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)(128 + p.tile_rows) * kbytes_stage);
+                    mbar_arrive_expect_tx(&full[s], (arows + (uint32_t)p.tile_rows) * kbytes_stage);
                     if (STAGE == 1)
                         tma_load_4d_hint(st, &tmA, 0, rg, 0, kt0, &full[s], pol_w);
                     else
@@ -268,19 +270,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t layout = (p.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
         const uint32_t sbo = 8u * p.kb;
         const int ksteps = p.kstage_elems / 64;
-        const uint32_t a_box = (128u * p.kb) >> 4;              // descriptor units (16 B)
+        const int MB = p.mblocks;
+        const uint32_t a_box = (128u * MB * p.kb) >> 4;         // descriptor units (16 B)
+        const uint32_t a_blk = (128u * p.kb) >> 4;              // next 128-row block
         const uint32_t b_box = ((uint32_t)p.tile_rows * p.kb) >> 4;
-        const uint32_t acc_cols = (uint32_t)(MW * p.tile_rows);  // per accumulator buffer
-        auto sf_cols = [&](int ss) { return tmem_base + p.sf_col0 + (uint32_t)(ss * 8 * p.natoms); };
+        const uint32_t acc_cols = (uint32_t)(MW * MB * p.tile_rows);  // per accumulator buffer
+        const uint32_t sf_stage = (uint32_t)((MB + 1) * 4 * p.natoms);
+        auto sf_cols = [&](int ss) { return tmem_base + p.sf_col0 + (uint32_t)ss * sf_stage; };
         auto copy_scales = [&](int ss) {  // lane 0 only
             uint8_t* st = smem + (size_t)ss * p.stage_bytes;
-            const uint32_t sfa = sf_cols(ss), sfb = sfa + 4u * p.natoms;
+            const uint32_t sfa = sf_cols(ss), sfb = sfa + 4u * MB * p.natoms;
             const uint64_t da = smem_desc(smem_u32(st + p.off_sa), 0, 128, 0);
             const uint64_t db = smem_desc(smem_u32(st + p.off_sb), 0, 128, 0);
-            for (int c = 0; c < p.natoms; ++c) {
-                tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
-                tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
-            }
+            for (int c = 0; c < MB * p.natoms; ++c) tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
+            for (int c = 0; c < p.natoms; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
         };
         auto ready = [&](long gg) -> bool {  // lane 0: stage gg resident and rearranged?
             const int ss = (int)(gg % NS);
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)a * acc_cols + (uint32_t)(w * p.tile_rows);
+            const uint32_t d = tmem_base + (uint32_t)a * acc_cols + (uint32_t)(w * MB * p.tile_rows);
             const uint32_t idesc_even = mxf4_idesc(128, (uint32_t)x.nrows, 0, 0);
             const uint32_t idesc_odd = mxf4_idesc(128, (uint32_t)x.nrows, 2, 2);
             const bool more_items = it + (int)gridDim.x < num_items;
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 // this warp's next stage: in this item, or the first stage of the next
                 const long gn = g + MW;
-                const bool next_exists = (ks + MW < x.ks1) || more_items;
+                const bool next_exists = p.lookahead && ((ks + MW < x.ks1) || more_items);
                 int rd = 0;
                 if (lane == 0 && next_exists) rd = ready(gn) ? 1 : 0;
                 rd = __shfl_sync(0xffffffffu, rd, 0);
@@ -337,16 +340,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint8_t* st = smem + (size_t)s * p.stage_bytes;
                     const uint64_t ad0 = smem_desc(smem_u32(st), 16, sbo, layout);
                     const uint64_t bd0 = smem_desc(smem_u32(st + p.off_b), 16, sbo, layout);
-                    const uint32_t sfa = sf_cols(s), sfb = sfa + 4u * p.natoms;
-                    if (ksteps == 8)
-                        issue_stage_mmas<8, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa,
-                                               sfb, !first);
-                    else if (ksteps == 4)
-                        issue_stage_mmas<4, 4>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa,
-                                               sfb, !first);
-                    else
-                        issue_stage_mmas<2, 2>(d, ad0, bd0, a_box, b_box, idesc_even, idesc_odd, sfa,
-                                               sfb, !first);
+                    const uint32_t sfa = sf_cols(s), sfb = sfa + 4u * MB * p.natoms;
+                    for (int h = 0; h < MB; ++h) {
+                        // block h: its own accumulator columns, A rows and weight scales
+                        const uint32_t dh = d + (uint32_t)(h * p.tile_rows);
+                        const uint64_t adh = ad0 + (uint64_t)(h * a_blk);
+                        const uint32_t sfah = sfa + 4u * (uint32_t)(h * p.natoms);
+                        if (ksteps == 8)
+                            issue_stage_mmas<8, 4>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
+                                                   sfah, sfb, !first);
+                        else if (ksteps == 4)
+                            issue_stage_mmas<4, 4>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
+                                                   sfah, sfb, !first);
+                        else
+                            issue_stage_mmas<2, 2>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
+                                                   sfah, sfb, !first);
+                    }
                     tc_commit(&empty[s]);
                 }
                 __syncwarp();
@@ -382,7 +391,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                sf_to_atoms(st + p.off_sa, p.sr_a, p.natoms, lane);
+                // block h's rows sit at h * 128 * sr_a; its natoms atoms replace them
+                // in place (128 * sr_a == natoms * 512)
+                for (int h = 0; h < p.mblocks; ++h)
+                    sf_to_atoms(st + p.off_sa + h * 128 * p.sr_a, p.sr_a, p.natoms, lane);
                 sf_to_atoms(st + p.off_sb, 16, p.natoms, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -421,8 +433,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t aph = (uint32_t)(local / p.acc_bufs) & 1u;
             if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) break;
             tc_fence_after();
-            const uint32_t tacc =
-                tmem_base + ((q * 32u) << 16) + (uint32_t)(a * MW * p.tile_rows);
+            const int MB = p.mblocks;
+            const uint32_t tacc_item =
+                tmem_base + ((q * 32u) << 16) + (uint32_t)(a * MW * MB * p.tile_rows);
+            uint32_t tacc = tacc_item;  // block 0; stage 2 moves it per block
             const int nchunks = x.nrows / 16;
             // MMA warp w wrote an accumulator for this item iff one of the item's
             // stages g has g % MW == w.
@@ -431,15 +445,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const bool has0 = (MW == 1) || ((gbeg & 1) == 0) || nst > 1;
             // v = sum of the MMA warps' partial accumulators, warp 0's first
             auto load_acc = [&](int c, float (&v)[16]) {
+                // MMA warp 1's accumulator starts MB * tile_rows columns after warp 0's
+                const uint32_t w1off = (uint32_t)(MB * p.tile_rows);
                 if (has0 && has1) {
                     float t[16];
                     tmem_ld16(tacc + 16u * c, v);
-                    tmem_ld16(tacc + (uint32_t)p.tile_rows + 16u * c, t);
+                    tmem_ld16(tacc + w1off + 16u * c, t);
                     tmem_ld_wait();
 #pragma unroll
                     for (int k = 0; k < 16; ++k) v[k] = v[k] + t[k];
                 } else {
-                    tmem_ld16(tacc + (has0 ? 0u : (uint32_t)p.tile_rows) + 16u * c, v);
+                    tmem_ld16(tacc + (has0 ? 0u : w1off) + 16u * c, v);
                     tmem_ld_wait();
                 }
             };
@@ -538,11 +554,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             } else {
-                const int n = x.f * 128 + 32 * (int)q + (int)lane;  // output feature of this lane
+              for (int h = 0; h < MB; ++h) {
+                tacc = tacc_item + (uint32_t)(h * p.tile_rows);
+                // output feature of this lane in block h
+                const int n = (x.f * MB + h) * 128 + 32 * (int)q + (int)lane;
                 for (int c = 0; c < nchunks; ++c) {
                     float v[16];
                     load_acc(c, v);
-                    if (c + 1 == nchunks) {
+                    if (h + 1 == MB && c + 1 == nchunks) {
                         release();
                         released = true;
                     }
@@ -560,6 +579,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (rid < R) p.ws.P[(size_t)rid * p.D + n] = wv * v[i];
                     }
                 }
+              }
             }
             if (!released) release();
         }

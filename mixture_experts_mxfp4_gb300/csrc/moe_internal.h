@@ -49,6 +49,8 @@ struct GemmParams {
     int mma_warps;      // MMA-issuing warps (1 or 2); warp w takes the CTA's stages g % mma_warps == w
     int ctas_per_sm;    // CTAs per SM (1 or 2)
     int acc_bufs;       // TMEM accumulator buffers (items in flight between MMA and epilogue)
+    int mblocks;        // 128-row weight blocks per item sharing one route tile (stage 2: 1 or 2)
+    int lookahead;      // MMA warps copy the next stage's scale factors early (needs ns % mma_warps == 0)
     uint32_t tmem_cols; // TMEM columns allocated
     uint32_t sf_col0;   // first TMEM column of the per-stage scale-factor regions
     uint32_t stage_bytes, off_b, off_sa, off_sb; // per-stage layout (A at 0)
