@@ -134,6 +134,16 @@ const char* moe_mxfp4_status_string(moe_status_t status);
  */
 moe_status_t moe_mxfp4_last_device_status(cudaStream_t stream);
 
+/*
+ * Self-check of device-side failure reporting: enqueue one kernel that waits on
+ * a barrier nothing arrives on, through the same bounded wait the GEMM kernels
+ * use, with a limit of limit_us microseconds (1 .. 1e6).  The wait runs out,
+ * the kernel records the timeout in the registered workspace's status word and
+ * returns; moe_mxfp4_last_device_status then reports MOE_ERR_DEVICE_TIMEOUT and
+ * the next forward call clears the word.  The device stays usable.
+ */
+moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ inspection */
 
 /* Workspace regions, for tests and tools that inspect intermediate results. */

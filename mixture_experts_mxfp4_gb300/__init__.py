@@ -45,6 +45,7 @@ EXPORTS = [
     "moe_mxfp4_kernel_times",
     "moe_mxfp4_last_call_ms",
     "moe_mxfp4_forward_noalloc",
+    "moe_mxfp4_check_wait_timeout",
 ]
 
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
@@ -114,6 +115,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), i]
     lib.moe_mxfp4_last_call_ms.restype = ctypes.c_float
     lib.moe_mxfp4_last_call_ms.argtypes = []
+    lib.moe_mxfp4_check_wait_timeout.restype = i
+    lib.moe_mxfp4_check_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.moe_mxfp4_forward_noalloc.restype = i
     lib.moe_mxfp4_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P]
     _lib = lib
@@ -161,6 +164,11 @@ def forward_noalloc_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_wei
         ctypes.c_void_p(w2), ctypes.c_void_p(w2_scale), ctypes.c_void_p(topk_ids),
         ctypes.c_void_p(topk_weights), ctypes.c_void_p(out), T, d_model, d_inter, E, topk,
         ctypes.c_void_p(stream)))
+
+
+def check_wait_timeout(limit_us: int, stream: int = 0) -> int:
+    """Enqueue the bounded-wait self-check (see include/moe_mxfp4.h); status code."""
+    return int(load_library().moe_mxfp4_check_wait_timeout(int(limit_us), ctypes.c_void_p(stream)))
 
 
 def last_device_status(stream: int = 0) -> int:

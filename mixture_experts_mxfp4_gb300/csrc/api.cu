@@ -567,6 +567,22 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
                                 T, D, I, E, K, base, dev, stream);
 }
 
+moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
+    if (limit_us == 0 || limit_us > 1000000u) return MOE_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void* base;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        base = g_ws[dev].ptr;
+    }
+    if (!base) return MOE_ERR_WORKSPACE;
+    if (launch_check_wait(static_cast<uint32_t*>(base), (uint64_t)limit_us * 1000u, stream) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
 int moe_mxfp4_num_kernels(void) { return kNumKernels; }
 
 moe_status_t moe_mxfp4_set_kernel_timing(int mode) {

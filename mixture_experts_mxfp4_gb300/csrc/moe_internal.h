@@ -80,6 +80,7 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
                                   const float* topk_weights, void* out, int T, int D, int I, int E,
                                   int K, void* base, int dev, cudaStream_t stream);
 
+cudaError_t launch_check_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, int K, int E,
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream);

@@ -19,6 +19,7 @@ enum : uint32_t {
     kErrTimeoutTmemFull = 1u << 2, // epilogue waited for an accumulator
     kErrTimeoutTmemEmpty = 1u << 3,// MMA warp waited for a drained accumulator
     kErrTimeoutDrain = 1u << 4,    // abort path waited for outstanding copies/MMAs
+    kErrSelfCheck = 1u << 5,       // moe_mxfp4_check_wait_timeout's deliberate wait ran out
 };
 
 // A wait gives up after this many nanoseconds of %globaltimer.  Legitimate waits
@@ -44,6 +45,10 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -85,7 +90,8 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // (after recording `err_bit` in *status and setting *abort_flag) when the time
 // limit passes or another thread of the CTA already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                          uint32_t err_bit, volatile int* abort_flag) {
+                                          uint32_t err_bit, volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -93,7 +99,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 atomicOr(status, err_bit);
                 *abort_flag = 1;
                 return false;

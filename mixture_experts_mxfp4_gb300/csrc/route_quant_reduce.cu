@@ -312,4 +312,28 @@ cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, v
                               static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out));
 }
 
+// ============================================================== wait self-check
+//
+// One thread waits on an mbarrier that nothing arrives on, through the same
+// bounded wait the GEMM kernels use, with a short limit: the wait runs out,
+// records kErrSelfCheck in the status word and the kernel returns normally.
+
+__global__ void moe_check_wait_kernel(uint32_t* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    status[0] = 0;
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    const bool ok = mbar_wait(&bar, 0, status, kErrSelfCheck, &abort_flag, limit_ns);
+    if (ok) status[1] = 1;  // cannot happen: nothing arrives
+    mbar_inval(&bar);
+}
+
+cudaError_t launch_check_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream) {
+    moe_check_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 }  // namespace moe

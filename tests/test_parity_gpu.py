@@ -288,3 +288,25 @@ def test_deterministic_repeat(moe):
                        t["topk_ids"], t["topk_weights"])
         torch.cuda.synchronize()
         assert torch.equal(o2.view(torch.int16), ref.view(torch.int16))
+
+
+# ------------------------------------------------------------------ failure reporting
+
+def test_bounded_wait_timeout_is_reported_and_recoverable(moe):
+    """A device wait that runs out (a barrier nothing arrives on, 20 ms limit)
+    is reported as MOE_ERR_DEVICE_TIMEOUT; the next forward clears it."""
+    w = workloads.WORKLOADS[workloads.TINY]
+    inp = workloads.make_inputs(w)
+    m, t, out = run_gpu(moe, inp, w)
+    moe.set_workspace(m.ws_ptr, m.ws_bytes)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert moe.check_wait_timeout(20000, stream) == 0
+    assert moe.last_device_status(stream) == 6  # MOE_ERR_DEVICE_TIMEOUT
+    status = m.region("status", torch.int32, (16,)).cpu().numpy()
+    assert status[0] & (1 << 5)
+    out2 = m.forward(t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"],
+                     t["topk_ids"], t["topk_weights"])
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    assert moe.check_wait_timeout(0, stream) == 1  # limit out of range
