@@ -232,18 +232,17 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int 
     return make_map(m, base, inner, vrows, stride, 16, brows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Pipeline geometry of one GEMM stage for contraction length Kc.  Narrow route
-// tiles (decode) use two MMA-issuing warps: a single stream of scale-factor
-// copies and narrow MMAs leaves the tensor pipe idle between instructions, and a
-// second stream fills it (measured ~2x per SM), while one CTA per SM keeps a
-// deep shared-memory ring to hide the TMA latency.
+// Pipeline geometry of one GEMM stage for contraction length Kc.  A kernel
+// that allocates tensor memory runs one CTA per SM (the occupancy calculator
+// reports 1 for any kernel containing tcgen05.alloc, whatever its threads,
+// registers or shared memory), so each CTA owns the SM's 227 KB of shared
+// memory and 512 TMEM columns.  Narrow route tiles (decode) use two
+// MMA-issuing warps: a single stream of scale-factor copies and narrow MMAs
+// leaves the tensor pipe idle between instructions, and a second stream fills
+// it (measured ~2x per SM).
 void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplits,
                    int mblocks) {
     g.mblocks = mblocks;
-    // Single-stage items (short contraction, e.g. stage 2 at d_inter <= 512):
-    // per-item work (tile lookup, barrier round trips) dominates, so two CTAs
-    // share each SM.
-    g.ctas_per_sm = (!stage1 && Kc <= 512 && tile_rows <= 64) ? 2 : 1;
     g.kstage_elems = Kc >= 512 ? 512 : Kc;
     g.kstages = Kc / g.kstage_elems;
     g.kb = g.kstage_elems >= 256 ? 128 : 64;
@@ -264,12 +263,12 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplit
     g.off_sb = g.off_sa + sa_bytes;
     g.stage_bytes = (uint32_t)round_up(g.off_sb + 2048, 1024);
     const uint32_t xchg = stage1 ? (uint32_t)(kEpiGroups * kXchgBytes) : 0u;
-    const uint32_t fixed = 1024 /*align slack*/ + 512 /*barriers*/ + xchg;
-    // 227 KB of shared memory per SM, split between the CTAs of an SM
-    const uint32_t budget = (g.ctas_per_sm == 2 ? 113u * 1024u : 227u * 1024u) - fixed;
+    const uint32_t tcache = (uint32_t)kTileCache * 16u;
+    const uint32_t fixed = 1024 /*align slack*/ + 512 /*barriers*/ + xchg + tcache;
+    const uint32_t budget = 227u * 1024u - fixed;
     int ns = (int)(budget / g.stage_bytes);
     if (ns > kMaxStages) ns = kMaxStages;
-    const uint32_t tmem_limit = 512u / (uint32_t)g.ctas_per_sm;
+    const uint32_t tmem_limit = 512u;
     // TMEM: acc_bufs accumulator buffers x one accumulator of N columns per MMA
     // warp, plus the per-stage scale factors.  Single-stage items (short K) keep
     // more items in flight between the MMA warps and the epilogue.
@@ -284,17 +283,16 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplit
     while (ns > 1 && cols_for(nb, mw, ns) > tmem_limit) --ns;
     // The MMA warps' look-ahead tests slot (g + mw) % ns by parity; that is only
     // unambiguous when the slot's previous stage (g + mw - ns) belonged to the
-    // same warp, i.e. when ns is a multiple of mw; otherwise it is switched off.
-    g.lookahead = (ns % mw == 0) ? 1 : 0;
+    // same warp, i.e. when ns is a multiple of mw (and ns > mw); otherwise it is
+    // switched off.  Odd ring depths measured faster than trimming to even.
+    g.lookahead = (ns % mw == 0 && ns > mw) ? 1 : 0;
     g.mma_warps = mw;
     g.acc_bufs = nb;
     g.num_stages = ns;
     g.off_bar = (uint32_t)ns * g.stage_bytes;
     g.off_xchg = g.off_bar + 512;  // barriers, TMEM slot and abort flag fit in 512 bytes
-    g.smem_bytes = g.off_xchg + xchg + 1024u;
-    // with one CTA per SM, ask for more than half the SM's shared memory so that
-    // two CTAs never share an SM (and its TMEM)
-    if (g.ctas_per_sm == 1 && g.smem_bytes < 118u * 1024u) g.smem_bytes = 118u * 1024u;
+    g.off_tiles = g.off_xchg + xchg;
+    g.smem_bytes = g.off_tiles + tcache + 1024u;
     const uint32_t cols = cols_for(nb, mw, ns);
     uint32_t alloc = 32;
     while (alloc < cols) alloc <<= 1;
@@ -404,7 +402,7 @@ namespace {
 // their eight TMA descriptors.  They depend only on the shape, the weight
 // pointers and the workspace, so they are built once and reused; this keeps
 // the per-call host work to the five launches.
-struct alignas(64) LaunchState {
+struct LaunchState {
     CUtensorMap mA1, mSA1, mB1, mSB1, mA2, mSA2, mB2, mSB2;
     moe::GemmParams g1, g2;
     moe_mxfp4_plan_t pl;
@@ -520,11 +518,11 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     mark(1);
     if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
-    if (launch_gemm(1, st->mA1, st->mSA1, st->mB1, st->mSB1, g1, sms * g1.ctas_per_sm, stream) !=
+    if (launch_gemm(1, st->mA1, st->mSA1, st->mB1, st->mSB1, g1, sms, stream) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     mark(3);
-    if (launch_gemm(2, st->mA2, st->mSA2, st->mB2, st->mSB2, g2, sms * g2.ctas_per_sm, stream) !=
+    if (launch_gemm(2, st->mA2, st->mSA2, st->mB2, st->mSB2, g2, sms, stream) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     mark(4);

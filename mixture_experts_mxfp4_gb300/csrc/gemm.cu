@@ -44,14 +44,16 @@ struct Item {
     int e, row0, nrows, f, ks0, ks1, unit, split;
 };
 
-__device__ __forceinline__ Item decode_item(const GemmParams& p, int it) {
+// Item `it`: route tile it / (n_ftiles * ksplits), then feature tile, then K
+// split.  The first kTileCache route tiles are read from the shared-memory copy.
+__device__ __forceinline__ Item decode_item(const GemmParams& p, int it, const int4* tcache) {
     Item x;
     const int per_tile = p.n_ftiles * p.ksplits;
     const int tile = it / per_tile;
     const int rem = it - tile * per_tile;
     x.f = rem / p.ksplits;
     x.split = rem - x.f * p.ksplits;
-    const int4 t = p.ws.tiles[tile];
+    const int4 t = tile < kTileCache ? tcache[tile] : __ldcg(p.ws.tiles + tile);
     x.e = t.x;
     x.row0 = t.y;
     x.nrows = t.z;
@@ -100,22 +102,24 @@ __device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, ui
     }
 }
 
-// Issue one stage's MMAs (one thread).  KSTEPS = K-steps of 64 in the stage,
+// Issue KSTEPS of a stage's K-steps of 64, starting at K-step j0 (one thread).
 // SPB = K-steps per TMA box row (4 for 128-byte rows, 2 for 64-byte rows).
 // Descriptors advance by constant offsets: +32 bytes per K-step inside a
-// swizzled row, + one box per SPB steps.
+// swizzled row, + one box per SPB steps; K-step j uses scale-factor atom j / 2
+// and the even/odd scale-factor selector j % 2.
 template <int KSTEPS, int SPB>
 __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, uint64_t bdesc0,
                                                  uint32_t a_box, uint32_t b_box, uint32_t idesc_even,
                                                  uint32_t idesc_odd, uint32_t sfa, uint32_t sfb,
-                                                 bool accumulate) {
+                                                 int j0, bool accumulate) {
 #pragma unroll
-    for (int j = 0; j < KSTEPS; ++j) {
-        const uint32_t kt = (uint32_t)(j / SPB), kk = (uint32_t)(j % SPB);
+    for (int i = 0; i < KSTEPS; ++i) {
+        const uint32_t j = (uint32_t)(j0 + i);
+        const uint32_t kt = j / SPB, kk = j % SPB;
         const uint64_t ad = adesc0 + (uint64_t)(kt * a_box + kk * 2u);
         const uint64_t bd = bdesc0 + (uint64_t)(kt * b_box + kk * 2u);
-        mma_mxf4(d, ad, bd, (j & 1) ? idesc_odd : idesc_even, sfa + 4u * (j >> 1),
-                 sfb + 4u * (j >> 1), (accumulate || j > 0) ? 1u : 0u);
+        mma_mxf4(d, ad, bd, (j & 1u) ? idesc_odd : idesc_even, sfa + 4u * (j >> 1),
+                 sfb + 4u * (j >> 1), (accumulate || i > 0) ? 1u : 0u);
     }
 }
 
@@ -140,8 +144,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* sfull = sfready + kMaxStages;
     uint64_t* tfull = sfull + kMaxStages;
     uint64_t* tempty = tfull + kMaxAccBufs;
-    uint64_t* drain = tempty + kMaxAccBufs;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* drain = tempty + kMaxAccBufs;  // one per MMA warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // per epilogue group: 4 KB exchange buffer, then a flag word
     float* xchg = reinterpret_cast<float*>(smem + p.off_xchg);
@@ -160,7 +164,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tfull[a], (uint32_t)p.mma_warps);
             mbar_init(&tempty[a], 128);
         }
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -173,9 +178,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Everything above overlaps the previous kernel; from here on the kernel
     // reads what earlier kernels wrote, and TMEM is free once they have exited.
     grid_dep_wait();
-    const int num_tiles = p.ws.num_valid[2];
+    const int num_tiles = __ldcg(p.ws.num_valid + 2);
     const int num_items = num_tiles * p.n_ftiles * p.ksplits;
     if ((int)blockIdx.x >= num_items) return;
+    int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
+    for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kGemmThreads)
+        tcache[i] = __ldcg(p.ws.tiles + i);
     if (warp == 2) {
         tmem_alloc(tmem_slot, p.tmem_cols);
         tmem_relinquish();
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t issued = 0;   // bit s: stage s has been filled at least once
             uint32_t last_ph = 0;  // bit s: parity of the last fill of stage s
             for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-                const Item x = decode_item(p, it);
+                const Item x = decode_item(p, it, tcache);
                 for (int ks = x.ks0; ks < x.ks1; ++ks) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, status, kErrTimeoutEmpty, abort_flag)) {
                         ok = false;
@@ -262,9 +270,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ MMA
         // The CTA's stages are numbered g = 0, 1, ... in (item, k-stage) order;
         // MMA warp w issues the stages with g % mma_warps == w into its own
-        // accumulator.  When this warp's next stage is already resident, its
-        // scale factors are copied to TMEM before this stage's MMAs are issued,
-        // so the MMAs never wait on just-issued copies.
+        // accumulator (two instruction streams keep the tensor pipe busy with
+        // narrow MMAs; the epilogue adds the accumulators in a fixed order).
+        // When this warp's next stage is already resident, its scale factors are
+        // copied before this stage's MMAs are issued.  Slot and phase indices
+        // advance incrementally (no division on the per-stage path).
         const int w = (int)warp - 1;
         const int MW = p.mma_warps;
         const uint32_t layout = (p.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
@@ -285,19 +295,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int c = 0; c < MB * p.natoms; ++c) tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
             for (int c = 0; c < p.natoms; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
         };
-        auto ready = [&](long gg) -> bool {  // lane 0: stage gg resident and rearranged?
-            const int ss = (int)(gg % NS);
-            const uint32_t pp = (uint32_t)((gg / NS) & 1);
-            return mbar_test(&full[ss], pp) && mbar_test(&sfready[ss], pp);
+        // this warp's stages: g = w, w + MW, ...; slot s = g % NS, parity ph = (g / NS) & 1
+        auto advance = [&](int& ss, uint32_t& pp) {
+            ss += MW;
+            while (ss >= NS) {
+                ss -= NS;
+                pp ^= 1u;
+            }
         };
-        long g = 0;       // flattened index of the current (item, k-stage)
-        long pre = -1;    // stage whose scale factors are already in TMEM
+        const int my_items = (num_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+        const long g_total = (long)my_items * (p.kstages / p.ksplits);
+        long g = 0;          // index of the current stage in the CTA's sequence
+        int s = w % NS;      // slot of this warp's next stage
+        uint32_t ph = (uint32_t)(w / NS) & 1u;
+        bool pre = false;    // that stage's scale factors are already in TMEM
+        int a = 0;           // accumulator buffer of the current item
+        uint32_t aph = 0;    // and its use parity
         bool ok = true;
-        int local = 0;
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x, ++local) {
-            const Item x = decode_item(p, it);
-            const int a = local % p.acc_bufs;
-            const uint32_t aph = (uint32_t)(local / p.acc_bufs) & 1u;
+        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
+            const Item x = decode_item(p, it, tcache);
             if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
                 ok = false;
                 break;
@@ -306,13 +322,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t d = tmem_base + (uint32_t)a * acc_cols + (uint32_t)(w * MB * p.tile_rows);
             const uint32_t idesc_even = mxf4_idesc(128, (uint32_t)x.nrows, 0, 0);
             const uint32_t idesc_odd = mxf4_idesc(128, (uint32_t)x.nrows, 2, 2);
-            const bool more_items = it + (int)gridDim.x < num_items;
             bool first = true;
             for (int ks = x.ks0; ks < x.ks1; ++ks, ++g) {
-                if ((int)(g % MW) != w) continue;
-                const int s = (int)(g % NS);
-                const uint32_t ph = (uint32_t)((g / NS) & 1);
-                if (pre != g) {
+                if ((int)(g & (MW - 1)) != w) continue;  // MW is 1 or 2
+                if (!pre) {
                     if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
                         !mbar_wait_warp(&sfready[s], ph, status, kErrTimeoutFull, abort_flag)) {
                         ok = false;
@@ -323,18 +336,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         copy_scales(s);
                     }
                 }
-                // this warp's next stage: in this item, or the first stage of the next
-                const long gn = g + MW;
-                const bool next_exists = p.lookahead && ((ks + MW < x.ks1) || more_items);
+                // this warp's next stage g + MW (its slot's previous fill, stage
+                // g + MW - NS, was this warp's when NS % MW == 0)
+                int sn = s;
+                uint32_t pn = ph;
+                advance(sn, pn);
                 int rd = 0;
-                if (lane == 0 && next_exists) rd = ready(gn) ? 1 : 0;
+                if (lane == 0 && p.lookahead && g + MW < g_total)
+                    rd = (mbar_test(&full[sn], pn) && mbar_test(&sfready[sn], pn)) ? 1 : 0;
                 rd = __shfl_sync(0xffffffffu, rd, 0);
-                if (rd) {
-                    if (lane == 0) {
-                        tc_fence_after();
-                        copy_scales((int)(gn % NS));
-                    }
-                    pre = gn;
+                if (rd && lane == 0) {
+                    tc_fence_after();
+                    copy_scales(sn);
                 }
                 if (lane == 0) {
                     uint8_t* st = smem + (size_t)s * p.stage_bytes;
@@ -348,29 +361,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint32_t sfah = sfa + 4u * (uint32_t)(h * p.natoms);
                         if (ksteps == 8)
                             issue_stage_mmas<8, 4>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
-                                                   sfah, sfb, !first);
+                                                   sfah, sfb, 0, !first);
                         else if (ksteps == 4)
                             issue_stage_mmas<4, 4>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
-                                                   sfah, sfb, !first);
+                                                   sfah, sfb, 0, !first);
                         else
                             issue_stage_mmas<2, 2>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
-                                                   sfah, sfb, !first);
+                                                   sfah, sfb, 0, !first);
                     }
                     tc_commit(&empty[s]);
                 }
                 __syncwarp();
+                pre = rd != 0;
+                s = sn;
+                ph = pn;
                 first = false;
             }
             if (!ok) break;
             // every MMA warp arrives once per item (a warp without stages in it too)
             if (lane == 0) tc_commit(&tfull[a]);
             __syncwarp();
+            if (++a == p.acc_bufs) {
+                a = 0;
+                aph ^= 1u;
+            }
         }
         if (!ok && lane == 0) {
-            // Wait for every MMA/copy already issued before TMEM is freed.
-            tc_commit(drain);
+            // Wait for every MMA/copy this warp issued before TMEM is freed.
+            tc_commit(&drain[w]);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(smem_u32(drain), 0)) {
+            while (!mbar_try_wait(smem_u32(&drain[w]), 0)) {
                 if (globaltimer_ns() - t0 > kWaitLimitNs) {
                     atomicOr(status, kErrTimeoutDrain);
                     break;
@@ -384,7 +404,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t ph = 0;
         bool ok = true;
         for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-            const Item x = decode_item(p, it);
+            const Item x = decode_item(p, it, tcache);
             for (int ks = x.ks0; ks < x.ks1; ++ks) {
                 if (!mbar_wait_warp(&sfull[s], ph, status, kErrTimeoutFull, abort_flag)) {
                     ok = false;
@@ -418,19 +438,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int R = p.R;
         const int MW = p.mma_warps;
         int local = 0;
-        int g0 = 0;  // flattened index of the item's first k-stage (as the MMA warps count)
+        int a_next = 0;         // accumulator buffer of the CTA's item `local`
+        uint32_t aph_next = 0;  // and its use parity
+        const int per = p.kstages / p.ksplits;  // stages per item
+        int g0 = 0;             // index of the item's first stage (as the MMA warps count)
         for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++local) {
-            const Item x = decode_item(p, it);
-            const int nst = x.ks1 - x.ks0;
+            const int a = a_next;
+            const uint32_t aph = aph_next;
+            if (++a_next == p.acc_bufs) {
+                a_next = 0;
+                aph_next ^= 1u;
+            }
             const int gbeg = g0;
-            g0 += nst;
+            g0 += per;
             if ((local & (kEpiGroups - 1)) != grp) continue;
+            const Item x = decode_item(p, it, tcache);
             // route metadata of the tile's first 16 slots, fetched before waiting
             const int slot0 = x.row0 + (int)(lane & 15);
             int rid_pre = __ldg(p.ws.sorted_ids + slot0);
             float w_pre = STAGE == 2 ? __ldg(p.ws.sorted_w + slot0) : 0.0f;
-            const int a = local % p.acc_bufs;
-            const uint32_t aph = (uint32_t)(local / p.acc_bufs) & 1u;
             if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) break;
             tc_fence_after();
             const int MB = p.mblocks;
@@ -440,9 +466,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int nchunks = x.nrows / 16;
             // MMA warp w wrote an accumulator for this item iff one of the item's
             // stages g has g % MW == w.
-            bool has1 = false;
-            if (MW == 2) has1 = ((gbeg & 1) == 1) || nst > 1;
-            const bool has0 = (MW == 1) || ((gbeg & 1) == 0) || nst > 1;
+            const int nst = x.ks1 - x.ks0;
+            const bool has1 = MW == 2 && (((gbeg & 1) == 1) || nst > 1);
+            const bool has0 = MW == 1 || ((gbeg & 1) == 0) || nst > 1;
             // v = sum of the MMA warps' partial accumulators, warp 0's first
             auto load_acc = [&](int c, float (&v)[16]) {
                 // MMA warp 1's accumulator starts MB * tile_rows columns after warp 0's

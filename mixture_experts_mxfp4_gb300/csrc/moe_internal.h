@@ -47,14 +47,13 @@ struct GemmParams {
     int b_scale_x;      // 1 when activation scales advance 16 bytes per stage
     int num_stages;     // shared-memory pipeline depth
     int mma_warps;      // MMA-issuing warps (1 or 2); warp w takes the CTA's stages g % mma_warps == w
-    int ctas_per_sm;    // CTAs per SM (1 or 2)
     int acc_bufs;       // TMEM accumulator buffers (items in flight between MMA and epilogue)
     int mblocks;        // 128-row weight blocks per item sharing one route tile (stage 2: 1 or 2)
     int lookahead;      // MMA warps copy the next stage's scale factors early (needs ns % mma_warps == 0)
     uint32_t tmem_cols; // TMEM columns allocated
     uint32_t sf_col0;   // first TMEM column of the per-stage scale-factor regions
     uint32_t stage_bytes, off_b, off_sa, off_sb; // per-stage layout (A at 0)
-    uint32_t off_bar, off_xchg;                  // barriers, epilogue exchange buffer
+    uint32_t off_bar, off_xchg, off_tiles;       // barriers, epilogue exchange buffer, tile cache
     uint32_t smem_bytes;                         // dynamic shared memory requested
     int a2s_stride;
     int a1s_stride;
@@ -68,6 +67,7 @@ constexpr int kXchgBytes = 4352;     // per epilogue group: 4 KB exchange + flag
 constexpr int kMaxStages = 8;
 constexpr int kGemmSmemLimit = 227 * 1024;  // dynamic shared memory limit set on the GEMMs
 constexpr int kMaxAccBufs = 4;
+constexpr int kTileCache = 512;      // route tiles kept in shared memory (the rest read from L2)
 
 // Host-side pieces of the forward call shared by its entry points (api.cu).
 moe_status_t validate_forward(const void* hidden, const void* w13, const void* w13_scale,
