@@ -149,7 +149,7 @@ moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream
 /* Workspace regions, for tests and tools that inspect intermediate results. */
 typedef enum {
     MOE_WS_STATUS = 0,      /* u32 [16]: [0] error bits, [1] where a wait gave up            */
-    MOE_WS_COUNTERS = 1,    /* u32 [counters]: split-K arrival counters (zeroed per call)    */
+    MOE_WS_COUNTERS = 1,    /* u32: split-K arrivals per stage-1 unit, then finished stage-1 units per route tile (zeroed per call) */
     MOE_WS_SORTED_IDS = 2,  /* i32 [cap]: route id t*topk+k per sorted slot, T*topk = padding */
     MOE_WS_SORTED_W = 3,    /* f32 [cap]: topk weight of the slot's route, 0 for padding      */
     MOE_WS_BLOCK_EXPERT = 4,/* i32 [cap/block_m]: expert of each block, -1 unused             */
@@ -190,8 +190,8 @@ const char* moe_mxfp4_version(void);
 
 /* ------------------------------------------------------------------ timing */
 
-/* Number of kernels one forward call launches (route, quant, stage-1 GEMM,
- * stage-2 GEMM, top-k sum). */
+/* Number of kernels one forward call launches (route, quant, the GEMM kernel
+ * that runs both grouped GEMMs, top-k sum). */
 int moe_mxfp4_num_kernels(void);
 
 /*

@@ -51,7 +51,7 @@ EXPORTS = [
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
 STATIC_WORKSPACE_BYTES = 64 << 20
 
-KERNEL_NAMES = ["route", "quant", "gemm_stage1", "gemm_stage2", "topk_sum"]
+KERNEL_NAMES = ["route", "quant", "gemm", "topk_sum"]
 
 
 class MoeError(RuntimeError):

@@ -23,7 +23,7 @@ struct WorkspaceReg {
     size_t bytes = 0;
 };
 
-constexpr int kNumKernels = 5;
+constexpr int kNumKernels = 4;
 
 struct Timing {
     int mode = 0;
@@ -86,7 +86,8 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
             if (kst % s == 0 && s <= (want > 1 ? want : 1)) best = s;
         pl->stage1_splits = pl->tile_rows <= 64 ? best : 1;
     }
-    const size_t n_counters = (size_t)pl->max_tiles * (size_t)(I / 64);
+    // per stage-1 unit (split-K arrivals), then per route tile (finished units)
+    const size_t n_counters = (size_t)pl->max_tiles * (size_t)(I / 64) + (size_t)pl->max_tiles;
     size_t b[MOE_WS_NUM_REGIONS];
     b[MOE_WS_STATUS] = 16 * sizeof(uint32_t);
     b[MOE_WS_COUNTERS] = n_counters * sizeof(uint32_t);
@@ -102,8 +103,9 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     b[MOE_WS_A2Q] = (size_t)cap * (I / 2);
     b[MOE_WS_A2S] = (size_t)cap * pl->a2s_stride;
     b[MOE_WS_P] = (size_t)R * D * 4;
+    const size_t n_units = (size_t)pl->max_tiles * (size_t)(I / 64);
     b[MOE_WS_PARTIAL] = pl->stage1_splits > 1
-                            ? n_counters * (size_t)pl->stage1_splits * pl->tile_rows * 128 * 4
+                            ? n_units * (size_t)pl->stage1_splits * pl->tile_rows * 128 * 4
                             : 0;
     size_t off = 0;
     for (int i = 0; i < MOE_WS_NUM_REGIONS; ++i) {
@@ -114,7 +116,8 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     pl->workspace_bytes = off;
 }
 
-WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl) {
+// n_units: stage-1 units (max_tiles * I / 64); the route-tile counters follow them.
+WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl, size_t n_units) {
     uint8_t* b = static_cast<uint8_t*>(base);
     WsPtrs w;
     w.status = reinterpret_cast<uint32_t*>(b + pl.offset[MOE_WS_STATUS]);
@@ -132,6 +135,7 @@ WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl) {
     w.a2s = b + pl.offset[MOE_WS_A2S];
     w.P = reinterpret_cast<float*>(b + pl.offset[MOE_WS_P]);
     w.partial = reinterpret_cast<float*>(b + pl.offset[MOE_WS_PARTIAL]);
+    w.tile_done = w.counters + n_units;
     return w;
 }
 
@@ -232,55 +236,66 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int 
     return make_map(m, base, inner, vrows, stride, 16, brows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Pipeline geometry of one GEMM stage for contraction length Kc.  A kernel
-// that allocates tensor memory runs one CTA per SM (the occupancy calculator
-// reports 1 for any kernel containing tcgen05.alloc, whatever its threads,
-// registers or shared memory), so each CTA owns the SM's 227 KB of shared
-// memory and 512 TMEM columns.  Narrow route tiles (decode) use two
-// MMA-issuing warps: a single stream of scale-factor copies and narrow MMAs
-// leaves the tensor pipe idle between instructions, and a second stream fills
-// it (measured ~2x per SM).
-void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplits,
-                   int mblocks) {
-    g.mblocks = mblocks;
-    g.kstage_elems = Kc >= 512 ? 512 : Kc;
-    g.kstages = Kc / g.kstage_elems;
-    g.kb = g.kstage_elems >= 256 ? 128 : 64;
-    g.nkt = (g.kstage_elems / 2) / g.kb;
-    g.natoms = g.kstage_elems / 128;
+// Layout of one GEMM stage for contraction length Kc inside a ring slot.
+// Returns the bytes one stage of it occupies.
+uint32_t stage_geometry(StageGeom& q, int Kc, int tile_rows, int mblocks) {
+    q.mblocks = mblocks;
+    q.kstage_elems = Kc >= 512 ? 512 : Kc;
+    q.kstages = Kc / q.kstage_elems;
+    q.kb = q.kstage_elems >= 256 ? 128 : 64;
+    q.nkt = (q.kstage_elems / 2) / q.kb;
+    q.natoms = q.kstage_elems / 128;
     const int S = Kc / 32;
-    g.a_scale_small = S < 16 ? 1 : 0;
-    g.sr_a = S < 16 ? S : 16;
-    g.b_scale_x = S >= 16 ? 1 : 0;
-    g.tile_rows = tile_rows;
-    const uint32_t a_bytes = 128u * mblocks * (g.kstage_elems / 2);
-    const uint32_t b_bytes = (uint32_t)tile_rows * (g.kstage_elems / 2);
+    q.a_scale_small = S < 16 ? 1 : 0;
+    q.sr_a = S < 16 ? S : 16;
+    q.b_scale_x = S >= 16 ? 1 : 0;
+    const uint32_t a_bytes = 128u * mblocks * (q.kstage_elems / 2);
+    const uint32_t b_bytes = (uint32_t)tile_rows * (q.kstage_elems / 2);
     // raw weight scales (128 * mblocks rows of sr_a bytes), rearranged in place
-    uint32_t sa_bytes = 128u * mblocks * (uint32_t)g.sr_a;
+    uint32_t sa_bytes = 128u * mblocks * (uint32_t)q.sr_a;
     if (sa_bytes < 2048u) sa_bytes = 2048u;
-    g.off_b = a_bytes;
-    g.off_sa = g.off_b + b_bytes;
-    g.off_sb = g.off_sa + sa_bytes;
-    g.stage_bytes = (uint32_t)round_up(g.off_sb + 2048, 1024);
-    const uint32_t xchg = stage1 ? (uint32_t)(kEpiGroups * kXchgBytes) : 0u;
+    q.off_b = a_bytes;
+    q.off_sa = q.off_b + b_bytes;
+    q.off_sb = q.off_sa + sa_bytes;
+    return (uint32_t)round_up(q.off_sb + 2048, 1024);
+}
+
+// Geometry of the fused GEMM kernel.  A kernel that allocates tensor memory runs
+// one CTA per SM (the occupancy calculator reports 1 for any kernel containing
+// tcgen05.alloc, whatever its threads, registers or shared memory), so each CTA
+// owns the SM's 227 KB of shared memory and 512 TMEM columns.  The ring slots
+// hold either stage's layout.  Narrow route tiles (decode) use two MMA-issuing
+// warps: a single stream of scale-factor copies and narrow MMAs leaves the
+// tensor pipe idle between instructions, and a second stream fills it.
+void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int ksplits1, int mblocks2) {
+    g.tile_rows = tile_rows;
+    const uint32_t b1 = stage_geometry(g.g[0], D, tile_rows, 1);
+    const uint32_t b2 = stage_geometry(g.g[1], I, tile_rows, mblocks2);
+    g.g[0].n_ftiles = I / 64;
+    g.g[0].ksplits = ksplits1;
+    g.g[1].n_ftiles = D / (128 * mblocks2);
+    g.g[1].ksplits = 1;
+    g.slot_bytes = b1 > b2 ? b1 : b2;
+    const uint32_t xchg = (uint32_t)(kEpiGroups * kXchgBytes);  // stage-1 epilogue
     const uint32_t tcache = (uint32_t)kTileCache * 16u;
     const uint32_t fixed = 1024 /*align slack*/ + 512 /*barriers*/ + xchg + tcache;
     const uint32_t budget = 227u * 1024u - fixed;
-    int ns = (int)(budget / g.stage_bytes);
+    int ns = (int)(budget / g.slot_bytes);
     if (ns > kMaxStages) ns = kMaxStages;
-    const uint32_t tmem_limit = 512u;
-    // TMEM: acc_bufs accumulator buffers x one accumulator of N columns per MMA
-    // warp, plus the per-stage scale factors.  Single-stage items (short K) keep
-    // more items in flight between the MMA warps and the epilogue.
-    int nb = g.kstages / ksplits <= 2 ? 4 : 2;
+    const int mbmax = mblocks2 > 1 ? mblocks2 : 1;
     int mw = tile_rows <= 64 ? 2 : 1;
-    // per stage: mblocks + 1 scale-factor atoms (weights, route tile) per K chunk
+    // TMEM: acc_bufs accumulator buffers of one N-column accumulator per MMA warp
+    // and weight block, plus each ring slot's scale factors ((mblocks + 1) atoms
+    // of 4 columns per 128-element chunk).
+    auto sf_of = [](const StageGeom& q) { return (uint32_t)((q.mblocks + 1) * 4 * q.natoms); };
+    const uint32_t sfc = sf_of(g.g[0]) > sf_of(g.g[1]) ? sf_of(g.g[0]) : sf_of(g.g[1]);
     auto cols_for = [&](int b, int m, int n) {
-        return (uint32_t)(b * m * mblocks * tile_rows) + (uint32_t)n * (mblocks + 1) * 4u * g.natoms;
+        return (uint32_t)(b * m * mbmax * tile_rows) + (uint32_t)n * sfc;
     };
-    if (cols_for(nb, mw, ns) > tmem_limit) nb = 2;
-    if (cols_for(nb, mw, ns) > tmem_limit) mw = 1;
-    while (ns > 1 && cols_for(nb, mw, ns) > tmem_limit) --ns;
+    int nb = 4;
+    if (cols_for(nb, mw, ns) > 512u) nb = 2;
+    if (cols_for(nb, mw, ns) > 512u) mw = 1;
+    while (ns > 1 && cols_for(nb, mw, ns) > 512u) --ns;
     // The MMA warps' look-ahead tests slot (g + mw) % ns by parity; that is only
     // unambiguous when the slot's previous stage (g + mw - ns) belonged to the
     // same warp, i.e. when ns is a multiple of mw (and ns > mw); otherwise it is
@@ -289,7 +304,9 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplit
     g.mma_warps = mw;
     g.acc_bufs = nb;
     g.num_stages = ns;
-    g.off_bar = (uint32_t)ns * g.stage_bytes;
+    g.acc_cols = (uint32_t)(mw * mbmax * tile_rows);
+    g.sf_cols = sfc;
+    g.off_bar = (uint32_t)ns * g.slot_bytes;
     g.off_xchg = g.off_bar + 512;  // barriers, TMEM slot and abort flag fit in 512 bytes
     g.off_tiles = g.off_xchg + xchg;
     g.smem_bytes = g.off_tiles + tcache + 1024u;
@@ -297,7 +314,7 @@ void gemm_geometry(GemmParams& g, int Kc, int tile_rows, bool stage1, int ksplit
     uint32_t alloc = 32;
     while (alloc < cols) alloc <<= 1;
     g.tmem_cols = alloc;
-    g.sf_col0 = (uint32_t)(nb * mw * mblocks * tile_rows);
+    g.sf_col0 = (uint32_t)nb * g.acc_cols;
 }
 
 int num_sms(int dev) {
@@ -403,8 +420,8 @@ namespace {
 // pointers and the workspace, so they are built once and reused; this keeps
 // the per-call host work to the five launches.
 struct LaunchState {
-    CUtensorMap mA1, mSA1, mB1, mSB1, mA2, mSA2, mB2, mSB2;
-    moe::GemmParams g1, g2;
+    CUtensorMap maps[8];  // stage-1 A, SA, B, SB, stage-2 A, SA, B, SB
+    moe::GemmParams gp;
     moe_mxfp4_plan_t pl;
     const void* key_ptr[5];
     int key_shape[5];
@@ -420,41 +437,34 @@ bool build_state(LaunchState& st, const void* w13, const void* w13_scale, const 
     using namespace moe;
     moe_mxfp4_plan_t& pl = st.pl;
     fill_plan(T, D, I, E, K, &pl);
-    const WsPtrs ws = ws_ptrs(base, pl);
-    const int R = T * K;
-
-    GemmParams& g1 = st.g1;
-    memset(&g1, 0, sizeof(g1));
-    g1.ws = ws;
-    g1.D = D; g1.I = I; g1.E = E; g1.K = K; g1.R = R;
-    g1.a1s_stride = pl.a1s_stride;
-    g1.a2s_stride = pl.a2s_stride;
-    gemm_geometry(g1, D, pl.tile_rows, true, pl.stage1_splits, 1);
-    g1.n_ftiles = I / 64;
-    g1.ksplits = pl.stage1_splits;
-
-    GemmParams& g2 = st.g2;
-    g2 = g1;
+    const WsPtrs ws = ws_ptrs(base, pl, (size_t)pl.max_tiles * (size_t)(I / 64));
+    GemmParams& gp = st.gp;
+    memset(&gp, 0, sizeof(gp));
+    gp.ws = ws;
+    gp.D = D; gp.I = I; gp.E = E; gp.K = K; gp.R = T * K;
+    gp.a1s_stride = pl.a1s_stride;
+    gp.a2s_stride = pl.a2s_stride;
     // stage 2 on narrow tiles: two 128-row blocks of w2 per item share the route tile
     const int mb2 = (pl.tile_rows <= 64 && D % 256 == 0) ? 2 : 1;
-    gemm_geometry(g2, I, pl.tile_rows, false, 1, mb2);
-    g2.n_ftiles = D / (128 * mb2);
-    g2.ksplits = 1;
+    gemm_geometry(gp, D, I, pl.tile_rows, pl.stage1_splits, mb2);
+    const StageGeom& q1 = gp.g[0];
+    const StageGeom& q2 = gp.g[1];
 
     const int tr = pl.tile_rows;
+    CUtensorMap* m = st.maps;
     bool ok = true;
     // stage 1: A = 64 gate rows + the 64 up rows I rows further, both K-boxes of a stage
-    ok = ok && make_operand_map(&st.mA1, w13, (uint64_t)E * 2 * I, D, g1.kb, g1.nkt, 64, 2,
+    ok = ok && make_operand_map(&m[0], w13, (uint64_t)E * 2 * I, D, q1.kb, q1.nkt, 64, 2,
                                 (uint64_t)I * (D / 2));
-    ok = ok && make_scale_map(&st.mSA1, w13_scale, (uint64_t)E * 2 * I, D / 32, 64, 2, (uint64_t)I);
-    ok = ok && make_operand_map(&st.mB1, ws.a1q, pl.cap, D, g1.kb, g1.nkt, tr, 1, 0);
-    ok = ok && make_map(&st.mSB1, ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, tr,
+    ok = ok && make_scale_map(&m[1], w13_scale, (uint64_t)E * 2 * I, D / 32, 64, 2, (uint64_t)I);
+    ok = ok && make_operand_map(&m[2], ws.a1q, pl.cap, D, q1.kb, q1.nkt, tr, 1, 0);
+    ok = ok && make_map(&m[3], ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
-    // stage 2: A = 128 rows of w2
-    ok = ok && make_operand_map(&st.mA2, w2, (uint64_t)E * D, I, g2.kb, g2.nkt, 128 * g2.mblocks, 1, 0);
-    ok = ok && make_scale_map(&st.mSA2, w2_scale, (uint64_t)E * D, I / 32, 128 * g2.mblocks, 1, 0);
-    ok = ok && make_operand_map(&st.mB2, ws.a2q, pl.cap, I, g2.kb, g2.nkt, tr, 1, 0);
-    ok = ok && make_map(&st.mSB2, ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, tr,
+    // stage 2: A = 128 * mblocks rows of w2
+    ok = ok && make_operand_map(&m[4], w2, (uint64_t)E * D, I, q2.kb, q2.nkt, 128 * q2.mblocks, 1, 0);
+    ok = ok && make_scale_map(&m[5], w2_scale, (uint64_t)E * D, I / 32, 128 * q2.mblocks, 1, 0);
+    ok = ok && make_operand_map(&m[6], ws.a2q, pl.cap, I, q2.kb, q2.nkt, tr, 1, 0);
+    ok = ok && make_map(&m[7], ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     return ok;
 }
@@ -499,13 +509,12 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
         return MOE_ERR_CUDA;
     const LaunchState* st = &state;
     const moe_mxfp4_plan_t& pl = st->pl;
-    const GemmParams& g1 = st->g1;
-    const GemmParams& g2 = st->g2;
-    const WsPtrs& ws = g1.ws;
+    const GemmParams& gp = st->gp;
+    const WsPtrs& ws = gp.ws;
 
     // ---------------------------------------------------------- launches
     const int sms = num_sms(dev);
-    const int n_counters = pl.max_tiles * (I / 64);
+    const int n_counters = pl.max_tiles * (I / 64) + pl.max_tiles;
     Timing& tm = g_timing[dev];
     const bool timed = tm.enabled && tm.created;
     auto mark = [&](int i) {
@@ -518,16 +527,10 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     mark(1);
     if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(2);
-    if (launch_gemm(1, st->mA1, st->mSA1, st->mB1, st->mSB1, g1, sms, stream) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (launch_gemm(st->maps, gp, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);
-    if (launch_gemm(2, st->mA2, st->mSA2, st->mB2, st->mSB2, g2, sms, stream) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    mark(4);
     if (launch_reduce(topk_ids, T, K, E, D, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    mark(5);
+    mark(4);
     if (timed) tm.recorded = true;
     return MOE_OK;
 }

@@ -1,4 +1,5 @@
-// Grouped block-scaled MXFP4 GEMMs of the MoE forward on tcgen05 tensor cores.
+// Grouped block-scaled MXFP4 GEMMs of the MoE forward on tcgen05 tensor cores,
+// both stages in one persistent kernel.
 //
 // Operand roles (weights on the MMA M side, routes on the N side): for one work
 // item the CTA computes
@@ -18,6 +19,16 @@
 // output; flower_moe.py passes sorted_weights to stage 2): A = 128 rows of w2,
 // the epilogue writes w[route] * y into P[route, :] for the per-token sum.
 //
+// One launch runs both stages: every CTA takes its stage-1 items, then its
+// stage-2 items, through the same shared-memory ring, so stage-2 weight tiles
+// stream in while other CTAs finish stage 1.  A stage-2 item's route tile (the
+// stage-1 output of one route tile) is loaded once every stage-1 feature tile of
+// that route tile has been written: the epilogue that completes a feature tile
+// counts it in tile_done (release), the producer polls the count (acquire,
+// bounded) before it issues the route-tile copy.  Stage-1 work never waits on
+// stage 2 and the grid is one CTA per SM, so every dependency is on work that
+// is already resident.
+//
 // Pipeline (one CTA per SM, persistent over work items):
 //   warp 0  TMA producer: one box each for the weight tile, the route tile and
 //           the two raw scale tiles per stage -> smem ring
@@ -29,7 +40,7 @@
 //   warp 2  also allocates / frees TMEM
 //   warp 3  rearranges each stage's raw scale tiles into the tcgen05
 //           scale-factor layout ahead of the MMA warps
-//   warps 4-7  epilogue: tcgen05.ld of the double-buffered accumulators; the two
+//   warps 4-11  epilogue: two groups of four warps take alternate items; the two
 //           MMA warps' partial accumulators are summed in a fixed order
 // All waits are bounded (ptx.cuh).
 #include <cuda_bf16.h>
@@ -41,26 +52,28 @@
 namespace moe {
 
 struct Item {
-    int e, row0, nrows, f, ks0, ks1, unit, split;
+    int e, row0, nrows, f, ks0, ks1, unit, split, tile;
 };
 
-// Item `it`: route tile it / (n_ftiles * ksplits), then feature tile, then K
-// split.  The first kTileCache route tiles are read from the shared-memory copy.
-__device__ __forceinline__ Item decode_item(const GemmParams& p, int it, const int4* tcache) {
+// Item `it` of a stage: route tile it / (n_ftiles * ksplits), then feature tile,
+// then K split.  The first kTileCache route tiles come from the shared-memory copy.
+__device__ __forceinline__ Item decode_item(const StageGeom& q, const int4* gtiles, int it,
+                                            const int4* tcache) {
     Item x;
-    const int per_tile = p.n_ftiles * p.ksplits;
+    const int per_tile = q.n_ftiles * q.ksplits;
     const int tile = it / per_tile;
     const int rem = it - tile * per_tile;
-    x.f = rem / p.ksplits;
-    x.split = rem - x.f * p.ksplits;
-    const int4 t = tile < kTileCache ? tcache[tile] : __ldcg(p.ws.tiles + tile);
+    x.f = rem / q.ksplits;
+    x.split = rem - x.f * q.ksplits;
+    const int4 t = tile < kTileCache ? tcache[tile] : __ldcg(gtiles + tile);
     x.e = t.x;
     x.row0 = t.y;
     x.nrows = t.z;
-    const int per = p.kstages / p.ksplits;
+    const int per = q.kstages / q.ksplits;
     x.ks0 = x.split * per;
     x.ks1 = x.ks0 + per;
-    x.unit = tile * p.n_ftiles + x.f;
+    x.unit = tile * q.n_ftiles + x.f;
+    x.tile = tile;
     return x;
 }
 
@@ -123,10 +136,12 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, ui
     }
 }
 
-template <int STAGE>
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmSA,
-                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmSB,
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmSA1,
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSB1,
+                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmSA2,
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmSB2,
                     const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -170,17 +185,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmSA);
-        tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmSB);
+        tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmSA1);
+        tma_prefetch_desc(&tmB1);
+        tma_prefetch_desc(&tmSB1);
+        tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmSA2);
+        tma_prefetch_desc(&tmB2);
+        tma_prefetch_desc(&tmSB2);
     }
     // Everything above overlaps the previous kernel; from here on the kernel
     // reads what earlier kernels wrote, and TMEM is free once they have exited.
     grid_dep_wait();
     const int num_tiles = __ldcg(p.ws.num_valid + 2);
-    const int num_items = num_tiles * p.n_ftiles * p.ksplits;
-    if ((int)blockIdx.x >= num_items) return;
+    const int nitems[2] = {num_tiles * p.g[0].n_ftiles * p.g[0].ksplits, num_tiles * p.g[1].n_ftiles};
+    if ((int)blockIdx.x >= nitems[0] && (int)blockIdx.x >= nitems[1]) return;
     int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
     for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kGemmThreads)
         tcache[i] = __ldcg(p.ws.tiles + i);
@@ -192,8 +211,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
-    const int kbytes_stage = p.kstage_elems / 2;  // bytes of one row per stage
+    const int G = (int)gridDim.x;
+    const int b0 = (int)blockIdx.x;
+    // stages of this CTA in both phases (items b0, b0 + G, ... of each stage)
+    auto my_items = [&](int ph) { return b0 < nitems[ph] ? (nitems[ph] - b0 + G - 1) / G : 0; };
+    const long g_total = (long)my_items(0) * (p.g[0].kstages / p.g[0].ksplits) +
+                         (long)my_items(1) * (p.g[1].kstages / p.g[1].ksplits);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -204,47 +227,83 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             uint32_t issued = 0;   // bit s: stage s has been filled at least once
             uint32_t last_ph = 0;  // bit s: parity of the last fill of stage s
-            for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-                const Item x = decode_item(p, it, tcache);
-                for (int ks = x.ks0; ks < x.ks1; ++ks) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, status, kErrTimeoutEmpty, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                    const int kt0 = ks * p.nkt;  // first K box of the stage
-                    const int rg = STAGE == 1 ? x.e * 2 * p.I + x.f * 64
-                                              : x.e * p.D + x.f * 128 * p.mblocks;
-                    const uint32_t arows = 128u * (uint32_t)p.mblocks;
-                    // raw scale tiles first, on their own barrier
-                    mbar_arrive_expect_tx(&sfull[s], arows * p.sr_a + (uint32_t)p.tile_rows * 16u);
-                    if (STAGE == 1) {
-                        // the 64 gate rows and the 64 matching up rows (I rows further)
-                        if (p.a_scale_small)
-                            tma_load_3d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), 0, &sfull[s]);
-                        else
-                            tma_load_3d(st + p.off_sa, &tmSA, ks * 16, rg, 0, &sfull[s]);
-                    } else {
-                        if (p.a_scale_small)
-                            tma_load_2d(st + p.off_sa, &tmSA, 0, rg / (16 / p.sr_a), &sfull[s]);
-                        else
-                            tma_load_2d(st + p.off_sa, &tmSA, ks * 16, rg, &sfull[s]);
-                    }
-                    tma_load_2d(st + p.off_sb, &tmSB, p.b_scale_x ? ks * 16 : 0, x.row0, &sfull[s]);
-                    // weight tile and route tile
-                    mbar_arrive_expect_tx(&full[s], (arows + (uint32_t)p.tile_rows) * kbytes_stage);
-                    if (STAGE == 1)
-                        tma_load_4d_hint(st, &tmA, 0, rg, 0, kt0, &full[s], pol_w);
-                    else
-                        tma_load_3d_hint(st, &tmA, 0, rg, kt0, &full[s], pol_w);
-                    // route tile: tile_rows sorted slots from row0 (rows past the tile's
-                    // own are read but never used; past the end they are zero-filled)
-                    tma_load_3d(st + p.off_b, &tmB, 0, x.row0, kt0, &full[s]);
-                    issued |= 1u << s;
-                    last_ph = (last_ph & ~(1u << s)) | (ph << s);
-                    if (++s == NS) {
-                        s = 0;
-                        ph ^= 1u;
+            int ready_tile = -1;   // last route tile seen complete by stage 1
+            const uint32_t need = (uint32_t)p.g[0].n_ftiles;
+            for (int phs = 0; phs < 2 && ok; ++phs) {
+                const StageGeom& q = p.g[phs];
+                const CUtensorMap* mA = phs ? &tmA2 : &tmA1;
+                const CUtensorMap* mSA = phs ? &tmSA2 : &tmSA1;
+                const CUtensorMap* mB = phs ? &tmB2 : &tmB1;
+                const CUtensorMap* mSB = phs ? &tmSB2 : &tmSB1;
+                const int kbytes_stage = q.kstage_elems / 2;  // bytes of one row per stage
+                const uint32_t arows = 128u * (uint32_t)q.mblocks;
+                for (int it = b0; it < nitems[phs] && ok; it += G) {
+                    const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                    for (int ks = x.ks0; ks < x.ks1; ++ks) {
+                        if (!mbar_wait(&empty[s], ph ^ 1u, status, kErrTimeoutEmpty, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* st = smem + (size_t)s * p.slot_bytes;
+                        const int kt0 = ks * q.nkt;  // first K box of the stage
+                        const int rg = phs == 0 ? x.e * 2 * p.I + x.f * 64
+                                                : x.e * p.D + x.f * 128 * q.mblocks;
+                        // weight scales, then the weight tile: they do not depend on stage 1
+                        mbar_arrive_expect_tx(&sfull[s], arows * q.sr_a + (uint32_t)p.tile_rows * 16u);
+                        mbar_arrive_expect_tx(&full[s], (arows + (uint32_t)p.tile_rows) * kbytes_stage);
+                        if (phs == 0) {
+                            // the 64 gate rows and the 64 matching up rows (I rows further)
+                            if (q.a_scale_small)
+                                tma_load_3d(st + q.off_sa, mSA, 0, rg / (16 / q.sr_a), 0, &sfull[s]);
+                            else
+                                tma_load_3d(st + q.off_sa, mSA, ks * 16, rg, 0, &sfull[s]);
+                            tma_load_4d_hint(st, mA, 0, rg, 0, kt0, &full[s], pol_w);
+                        } else {
+                            if (q.a_scale_small)
+                                tma_load_2d(st + q.off_sa, mSA, 0, rg / (16 / q.sr_a), &sfull[s]);
+                            else
+                                tma_load_2d(st + q.off_sa, mSA, ks * 16, rg, &sfull[s]);
+                            tma_load_3d_hint(st, mA, 0, rg, kt0, &full[s], pol_w);
+                            if (x.tile != ready_tile) {
+                                // the route tile's stage-1 output: every feature tile written
+                                const uint64_t t0 = globaltimer_ns();
+                                bool got = false;
+                                for (uint32_t n = 0;; ++n) {
+                                    if (ld_acquire_gpu(p.ws.tile_done + x.tile) >= need) {
+                                        got = true;
+                                        break;
+                                    }
+                                    if ((n & 63u) == 63u) {
+                                        if (*abort_flag) break;
+                                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                                            atomicOr(status, kErrTimeoutTile);
+                                            *abort_flag = 1;
+                                            break;
+                                        }
+                                    }
+                                }
+                                // the route-tile copies below are issued either way so that
+                                // this stage's barriers complete (on abort they carry stale
+                                // data that is never used)
+                                if (got) {
+                                    fence_proxy_async_global();
+                                    ready_tile = x.tile;
+                                } else {
+                                    ok = false;
+                                }
+                            }
+                        }
+                        // route tile: tile_rows sorted slots from row0 (rows past the tile's
+                        // own are read but never used; past the end they are zero-filled)
+                        tma_load_2d(st + q.off_sb, mSB, q.b_scale_x ? ks * 16 : 0, x.row0, &sfull[s]);
+                        tma_load_3d(st + q.off_b, mB, 0, x.row0, kt0, &full[s]);
+                        issued |= 1u << s;
+                        last_ph = (last_ph & ~(1u << s)) | (ph << s);
+                        if (++s == NS) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        if (!ok) break;
                     }
                 }
             }
@@ -268,34 +327,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (warp == 1 || (warp == 2 && p.mma_warps == 2)) {
         // ------------------------------------------------------------ MMA
-        // The CTA's stages are numbered g = 0, 1, ... in (item, k-stage) order;
-        // MMA warp w issues the stages with g % mma_warps == w into its own
-        // accumulator (two instruction streams keep the tensor pipe busy with
-        // narrow MMAs; the epilogue adds the accumulators in a fixed order).
-        // When this warp's next stage is already resident, its scale factors are
+        // The CTA's stages are numbered g = 0, 1, ... in (stage, item, k-stage)
+        // order; MMA warp w issues the stages with g % mma_warps == w into its
+        // own accumulator (two instruction streams keep the tensor pipe busy with
+        // narrow MMAs; the epilogue adds the accumulators in a fixed order).  When
+        // this warp's next stage is already resident, its scale factors are
         // copied before this stage's MMAs are issued.  Slot and phase indices
         // advance incrementally (no division on the per-stage path).
         const int w = (int)warp - 1;
         const int MW = p.mma_warps;
-        const uint32_t layout = (p.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
-        const uint32_t sbo = 8u * p.kb;
-        const int ksteps = p.kstage_elems / 64;
-        const int MB = p.mblocks;
-        const uint32_t a_box = (128u * MB * p.kb) >> 4;         // descriptor units (16 B)
-        const uint32_t a_blk = (128u * p.kb) >> 4;              // next 128-row block
-        const uint32_t b_box = ((uint32_t)p.tile_rows * p.kb) >> 4;
-        const uint32_t acc_cols = (uint32_t)(MW * MB * p.tile_rows);  // per accumulator buffer
-        const uint32_t sf_stage = (uint32_t)((MB + 1) * 4 * p.natoms);
-        auto sf_cols = [&](int ss) { return tmem_base + p.sf_col0 + (uint32_t)ss * sf_stage; };
-        auto copy_scales = [&](int ss) {  // lane 0 only
-            uint8_t* st = smem + (size_t)ss * p.stage_bytes;
-            const uint32_t sfa = sf_cols(ss), sfb = sfa + 4u * MB * p.natoms;
-            const uint64_t da = smem_desc(smem_u32(st + p.off_sa), 0, 128, 0);
-            const uint64_t db = smem_desc(smem_u32(st + p.off_sb), 0, 128, 0);
-            for (int c = 0; c < MB * p.natoms; ++c) tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
-            for (int c = 0; c < p.natoms; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
-        };
-        // this warp's stages: g = w, w + MW, ...; slot s = g % NS, parity ph = (g / NS) & 1
         auto advance = [&](int& ss, uint32_t& pp) {
             ss += MW;
             while (ss >= NS) {
@@ -303,8 +343,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 pp ^= 1u;
             }
         };
-        const int my_items = (num_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-        const long g_total = (long)my_items * (p.kstages / p.ksplits);
+        auto sf_base = [&](int ss) { return tmem_base + p.sf_col0 + (uint32_t)ss * p.sf_cols; };
         long g = 0;          // index of the current stage in the CTA's sequence
         int s = w % NS;      // slot of this warp's next stage
         uint32_t ph = (uint32_t)(w / NS) & 1u;
@@ -312,78 +351,100 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int a = 0;           // accumulator buffer of the current item
         uint32_t aph = 0;    // and its use parity
         bool ok = true;
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-            const Item x = decode_item(p, it, tcache);
-            if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem_base + (uint32_t)a * acc_cols + (uint32_t)(w * MB * p.tile_rows);
-            const uint32_t idesc_even = mxf4_idesc(128, (uint32_t)x.nrows, 0, 0);
-            const uint32_t idesc_odd = mxf4_idesc(128, (uint32_t)x.nrows, 2, 2);
-            bool first = true;
-            for (int ks = x.ks0; ks < x.ks1; ++ks, ++g) {
-                if ((int)(g & (MW - 1)) != w) continue;  // MW is 1 or 2
-                if (!pre) {
-                    if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
-                        !mbar_wait_warp(&sfready[s], ph, status, kErrTimeoutFull, abort_flag)) {
-                        ok = false;
-                        break;
+        for (int phs = 0; phs < 2 && ok; ++phs) {
+            const StageGeom& q = p.g[phs];
+            const uint32_t layout = (q.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
+            const uint32_t sbo = 8u * q.kb;
+            const int ksteps = q.kstage_elems / 64;
+            const int MB = q.mblocks;
+            const uint32_t a_box = (128u * MB * q.kb) >> 4;  // descriptor units (16 B)
+            const uint32_t a_blk = (128u * q.kb) >> 4;       // next 128-row block
+            const uint32_t b_box = ((uint32_t)p.tile_rows * q.kb) >> 4;
+            // scale copies of slot ss for this stage's layout (lane 0 only); a
+            // look-ahead copy may reach into the next stage's layout
+            auto copy_scales = [&](int ss, const StageGeom& qq) {
+                uint8_t* st = smem + (size_t)ss * p.slot_bytes;
+                const uint32_t sfa = sf_base(ss), sfb = sfa + 4u * qq.mblocks * qq.natoms;
+                const uint64_t da = smem_desc(smem_u32(st + qq.off_sa), 0, 128, 0);
+                const uint64_t db = smem_desc(smem_u32(st + qq.off_sb), 0, 128, 0);
+                for (int c = 0; c < qq.mblocks * qq.natoms; ++c)
+                    tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
+                for (int c = 0; c < qq.natoms; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
+            };
+            const long g_phase_end = g + (long)my_items(phs) * (q.kstages / q.ksplits);
+            for (int it = b0; it < nitems[phs] && ok; it += G) {
+                const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)a * p.acc_cols + (uint32_t)(w * MB * p.tile_rows);
+                const uint32_t idesc_even = mxf4_idesc(128, (uint32_t)x.nrows, 0, 0);
+                const uint32_t idesc_odd = mxf4_idesc(128, (uint32_t)x.nrows, 2, 2);
+                bool first = true;
+                for (int ks = x.ks0; ks < x.ks1; ++ks, ++g) {
+                    if ((int)(g & (MW - 1)) != w) continue;  // MW is 1 or 2
+                    if (!pre) {
+                        if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
+                            !mbar_wait_warp(&sfready[s], ph, status, kErrTimeoutFull, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            tc_fence_after();
+                            copy_scales(s, q);
+                        }
+                    }
+                    // this warp's next stage g + MW (its slot's previous fill, stage
+                    // g + MW - NS, was this warp's when NS % MW == 0)
+                    int sn = s;
+                    uint32_t pn = ph;
+                    advance(sn, pn);
+                    int rd = 0;
+                    if (lane == 0 && p.lookahead && g + MW < g_total)
+                        rd = (mbar_test(&full[sn], pn) && mbar_test(&sfready[sn], pn)) ? 1 : 0;
+                    rd = __shfl_sync(0xffffffffu, rd, 0);
+                    if (rd && lane == 0) {
+                        tc_fence_after();
+                        copy_scales(sn, g + MW < g_phase_end ? q : p.g[1]);
                     }
                     if (lane == 0) {
-                        tc_fence_after();
-                        copy_scales(s);
+                        uint8_t* st = smem + (size_t)s * p.slot_bytes;
+                        const uint64_t ad0 = smem_desc(smem_u32(st), 16, sbo, layout);
+                        const uint64_t bd0 = smem_desc(smem_u32(st + q.off_b), 16, sbo, layout);
+                        const uint32_t sfa = sf_base(s), sfb = sfa + 4u * MB * q.natoms;
+                        for (int h = 0; h < MB; ++h) {
+                            // block h: its own accumulator columns, A rows and weight scales
+                            const uint32_t dh = d + (uint32_t)(h * p.tile_rows);
+                            const uint64_t adh = ad0 + (uint64_t)(h * a_blk);
+                            const uint32_t sfah = sfa + 4u * (uint32_t)(h * q.natoms);
+                            if (ksteps == 8)
+                                issue_stage_mmas<8, 4>(dh, adh, bd0, a_box, b_box, idesc_even,
+                                                       idesc_odd, sfah, sfb, 0, !first);
+                            else if (ksteps == 4)
+                                issue_stage_mmas<4, 4>(dh, adh, bd0, a_box, b_box, idesc_even,
+                                                       idesc_odd, sfah, sfb, 0, !first);
+                            else
+                                issue_stage_mmas<2, 2>(dh, adh, bd0, a_box, b_box, idesc_even,
+                                                       idesc_odd, sfah, sfb, 0, !first);
+                        }
+                        tc_commit(&empty[s]);
                     }
+                    __syncwarp();
+                    pre = rd != 0;
+                    s = sn;
+                    ph = pn;
+                    first = false;
                 }
-                // this warp's next stage g + MW (its slot's previous fill, stage
-                // g + MW - NS, was this warp's when NS % MW == 0)
-                int sn = s;
-                uint32_t pn = ph;
-                advance(sn, pn);
-                int rd = 0;
-                if (lane == 0 && p.lookahead && g + MW < g_total)
-                    rd = (mbar_test(&full[sn], pn) && mbar_test(&sfready[sn], pn)) ? 1 : 0;
-                rd = __shfl_sync(0xffffffffu, rd, 0);
-                if (rd && lane == 0) {
-                    tc_fence_after();
-                    copy_scales(sn);
-                }
-                if (lane == 0) {
-                    uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                    const uint64_t ad0 = smem_desc(smem_u32(st), 16, sbo, layout);
-                    const uint64_t bd0 = smem_desc(smem_u32(st + p.off_b), 16, sbo, layout);
-                    const uint32_t sfa = sf_cols(s), sfb = sfa + 4u * MB * p.natoms;
-                    for (int h = 0; h < MB; ++h) {
-                        // block h: its own accumulator columns, A rows and weight scales
-                        const uint32_t dh = d + (uint32_t)(h * p.tile_rows);
-                        const uint64_t adh = ad0 + (uint64_t)(h * a_blk);
-                        const uint32_t sfah = sfa + 4u * (uint32_t)(h * p.natoms);
-                        if (ksteps == 8)
-                            issue_stage_mmas<8, 4>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
-                                                   sfah, sfb, 0, !first);
-                        else if (ksteps == 4)
-                            issue_stage_mmas<4, 4>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
-                                                   sfah, sfb, 0, !first);
-                        else
-                            issue_stage_mmas<2, 2>(dh, adh, bd0, a_box, b_box, idesc_even, idesc_odd,
-                                                   sfah, sfb, 0, !first);
-                    }
-                    tc_commit(&empty[s]);
-                }
+                if (!ok) break;
+                // every MMA warp arrives once per item (a warp without stages in it too)
+                if (lane == 0) tc_commit(&tfull[a]);
                 __syncwarp();
-                pre = rd != 0;
-                s = sn;
-                ph = pn;
-                first = false;
-            }
-            if (!ok) break;
-            // every MMA warp arrives once per item (a warp without stages in it too)
-            if (lane == 0) tc_commit(&tfull[a]);
-            __syncwarp();
-            if (++a == p.acc_bufs) {
-                a = 0;
-                aph ^= 1u;
+                if (++a == p.acc_bufs) {
+                    a = 0;
+                    aph ^= 1u;
+                }
             }
         }
         if (!ok && lane == 0) {
@@ -403,25 +464,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int it = blockIdx.x; it < num_items && ok; it += gridDim.x) {
-            const Item x = decode_item(p, it, tcache);
-            for (int ks = x.ks0; ks < x.ks1; ++ks) {
-                if (!mbar_wait_warp(&sfull[s], ph, status, kErrTimeoutFull, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* st = smem + (size_t)s * p.stage_bytes;
-                // block h's rows sit at h * 128 * sr_a; its natoms atoms replace them
-                // in place (128 * sr_a == natoms * 512)
-                for (int h = 0; h < p.mblocks; ++h)
-                    sf_to_atoms(st + p.off_sa + h * 128 * p.sr_a, p.sr_a, p.natoms, lane);
-                sf_to_atoms(st + p.off_sb, 16, p.natoms, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sfready[s]);
-                if (++s == NS) {
-                    s = 0;
-                    ph ^= 1u;
+        for (int phs = 0; phs < 2 && ok; ++phs) {
+            const StageGeom& q = p.g[phs];
+            for (int it = b0; it < nitems[phs] && ok; it += G) {
+                const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                for (int ks = x.ks0; ks < x.ks1; ++ks) {
+                    if (!mbar_wait_warp(&sfull[s], ph, status, kErrTimeoutFull, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + (size_t)s * p.slot_bytes;
+                    // block h's rows sit at h * 128 * sr_a; its natoms atoms replace them
+                    // in place (128 * sr_a == natoms * 512)
+                    for (int h = 0; h < q.mblocks; ++h)
+                        sf_to_atoms(st + q.off_sa + h * 128 * q.sr_a, q.sr_a, q.natoms, lane);
+                    sf_to_atoms(st + q.off_sb, 16, q.natoms, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sfready[s]);
+                    if (++s == NS) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
         }
@@ -430,7 +494,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // Two groups of four warps take alternate items, so one item's global
         // traffic overlaps the next item's TMEM reads.  Each group covers the 128
         // TMEM lanes (warp % 4 = lane quadrant).
-        const uint32_t q = warp & 3u;            // TMEM lane quadrant of this warp
+        const uint32_t q4 = warp & 3u;           // TMEM lane quadrant of this warp
         const int grp = (int)(warp - 4) >> 2;    // epilogue group
         const uint32_t bar_id = 1u + (uint32_t)grp;
         float* xg = xchg + grp * (kXchgBytes / 4);
@@ -440,174 +504,188 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int local = 0;
         int a_next = 0;         // accumulator buffer of the CTA's item `local`
         uint32_t aph_next = 0;  // and its use parity
-        const int per = p.kstages / p.ksplits;  // stages per item
         int g0 = 0;             // index of the item's first stage (as the MMA warps count)
-        for (int it = blockIdx.x; it < num_items; it += gridDim.x, ++local) {
-            const int a = a_next;
-            const uint32_t aph = aph_next;
-            if (++a_next == p.acc_bufs) {
-                a_next = 0;
-                aph_next ^= 1u;
-            }
-            const int gbeg = g0;
-            g0 += per;
-            if ((local & (kEpiGroups - 1)) != grp) continue;
-            const Item x = decode_item(p, it, tcache);
-            // route metadata of the tile's first 16 slots, fetched before waiting
-            const int slot0 = x.row0 + (int)(lane & 15);
-            int rid_pre = __ldg(p.ws.sorted_ids + slot0);
-            float w_pre = STAGE == 2 ? __ldg(p.ws.sorted_w + slot0) : 0.0f;
-            if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) break;
-            tc_fence_after();
-            const int MB = p.mblocks;
-            const uint32_t tacc_item =
-                tmem_base + ((q * 32u) << 16) + (uint32_t)(a * MW * MB * p.tile_rows);
-            uint32_t tacc = tacc_item;  // block 0; stage 2 moves it per block
-            const int nchunks = x.nrows / 16;
-            // MMA warp w wrote an accumulator for this item iff one of the item's
-            // stages g has g % MW == w.
-            const int nst = x.ks1 - x.ks0;
-            const bool has1 = MW == 2 && (((gbeg & 1) == 1) || nst > 1);
-            const bool has0 = MW == 1 || ((gbeg & 1) == 0) || nst > 1;
-            // v = sum of the MMA warps' partial accumulators, warp 0's first
-            auto load_acc = [&](int c, float (&v)[16]) {
-                // MMA warp 1's accumulator starts MB * tile_rows columns after warp 0's
-                const uint32_t w1off = (uint32_t)(MB * p.tile_rows);
-                if (has0 && has1) {
-                    float t[16];
-                    tmem_ld16(tacc + 16u * c, v);
-                    tmem_ld16(tacc + w1off + 16u * c, t);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = v[k] + t[k];
-                } else {
-                    tmem_ld16(tacc + (has0 ? 0u : w1off) + 16u * c, v);
-                    tmem_ld_wait();
+        bool ok = true;
+        for (int phs = 0; phs < 2 && ok; ++phs) {
+            const StageGeom& q = p.g[phs];
+            const int per = q.kstages / q.ksplits;  // stages per item
+            const int MB = q.mblocks;
+            for (int it = b0; it < nitems[phs]; it += G, ++local) {
+                const int a = a_next;
+                const uint32_t aph = aph_next;
+                if (++a_next == p.acc_bufs) {
+                    a_next = 0;
+                    aph_next ^= 1u;
                 }
-            };
-            auto release = [&]() {
-                tc_fence_before();
-                mbar_arrive(&tempty[a]);
-            };
-            bool released = false;
-            if (STAGE == 1) {
-                const int n0 = x.f * 64;  // first feature of the tile
-                bool have = true;
-                if (p.ksplits > 1) {
-                    // Split-K: publish this split's partial sums, then the CTA that
-                    // completes the unit's count sums splits 0..S-1 in that order.
-                    float* part = p.ws.partial + (size_t)x.unit * p.ksplits * p.tile_rows * 128;
-                    for (int c = 0; c < nchunks; ++c) {
-                        float v[16];
-                        load_acc(c, v);
-                        if (c + 1 == nchunks) {
-                            release();
-                            released = true;
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            part[((size_t)x.split * p.tile_rows + 16 * c + i) * 128 + 32 * q + lane] = v[i];
-                    }
-                    __threadfence();
-                    named_bar_sync(bar_id, 128);
-                    if (q == 0 && lane == 0) {
-                        const uint32_t prev = atomicAdd(p.ws.counters + x.unit, 1u);
-                        *flag = (prev == (uint32_t)(p.ksplits - 1)) ? 1 : 0;
-                    }
-                    named_bar_sync(bar_id, 128);
-                    have = *flag != 0;
-                    if (have) __threadfence();
+                const int gbeg = g0;
+                g0 += per;
+                if ((local & (kEpiGroups - 1)) != grp) continue;
+                const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                // route metadata of the tile's first 16 slots, fetched before waiting
+                const int slot0 = x.row0 + (int)(lane & 15);
+                int rid_pre = __ldg(p.ws.sorted_ids + slot0);
+                float w_pre = phs == 1 ? __ldg(p.ws.sorted_w + slot0) : 0.0f;
+                if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                if (have) {
-                    const float* part = p.ws.partial + (size_t)x.unit * p.ksplits * p.tile_rows * 128;
-                    for (int c = 0; c < nchunks; ++c) {
-                        float v[16];
-                        if (p.ksplits > 1) {
+                tc_fence_after();
+                const uint32_t tacc_item = tmem_base + ((q4 * 32u) << 16) + (uint32_t)a * p.acc_cols;
+                uint32_t tacc = tacc_item;  // block 0; stage 2 moves it per block
+                const int nchunks = x.nrows / 16;
+                // MMA warp w wrote an accumulator for this item iff one of the item's
+                // stages g has g % MW == w.
+                const int nst = x.ks1 - x.ks0;
+                const bool has1 = MW == 2 && (((gbeg & 1) == 1) || nst > 1);
+                const bool has0 = MW == 1 || ((gbeg & 1) == 0) || nst > 1;
+                // v = sum of the MMA warps' partial accumulators, warp 0's first
+                auto load_acc = [&](int c, float (&v)[16]) {
+                    // MMA warp 1's accumulator starts MB * tile_rows columns after warp 0's
+                    const uint32_t w1off = (uint32_t)(MB * p.tile_rows);
+                    if (has0 && has1) {
+                        float t[16];
+                        tmem_ld16(tacc + 16u * c, v);
+                        tmem_ld16(tacc + w1off + 16u * c, t);
+                        tmem_ld_wait();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                v[i] = __ldcg(part + ((size_t)(16 * c + i)) * 128 + 32 * q + lane);
-                            for (int sp = 1; sp < p.ksplits; ++sp) {
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[i] = v[i] + __ldcg(part + ((size_t)sp * p.tile_rows + 16 * c + i) * 128 +
-                                                         32 * q + lane);
-                            }
-                        } else {
+                        for (int k = 0; k < 16; ++k) v[k] = v[k] + t[k];
+                    } else {
+                        tmem_ld16(tacc + (has0 ? 0u : w1off) + 16u * c, v);
+                        tmem_ld_wait();
+                    }
+                };
+                auto release = [&]() {
+                    tc_fence_before();
+                    mbar_arrive(&tempty[a]);
+                };
+                bool released = false;
+                if (phs == 0) {
+                    const int n0 = x.f * 64;  // first feature of the tile
+                    bool have = true;
+                    if (q.ksplits > 1) {
+                        // Split-K: publish this split's partial sums, then the CTA that
+                        // completes the unit's count sums splits 0..S-1 in that order.
+                        float* part = p.ws.partial + (size_t)x.unit * q.ksplits * p.tile_rows * 128;
+                        for (int c = 0; c < nchunks; ++c) {
+                            float v[16];
                             load_acc(c, v);
                             if (c + 1 == nchunks) {
                                 release();
                                 released = true;
                             }
-                        }
-                        if (q >= 2) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) xg[((q - 2) * 16 + i) * 32 + lane] = v[i];
+                            for (int i = 0; i < 16; ++i)
+                                part[((size_t)x.split * p.tile_rows + 16 * c + i) * 128 + 32 * q4 + lane] = v[i];
+                        }
+                        __threadfence();
+                        named_bar_sync(bar_id, 128);
+                        if (q4 == 0 && lane == 0) {
+                            const uint32_t prev = atomicAdd(p.ws.counters + x.unit, 1u);
+                            *flag = (prev == (uint32_t)(q.ksplits - 1)) ? 1 : 0;
                         }
                         named_bar_sync(bar_id, 128);
-                        if (q < 2) {
-                            const int rid_l =
-                                c == 0 ? rid_pre : __ldg(p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
-                            const int feat = n0 + 32 * (int)q;  // first feature of this warp's block
+                        have = *flag != 0;
+                        if (have) __threadfence();
+                    }
+                    if (have) {
+                        const float* part = p.ws.partial + (size_t)x.unit * q.ksplits * p.tile_rows * 128;
+                        for (int c = 0; c < nchunks; ++c) {
+                            float v[16];
+                            if (q.ksplits > 1) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[i] = __ldcg(part + ((size_t)(16 * c + i)) * 128 + 32 * q4 + lane);
+                                for (int sp = 1; sp < q.ksplits; ++sp) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i)
+                                        v[i] = v[i] + __ldcg(part + ((size_t)sp * p.tile_rows + 16 * c + i) * 128 +
+                                                             32 * q4 + lane);
+                                }
+                            } else {
+                                load_acc(c, v);
+                                if (c + 1 == nchunks) {
+                                    release();
+                                    released = true;
+                                }
+                            }
+                            if (q4 >= 2) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) xg[((q4 - 2) * 16 + i) * 32 + lane] = v[i];
+                            }
+                            named_bar_sync(bar_id, 128);
+                            if (q4 < 2) {
+                                const int rid_l =
+                                    c == 0 ? rid_pre : __ldg(p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
+                                const int feat = n0 + 32 * (int)q4;  // first feature of this warp's block
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const int rid = __shfl_sync(0xffffffffu, rid_l, i);
+                                    if (rid >= R) continue;  // padding slot (warp-uniform)
+                                    const float gv = v[i];
+                                    const float u = xg[(q4 * 16 + i) * 32 + lane];
+                                    const float sg = gv / (1.0f + expf(-gv));
+                                    const float hv = __bfloat162float(__float2bfloat16_rn(sg * u));
+                                    const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
+                                    const uint32_t amax = __reduce_max_sync(0xffffffffu, hb);
+                                    const uint32_t sbyte = mx_scale_byte(amax);
+                                    const uint32_t code =
+                                        e2m1_code(hv, sbyte, mx_inv_scale(sbyte == 255u ? 0u : sbyte));
+                                    const uint32_t nb = __shfl_down_sync(0xffffffffu, code, 1);
+                                    const uint32_t byte = (code | (nb << 4)) & 0xffu;
+                                    const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
+                                    const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
+                                    const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
+                                    const int slot = x.row0 + 16 * c + i;
+                                    if ((lane & 7u) == 0) {
+                                        const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+                                        *reinterpret_cast<uint32_t*>(p.ws.a2q + (size_t)slot * (p.I / 2) +
+                                                                     feat / 2 + lane / 2) = word;
+                                    }
+                                    if (lane == 0)
+                                        p.ws.a2s[(size_t)slot * p.a2s_stride + feat / 32] = (uint8_t)sbyte;
+                                }
+                            }
+                            named_bar_sync(bar_id, 128);
+                        }
+                        // This feature tile of the route tile is written: count it for the
+                        // stage-2 producers, whose TMA copies (async proxy) read it.
+                        fence_proxy_async_global();
+                        named_bar_sync(bar_id, 128);
+                        if (q4 == 0 && lane == 0) {
+                            __threadfence();
+                            atomicAdd(p.ws.tile_done + x.tile, 1u);
+                        }
+                    }
+                } else {
+                    for (int h = 0; h < MB; ++h) {
+                        tacc = tacc_item + (uint32_t)(h * p.tile_rows);
+                        // output feature of this lane in block h
+                        const int n = (x.f * MB + h) * 128 + 32 * (int)q4 + (int)lane;
+                        for (int c = 0; c < nchunks; ++c) {
+                            float v[16];
+                            load_acc(c, v);
+                            if (h + 1 == MB && c + 1 == nchunks) {
+                                release();
+                                released = true;
+                            }
+                            int rid_l = rid_pre;
+                            float w_l = w_pre;
+                            if (c > 0) {
+                                const int sl = x.row0 + 16 * c + (int)(lane & 15);
+                                rid_l = __ldg(p.ws.sorted_ids + sl);
+                                w_l = __ldg(p.ws.sorted_w + sl);
+                            }
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const int rid = __shfl_sync(0xffffffffu, rid_l, i);
-                                if (rid >= R) continue;  // padding slot (warp-uniform)
-                                const float g = v[i];
-                                const float u = xg[(q * 16 + i) * 32 + lane];
-                                const float sg = g / (1.0f + expf(-g));
-                                const float hv = __bfloat162float(__float2bfloat16_rn(sg * u));
-                                const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
-                                const uint32_t amax = __reduce_max_sync(0xffffffffu, hb);
-                                const uint32_t sbyte = mx_scale_byte(amax);
-                                const uint32_t code =
-                                    e2m1_code(hv, sbyte, mx_inv_scale(sbyte == 255u ? 0u : sbyte));
-                                const uint32_t nb = __shfl_down_sync(0xffffffffu, code, 1);
-                                const uint32_t byte = (code | (nb << 4)) & 0xffu;
-                                const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
-                                const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
-                                const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
-                                const int slot = x.row0 + 16 * c + i;
-                                if ((lane & 7u) == 0) {
-                                    const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                                    *reinterpret_cast<uint32_t*>(p.ws.a2q + (size_t)slot * (p.I / 2) +
-                                                                 feat / 2 + lane / 2) = word;
-                                }
-                                if (lane == 0)
-                                    p.ws.a2s[(size_t)slot * p.a2s_stride + feat / 32] = (uint8_t)sbyte;
+                                const float wv = __shfl_sync(0xffffffffu, w_l, i);
+                                if (rid < R) p.ws.P[(size_t)rid * p.D + n] = wv * v[i];
                             }
                         }
-                        named_bar_sync(bar_id, 128);
                     }
                 }
-            } else {
-              for (int h = 0; h < MB; ++h) {
-                tacc = tacc_item + (uint32_t)(h * p.tile_rows);
-                // output feature of this lane in block h
-                const int n = (x.f * MB + h) * 128 + 32 * (int)q + (int)lane;
-                for (int c = 0; c < nchunks; ++c) {
-                    float v[16];
-                    load_acc(c, v);
-                    if (h + 1 == MB && c + 1 == nchunks) {
-                        release();
-                        released = true;
-                    }
-                    int rid_l = rid_pre;
-                    float w_l = w_pre;
-                    if (c > 0) {
-                        const int sl = x.row0 + 16 * c + (int)(lane & 15);
-                        rid_l = __ldg(p.ws.sorted_ids + sl);
-                        w_l = __ldg(p.ws.sorted_w + sl);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int rid = __shfl_sync(0xffffffffu, rid_l, i);
-                        const float wv = __shfl_sync(0xffffffffu, w_l, i);
-                        if (rid < R) p.ws.P[(size_t)rid * p.D + n] = wv * v[i];
-                    }
-                }
-              }
+                if (!released) release();
             }
-            if (!released) release();
         }
     }
 
@@ -617,22 +695,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 2) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-cudaError_t launch_gemm(int stage, const CUtensorMap& tmA, const CUtensorMap& tmSA,
-                        const CUtensorMap& tmB, const CUtensorMap& tmSB, const GemmParams& p,
-                        int grid, cudaStream_t stream) {
-    auto kern = (stage == 1) ? moe_gemm_kernel<1> : moe_gemm_kernel<2>;
-    // Raise the dynamic shared-memory limit once per device to the largest size
-    // any configuration asks for.
-    static int limit_set[2][64];
+cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid, cudaStream_t stream) {
+    // Raise the dynamic shared-memory limit once per device.
+    static bool limit_set[64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (limit_set[stage - 1][dev] < (int)p.smem_bytes) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!limit_set[dev]) {
+        err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kGemmSmemLimit);
         if (err != cudaSuccess) return err;
-        limit_set[stage - 1][dev] = kGemmSmemLimit;
+        limit_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -644,7 +718,8 @@ cudaError_t launch_gemm(int stage, const CUtensorMap& tmA, const CUtensorMap& tm
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmA, tmSA, tmB, tmSB, p);
+    return cudaLaunchKernelEx(&cfg, moe_gemm_kernel, maps[0], maps[1], maps[2], maps[3], maps[4],
+                              maps[5], maps[6], maps[7], p);
 }
 
 }  // namespace moe

@@ -28,15 +28,14 @@ struct WsPtrs {
     uint8_t* a2s;          // [cap][a2s_stride]
     float* P;              // [R][D]
     float* partial;        // split-K partial accumulators
+    uint32_t* tile_done;   // [max_tiles]: stage-1 feature tiles completed per route tile
 };
 
-// Parameters of one grouped block-scaled GEMM launch (stage 1 or stage 2).
-struct GemmParams {
-    WsPtrs ws;
-    int D, I, E, K, R;
-    int tile_rows;      // maximum MMA N (routes per tile), multiple of 16, <= 128
-    int n_ftiles;       // stage 1: I / 64 feature tiles; stage 2: D / 128 output tiles
-    int ksplits;        // stage-1 K splits (1 = none)
+// Geometry of one grouped block-scaled GEMM stage (stage 1: gate_up, K = D;
+// stage 2: down, K = I) inside the fused GEMM kernel.
+struct StageGeom {
+    int n_ftiles;       // stage 1: I / 64 feature tiles; stage 2: D / (128 * mblocks) output tiles
+    int ksplits;        // K splits (stage 2: 1)
     int kstages;        // K / kstage_elems
     int kstage_elems;   // K elements per pipeline stage: 128, 256 or 512
     int kb;             // bytes per row of one TMA box along K: 64 or 128
@@ -45,16 +44,28 @@ struct GemmParams {
     int sr_a;           // bytes per raw weight-scale row in shared memory: 4, 8 or 16
     int a_scale_small;  // weight scales read through a [rows*S/16, 16] view
     int b_scale_x;      // 1 when activation scales advance 16 bytes per stage
-    int num_stages;     // shared-memory pipeline depth
+    int mblocks;        // 128-row weight blocks per item sharing one route tile
+    uint32_t off_b, off_sa, off_sb;  // route tile and raw scale tiles within a ring slot (A at 0)
+};
+
+// Parameters of the fused GEMM launch: every CTA runs its stage-1 items, then
+// its stage-2 items, through one shared-memory ring.
+struct GemmParams {
+    WsPtrs ws;
+    int D, I, E, K, R;
+    int tile_rows;      // maximum MMA N (routes per tile), multiple of 16, <= 128
+    StageGeom g[2];     // stage 1, stage 2
+    int num_stages;     // shared-memory ring depth
     int mma_warps;      // MMA-issuing warps (1 or 2); warp w takes the CTA's stages g % mma_warps == w
     int acc_bufs;       // TMEM accumulator buffers (items in flight between MMA and epilogue)
-    int mblocks;        // 128-row weight blocks per item sharing one route tile (stage 2: 1 or 2)
     int lookahead;      // MMA warps copy the next stage's scale factors early (needs ns % mma_warps == 0)
-    uint32_t tmem_cols; // TMEM columns allocated
-    uint32_t sf_col0;   // first TMEM column of the per-stage scale-factor regions
-    uint32_t stage_bytes, off_b, off_sa, off_sb; // per-stage layout (A at 0)
-    uint32_t off_bar, off_xchg, off_tiles;       // barriers, epilogue exchange buffer, tile cache
-    uint32_t smem_bytes;                         // dynamic shared memory requested
+    uint32_t slot_bytes;  // bytes per ring slot (the larger stage layout)
+    uint32_t acc_cols;    // TMEM columns per accumulator buffer
+    uint32_t sf_cols;     // TMEM scale-factor columns per ring slot
+    uint32_t tmem_cols;   // TMEM columns allocated
+    uint32_t sf_col0;     // first TMEM column of the per-slot scale-factor regions
+    uint32_t off_bar, off_xchg, off_tiles;  // barriers, epilogue exchange buffer, tile cache
+    uint32_t smem_bytes;                    // dynamic shared memory requested
     int a2s_stride;
     int a1s_stride;
 };
@@ -88,8 +99,8 @@ cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride
                          const WsPtrs& ws, cudaStream_t stream);
 cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
                           const WsPtrs& ws, cudaStream_t stream);
-cudaError_t launch_gemm(int stage, const CUtensorMap& tmA, const CUtensorMap& tmSA,
-                        const CUtensorMap& tmB, const CUtensorMap& tmSB, const GemmParams& p,
-                        int grid, cudaStream_t stream);
+// maps: stage-1 A, SA, B, SB, then stage-2 A, SA, B, SB
+cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
+                        cudaStream_t stream);
 
 }  // namespace moe

@@ -20,6 +20,7 @@ enum : uint32_t {
     kErrTimeoutTmemEmpty = 1u << 3,// MMA warp waited for a drained accumulator
     kErrTimeoutDrain = 1u << 4,    // abort path waited for outstanding copies/MMAs
     kErrSelfCheck = 1u << 5,       // moe_mxfp4_check_wait_timeout's deliberate wait ran out
+    kErrTimeoutTile = 1u << 6,     // stage-2 producer waited for a stage-1 route tile
 };
 
 // A wait gives up after this many nanoseconds of %globaltimer.  Legitimate waits
@@ -144,6 +145,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, u
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy global accesses with its later async-proxy
+// (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
