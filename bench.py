@@ -92,7 +92,7 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic():
-    """DRAM bytes per stage-1 launch from the committed ncu summary, or None when
+    """DRAM bytes per GEMM-kernel launch from the committed ncu summary, or None when
     the summary is missing or the kernel sources changed since it was taken."""
     try:
         text = open(PROFILE_SUMMARY).read()
