@@ -72,20 +72,9 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     pl->a1s_stride = (int)round_up((size_t)(D / 32), 16);
     pl->a2s_stride = (int)round_up((size_t)(I / 32), 16);
     pl->max_tiles = (int)(cap / kBlockM);
-    // Stage-1 K splits: decode batches have few (expert, feature-tile) units per
-    // SM, so the contraction over d_model is split and summed by the last CTA.
-    // Stage-1 K splits: decode batches have few (expert, feature-tile) units per
-    // SM, so the contraction over d_model is split and summed by the last CTA.
-    // (Finer splits measured slower: the split-K epilogue costs per item.)
-    {
-        const int kst = D >= 512 ? D / 512 : 1;
-        const double units = (double)(used < E ? used : E) * (I / 64);
-        int want = (int)(4.0 * 304.0 / (units > 1 ? units : 1));
-        int best = 1;
-        for (int s = 1; s <= kst && s <= 8; ++s)
-            if (kst % s == 0 && s <= (want > 1 ? want : 1)) best = s;
-        pl->stage1_splits = pl->tile_rows <= 64 ? best : 1;
-    }
+    // No K split of stage 1: the GEMM kernel evens out its CTAs' work with the
+    // distribution of stage-2 items instead.
+    pl->stage1_splits = 1;
     // per stage-1 unit (split-K arrivals), then per route tile (finished units)
     const size_t n_counters = (size_t)pl->max_tiles * (size_t)(I / 64) + (size_t)pl->max_tiles;
     size_t b[MOE_WS_NUM_REGIONS];

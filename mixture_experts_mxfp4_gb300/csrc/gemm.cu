@@ -21,7 +21,10 @@
 //
 // One launch runs both stages: every CTA takes its stage-1 items, then its
 // stage-2 items, through the same shared-memory ring, so stage-2 weight tiles
-// stream in while other CTAs finish stage 1.  A stage-2 item's route tile (the
+// stream in while other CTAs finish stage 1.  Stage-1 items go round-robin, so
+// the CTAs from n1 % G on have one item fewer; the first stage-2 items go
+// round-robin over those CTAs only (as many as one stage-1 item is worth), the
+// rest round-robin over all CTAs, which evens out the CTAs' work.  A stage-2 item's route tile (the
 // stage-1 output of one route tile) is loaded once every stage-1 feature tile of
 // that route tile has been written: the epilogue that completes a feature tile
 // counts it in tile_done (release), the producer polls the count (acquire,
@@ -199,7 +202,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     grid_dep_wait();
     const int num_tiles = __ldcg(p.ws.num_valid + 2);
     const int nitems[2] = {num_tiles * p.g[0].n_ftiles * p.g[0].ksplits, num_tiles * p.g[1].n_ftiles};
-    if ((int)blockIdx.x >= nitems[0] && (int)blockIdx.x >= nitems[1]) return;
+    const int G = (int)gridDim.x;
+    const int b0 = (int)blockIdx.x;
+    // stage-2 schedule: items [0, X) round-robin over the L CTAs with one stage-1
+    // item fewer (r1 = n1 % G on), items [X, n2) round-robin over all CTAs.  A
+    // stage-2 item (per2 stages) costs about 1.5 stage-1 stages (measured: its
+    // narrower MMAs and P epilogue), so one stage-1 item is worth 2*per1/(3*per2)
+    // stage-2 items.
+    const int per1 = p.g[0].kstages / p.g[0].ksplits, per2 = p.g[1].kstages;
+    const int r1 = nitems[0] % G;
+    const int L = r1 > 0 ? G - r1 : 0;
+    const int X = min(L * ((2 * per1) / (3 * per2)), nitems[1]);
+    const int seg1 = (L > 0 && b0 >= r1 && X > b0 - r1) ? (X - (b0 - r1) + L - 1) / L : 0;
+    const int my_items0 = b0 < nitems[0] ? (nitems[0] - b0 + G - 1) / G : 0;
+    const int my_items1 = seg1 + (X + b0 < nitems[1] ? (nitems[1] - X - b0 + G - 1) / G : 0);
+    // m-th item of this CTA in stage phs, or -1
+    auto item_of = [&](int phs, int m) -> int {
+        if (phs == 0) {
+            const int j = b0 + m * G;
+            return j < nitems[0] ? j : -1;
+        }
+        if (m < seg1) return (b0 - r1) + m * L;
+        const int j = X + b0 + (m - seg1) * G;
+        return j < nitems[1] ? j : -1;
+    };
+    if (my_items0 == 0 && my_items1 == 0) return;
     int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
     for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kGemmThreads)
         tcache[i] = __ldcg(p.ws.tiles + i);
@@ -211,12 +238,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int G = (int)gridDim.x;
-    const int b0 = (int)blockIdx.x;
-    // stages of this CTA in both phases (items b0, b0 + G, ... of each stage)
-    auto my_items = [&](int ph) { return b0 < nitems[ph] ? (nitems[ph] - b0 + G - 1) / G : 0; };
-    const long g_total = (long)my_items(0) * (p.g[0].kstages / p.g[0].ksplits) +
-                         (long)my_items(1) * (p.g[1].kstages / p.g[1].ksplits);
+    // stages of this CTA in both phases
+    const long g_total = (long)my_items0 * per1 + (long)my_items1 * per2;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -237,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const CUtensorMap* mSB = phs ? &tmSB2 : &tmSB1;
                 const int kbytes_stage = q.kstage_elems / 2;  // bytes of one row per stage
                 const uint32_t arows = 128u * (uint32_t)q.mblocks;
-                for (int it = b0; it < nitems[phs] && ok; it += G) {
+                for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                     const Item x = decode_item(q, p.ws.tiles, it, tcache);
                     for (int ks = x.ks0; ks < x.ks1; ++ks) {
                         if (!mbar_wait(&empty[s], ph ^ 1u, status, kErrTimeoutEmpty, abort_flag)) {
@@ -371,8 +394,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
                 for (int c = 0; c < qq.natoms; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
             };
-            const long g_phase_end = g + (long)my_items(phs) * (q.kstages / q.ksplits);
-            for (int it = b0; it < nitems[phs] && ok; it += G) {
+            const long g_phase_end = g + (long)(phs == 0 ? my_items0 : my_items1) * (q.kstages / q.ksplits);
+            for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
                     ok = false;
@@ -466,7 +489,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         for (int phs = 0; phs < 2 && ok; ++phs) {
             const StageGeom& q = p.g[phs];
-            for (int it = b0; it < nitems[phs] && ok; it += G) {
+            for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 for (int ks = x.ks0; ks < x.ks1; ++ks) {
                     if (!mbar_wait_warp(&sfull[s], ph, status, kErrTimeoutFull, abort_flag)) {
@@ -510,7 +533,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const StageGeom& q = p.g[phs];
             const int per = q.kstages / q.ksplits;  // stages per item
             const int MB = q.mblocks;
-            for (int it = b0; it < nitems[phs]; it += G, ++local) {
+            for (int m = 0, it = item_of(phs, 0); it >= 0; it = item_of(phs, ++m), ++local) {
                 const int a = a_next;
                 const uint32_t aph = aph_next;
                 if (++a_next == p.acc_bufs) {
