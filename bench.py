@@ -248,6 +248,10 @@ def run_gpu(args, w, world, rank, local):
     fargs = (t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"], t["topk_ids"],
              t["topk_weights"])
 
+    # launch mode: the library's automatic choice unless forced
+    moe.set_single_launch({"auto": 2, "single": 1, "separate": 0}[args.launch])
+    launches = moe.call_launches(w.T, w.D, w.I, w.E, w.K)
+    single = launches == 2
     moe.set_kernel_timing(2)
     for _ in range(args.warmup):
         flush.zero_()
@@ -349,7 +353,9 @@ def run_gpu(args, w, world, rank, local):
         "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_inter": w.I, "E": w.E,
                    "topk": w.K, "touched_experts": e_touched,
                    "l2": "flushed before every step (256 MiB write, untimed)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "launch": "single (routing + quantisation inside the GEMM kernel)"
+                   if single else "separate kernels"},
         "us_per_call": us_call,
         "per_kernel_us": {n: 1e3 * v / k_steps for n, v in per_kernel.items()},
         "per_kernel_note": f"{k_steps} steps with events between kernels (serialised)",
@@ -359,7 +365,7 @@ def run_gpu(args, w, world, rank, local):
                              "peak": peak, "unit": "GB/s", "frac": fwd_gbs / peak},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": moe.load_library().moe_mxfp4_num_kernels() * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clk,
     }
     if w.name in PUBLISHED_US:
@@ -378,6 +384,9 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", default="auto", choices=["auto", "single", "separate"],
+                    help="single: route and quantise inside the GEMM kernel (2 launches per "
+                         "call); separate: 4 kernels; auto: the library's choice by shape")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -63,9 +63,15 @@ size_t moe_mxfp4_workspace_size(int T, int d_model, int d_inter, int E, int topk
 
 /*
  * Register the caller-owned device workspace for the current CUDA device.
- * dev_ptr must be 256-byte aligned; bytes its size.  Passing NULL unregisters.
- * The library keeps the pointer, never frees it.  Not thread-safe with
- * concurrent forward calls on the same device.
+ * dev_ptr must be 256-byte aligned; bytes its size (at least 4096).  Passing
+ * NULL unregisters.  The library keeps the pointer, never frees it, and does
+ * no device work here (registering the same buffer again is free).  Not
+ * thread-safe with concurrent forward calls on the same device.
+ * The first 4096 bytes (region MOE_WS_STATUS) must be zero when a buffer is
+ * first used (e.g. allocate it zero-filled or cudaMemset it); the forward
+ * calls keep them so.  The rest needs no initialisation.  A kernel that finds
+ * a counter there already past its target reports MOE_ERR_DEVICE_TIMEOUT
+ * through moe_mxfp4_last_device_status (status bit 8).
  */
 moe_status_t moe_mxfp4_set_workspace(void* dev_ptr, size_t bytes);
 
@@ -148,8 +154,8 @@ moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream
 
 /* Workspace regions, for tests and tools that inspect intermediate results. */
 typedef enum {
-    MOE_WS_STATUS = 0,      /* u32 [16]: [0] error bits, [1] where a wait gave up            */
-    MOE_WS_COUNTERS = 1,    /* u32: split-K arrivals per stage-1 unit, then finished stage-1 units per route tile (zeroed per call) */
+    MOE_WS_STATUS = 0,      /* u32 [1024]: [0] error bits; [15], [16], [512..1024) the single-launch path's ready word, quantisation count and route-tile counters (zero between calls) */
+    MOE_WS_COUNTERS = 1,    /* u32 [max_tiles]: finished stage-1 feature tiles per route tile (multi-kernel path; zeroed per call) */
     MOE_WS_SORTED_IDS = 2,  /* i32 [cap]: route id t*topk+k per sorted slot, T*topk = padding */
     MOE_WS_SORTED_W = 3,    /* f32 [cap]: topk weight of the slot's route, 0 for padding      */
     MOE_WS_BLOCK_EXPERT = 4,/* i32 [cap/block_m]: expert of each block, -1 unused             */
@@ -162,7 +168,7 @@ typedef enum {
     MOE_WS_A2Q = 11,        /* u8 [cap][d_inter/2]: quantised SwiGLU output of each slot      */
     MOE_WS_A2S = 12,        /* u8 [cap][a2s_stride]: its e8m0 scales                          */
     MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id    */
-    MOE_WS_PARTIAL = 14,    /* f32: split-K partial accumulators of stage 1                   */
+    MOE_WS_PARTIAL = 14,    /* unused (0 bytes): no K split of stage 1                        */
     MOE_WS_NUM_REGIONS = 15
 } moe_ws_region_t;
 
@@ -172,7 +178,7 @@ typedef struct {
     int cap;            /* slots in the sorted arrays                                    */
     int a1s_stride;     /* bytes per row of MOE_WS_A1S                                   */
     int a2s_stride;     /* bytes per row of MOE_WS_A2S                                   */
-    int stage1_splits;  /* K splits of the stage-1 GEMM                                  */
+    int stage1_splits;  /* K splits of the stage-1 GEMM (1)                              */
     int max_tiles;      /* capacity of MOE_WS_TILES                                      */
     int reserved;
     size_t offset[MOE_WS_NUM_REGIONS]; /* byte offset of each region in the workspace     */
@@ -190,9 +196,34 @@ const char* moe_mxfp4_version(void);
 
 /* ------------------------------------------------------------------ timing */
 
-/* Number of kernels one forward call launches (route, quant, the GEMM kernel
- * that runs both grouped GEMMs, top-k sum). */
+/* Number of kernel slots of a forward call (route, quant, the GEMM kernel that
+ * runs both grouped GEMMs, top-k sum).  In single-launch mode the route and
+ * quant slots are empty: routing and quantisation run inside the GEMM kernel. */
 int moe_mxfp4_num_kernels(void);
+
+/*
+ * Launch mode for the current device (the single launch follows the fused
+ * FC1 -> activation -> FC2 persistent launch of b12x moe/fused/w4a16/kernel.py,
+ * where one grid runs every step).  In a single launch, shapes with
+ * T*topk <= 2048 and E <= 384 route and quantise inside the GEMM kernel: every
+ * CTA sorts all routes in shared memory and quantises a share of the hidden
+ * states, and the stage-1 route-tile copies wait (bounded) until all CTAs have
+ * counted their share; only the GEMM kernel and the top-k sum are launched.
+ * Otherwise: routing kernel, quantisation kernel, GEMM kernel, top-k sum.
+ *   mode 0: always separate kernels;
+ *   mode 1: single launch wherever the shape allows;
+ *   mode 2 (default): single launch for decode-sized calls (T*topk <= 256),
+ *           where it measured faster; separate kernels above.
+ * Results are identical in every mode.  Returns MOE_ERR_INVALID_ARG for other
+ * modes.
+ */
+moe_status_t moe_mxfp4_set_single_launch(int mode);
+
+/* Kernels a forward call of this shape launches on the current device under its
+ * launch mode: 4 (route, quant, GEMM, top-k sum), 2 (GEMM with routing and
+ * quantisation inside, top-k sum), 0 for T = 0, -1 for an invalid shape or no
+ * device. */
+int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk);
 
 /*
  * Optional instrumentation for benchmarks (events created once per device on

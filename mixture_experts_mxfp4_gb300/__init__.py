@@ -46,6 +46,8 @@ EXPORTS = [
     "moe_mxfp4_last_call_ms",
     "moe_mxfp4_forward_noalloc",
     "moe_mxfp4_check_wait_timeout",
+    "moe_mxfp4_set_single_launch",
+    "moe_mxfp4_call_launches",
 ]
 
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
@@ -111,6 +113,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_num_kernels.argtypes = []
     lib.moe_mxfp4_set_kernel_timing.restype = i
     lib.moe_mxfp4_set_kernel_timing.argtypes = [i]
+    lib.moe_mxfp4_set_single_launch.restype = i
+    lib.moe_mxfp4_set_single_launch.argtypes = [i]
+    lib.moe_mxfp4_call_launches.restype = i
+    lib.moe_mxfp4_call_launches.argtypes = [i, i, i, i, i]
     lib.moe_mxfp4_kernel_times.restype = i
     lib.moe_mxfp4_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), i]
     lib.moe_mxfp4_last_call_ms.restype = ctypes.c_float
@@ -175,6 +181,17 @@ def last_device_status(stream: int = 0) -> int:
     return int(load_library().moe_mxfp4_last_device_status(ctypes.c_void_p(stream)))
 
 
+def set_single_launch(mode):
+    """Launch mode: 0 separate kernels; 1 route and quantise inside the GEMM kernel
+    wherever the shape allows; 2 (default) single launch for decode-sized calls."""
+    _check(load_library().moe_mxfp4_set_single_launch(int(mode)), "moe_mxfp4_set_single_launch")
+
+
+def call_launches(T, d_model, d_inter, E, topk) -> int:
+    """Kernels one forward call of this shape launches under the current launch mode."""
+    return int(load_library().moe_mxfp4_call_launches(T, d_model, d_inter, E, topk))
+
+
 def set_kernel_timing(mode):
     """0 off, 1 events around every kernel, 2 events around the whole call only."""
     _check(load_library().moe_mxfp4_set_kernel_timing(int(mode)), "moe_mxfp4_set_kernel_timing")
@@ -216,7 +233,8 @@ class MoeMXFP4:
         self.shape = (T, d_model, d_inter, E, topk)
         self.plan = get_plan(T, d_model, d_inter, E, topk)
         n = max(int(self.plan.workspace_bytes), 256)
-        self.workspace = torch.empty(n + 256, dtype=torch.uint8, device=device)
+        # zero-filled: the status region must start at zero (the calls keep it so)
+        self.workspace = torch.zeros(n + 256, dtype=torch.uint8, device=device)
         base = self.workspace.data_ptr()
         self.ws_ptr = (base + 255) // 256 * 256
         self.ws_bytes = n

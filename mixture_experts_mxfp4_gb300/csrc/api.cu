@@ -36,6 +36,9 @@ struct Timing {
 std::mutex g_mu;
 WorkspaceReg g_ws[kMaxDevices];
 int g_num_sms[kMaxDevices];
+// moe_mxfp4_set_single_launch mode per device (0 separate, 1 single, 2 auto); -1 = unset
+int g_single_launch[kMaxDevices] = {};
+bool g_single_set[kMaxDevices] = {};
 Timing g_timing[kMaxDevices];
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -75,11 +78,9 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     // No K split of stage 1: the GEMM kernel evens out its CTAs' work with the
     // distribution of stage-2 items instead.
     pl->stage1_splits = 1;
-    // per stage-1 unit (split-K arrivals), then per route tile (finished units)
-    const size_t n_counters = (size_t)pl->max_tiles * (size_t)(I / 64) + (size_t)pl->max_tiles;
     size_t b[MOE_WS_NUM_REGIONS];
-    b[MOE_WS_STATUS] = 16 * sizeof(uint32_t);
-    b[MOE_WS_COUNTERS] = n_counters * sizeof(uint32_t);
+    b[MOE_WS_STATUS] = kStatusWords * sizeof(uint32_t);
+    b[MOE_WS_COUNTERS] = (size_t)pl->max_tiles * sizeof(uint32_t);  // finished feature tiles per route tile
     b[MOE_WS_SORTED_IDS] = (size_t)cap * 4;
     b[MOE_WS_SORTED_W] = (size_t)cap * 4;
     b[MOE_WS_BLOCK_EXPERT] = (size_t)(cap / kBlockM) * 4;
@@ -92,10 +93,7 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     b[MOE_WS_A2Q] = (size_t)cap * (I / 2);
     b[MOE_WS_A2S] = (size_t)cap * pl->a2s_stride;
     b[MOE_WS_P] = (size_t)R * D * 4;
-    const size_t n_units = (size_t)pl->max_tiles * (size_t)(I / 64);
-    b[MOE_WS_PARTIAL] = pl->stage1_splits > 1
-                            ? n_units * (size_t)pl->stage1_splits * pl->tile_rows * 128 * 4
-                            : 0;
+    b[MOE_WS_PARTIAL] = 0;  // (no K split)
     size_t off = 0;
     for (int i = 0; i < MOE_WS_NUM_REGIONS; ++i) {
         pl->offset[i] = off;
@@ -105,8 +103,7 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     pl->workspace_bytes = off;
 }
 
-// n_units: stage-1 units (max_tiles * I / 64); the route-tile counters follow them.
-WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl, size_t n_units) {
+WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl) {
     uint8_t* b = static_cast<uint8_t*>(base);
     WsPtrs w;
     w.status = reinterpret_cast<uint32_t*>(b + pl.offset[MOE_WS_STATUS]);
@@ -123,8 +120,8 @@ WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl, size_t n_units) {
     w.a2q = b + pl.offset[MOE_WS_A2Q];
     w.a2s = b + pl.offset[MOE_WS_A2S];
     w.P = reinterpret_cast<float*>(b + pl.offset[MOE_WS_P]);
-    w.partial = reinterpret_cast<float*>(b + pl.offset[MOE_WS_PARTIAL]);
-    w.tile_done = w.counters + n_units;
+    w.tile_done = w.counters;
+    w.quant_done = w.status + kFrontQuantWord;
     return w;
 }
 
@@ -256,14 +253,12 @@ uint32_t stage_geometry(StageGeom& q, int Kc, int tile_rows, int mblocks) {
 // hold either stage's layout.  Narrow route tiles (decode) use two MMA-issuing
 // warps: a single stream of scale-factor copies and narrow MMAs leaves the
 // tensor pipe idle between instructions, and a second stream fills it.
-void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int ksplits1, int mblocks2) {
+void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2) {
     g.tile_rows = tile_rows;
     const uint32_t b1 = stage_geometry(g.g[0], D, tile_rows, 1);
     const uint32_t b2 = stage_geometry(g.g[1], I, tile_rows, mblocks2);
     g.g[0].n_ftiles = I / 64;
-    g.g[0].ksplits = ksplits1;
     g.g[1].n_ftiles = D / (128 * mblocks2);
-    g.g[1].ksplits = 1;
     g.slot_bytes = b1 > b2 ? b1 : b2;
     const uint32_t xchg = (uint32_t)(kEpiGroups * kXchgBytes);  // stage-1 epilogue
     const uint32_t tcache = (uint32_t)kTileCache * 16u;
@@ -356,6 +351,7 @@ moe_status_t moe_mxfp4_set_workspace(void* dev_ptr, size_t bytes) {
     if (dev_ptr && (reinterpret_cast<uintptr_t>(dev_ptr) % kAlign) != 0) return MOE_ERR_MISALIGNED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    if (dev_ptr && bytes < kStatusWords * sizeof(uint32_t)) return MOE_ERR_WORKSPACE;
     std::lock_guard<std::mutex> lk(g_mu);
     g_ws[dev].ptr = dev_ptr;
     g_ws[dev].bytes = dev_ptr ? bytes : 0;
@@ -421,21 +417,41 @@ constexpr int kCacheWays = 4;
 LaunchState g_cache[kMaxDevices][kCacheWays];
 int g_cache_next[kMaxDevices];
 
+// Plan and GEMM geometry of a shape (no device pointers).
+void shape_geometry(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, GemmParams* gp) {
+    fill_plan(T, D, I, E, K, pl);
+    memset(gp, 0, sizeof(*gp));
+    gp->D = D; gp->I = I; gp->E = E; gp->K = K; gp->R = T * K;
+    gp->a1s_stride = pl->a1s_stride;
+    gp->a2s_stride = pl->a2s_stride;
+    // stage 2 on narrow tiles: two 128-row blocks of w2 per item share the route tile
+    const int mb2 = (pl->tile_rows <= 64 && D % 256 == 0) ? 2 : 1;
+    gemm_geometry(*gp, D, I, pl->tile_rows, mb2);
+}
+
+// Whether a call of this shape routes and quantises inside the GEMM kernel under
+// the device's launch mode (0 separate, 1 single where possible, 2 automatic).
+// The in-kernel routing scratch must fit in the ring, the route positions in the
+// exchange buffer and the route tiles in the tile cache (R / block_m + E <= 512).
+bool single_launch_for(int dev, int T, int E, int K, const GemmParams& gp) {
+    static_assert(kFrontMaxRoutes * 4 <= kEpiGroups * kXchgBytes, "route positions");
+    static_assert(kFrontMaxRoutes / kBlockM + kFrontMaxExperts <= kTileCache, "route tiles");
+    static_assert(kFrontTileWord + kTileCache <= kStatusWords, "route-tile counters");
+    const size_t scratch = sizeof(int) * ((size_t)(kGemmThreads / 32 + 1) * E + 1 + 2 * (kGemmThreads / 32) + 4);
+    const int mode = g_single_set[dev] ? g_single_launch[dev] : 2;
+    const long long routes = (long long)T * K;
+    return (mode == 1 || (mode == 2 && routes <= kFrontAutoRoutes)) && routes <= kFrontMaxRoutes &&
+           E <= kFrontMaxExperts && scratch <= (size_t)gp.num_stages * gp.slot_bytes;
+}
+
 bool build_state(LaunchState& st, const void* w13, const void* w13_scale, const void* w2,
                  const void* w2_scale, int T, int D, int I, int E, int K, void* base) {
     using namespace moe;
     moe_mxfp4_plan_t& pl = st.pl;
-    fill_plan(T, D, I, E, K, &pl);
-    const WsPtrs ws = ws_ptrs(base, pl, (size_t)pl.max_tiles * (size_t)(I / 64));
     GemmParams& gp = st.gp;
-    memset(&gp, 0, sizeof(gp));
+    shape_geometry(T, D, I, E, K, &pl, &gp);
+    const WsPtrs ws = ws_ptrs(base, pl);
     gp.ws = ws;
-    gp.D = D; gp.I = I; gp.E = E; gp.K = K; gp.R = T * K;
-    gp.a1s_stride = pl.a1s_stride;
-    gp.a2s_stride = pl.a2s_stride;
-    // stage 2 on narrow tiles: two 128-row blocks of w2 per item share the route tile
-    const int mb2 = (pl.tile_rows <= 64 && D % 256 == 0) ? 2 : 1;
-    gemm_geometry(gp, D, I, pl.tile_rows, pl.stage1_splits, mb2);
     const StageGeom& q1 = gp.g[0];
     const StageGeom& q2 = gp.g[1];
 
@@ -503,22 +519,39 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
 
     // ---------------------------------------------------------- launches
     const int sms = num_sms(dev);
-    const int n_counters = pl.max_tiles * (I / 64) + pl.max_tiles;
+    const int n_counters = pl.max_tiles;
     Timing& tm = g_timing[dev];
     const bool timed = tm.enabled && tm.created;
     auto mark = [&](int i) {
         if (timed && (tm.mode == 1 || i == 0 || i == kNumKernels)) cudaEventRecord(tm.ev[i], stream);
     };
+    // Single launch: routing and quantisation run inside the GEMM kernel (one
+    // launch before the top-k sum); otherwise route -> quant -> GEMM.
+    const bool front = single_launch_for(dev, T, E, K, gp);
+    GemmParams g = gp;
+    g.fused_front = front ? 1 : 0;
+    g.topk_ids = topk_ids;
+    g.topk_w = topk_weights;
+    g.hidden = hidden;
+    g.T = T;
+    g.cap = pl.cap;
+    if (front) g.ws.tile_done = ws.status + kFrontTileWord;  // zero between calls
     mark(0);
-    if (launch_route(topk_ids, topk_weights, T, K, E, pl.tile_rows, pl.cap, n_counters, ws,
-                     stream) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (!front) {
+        if (launch_route(topk_ids, topk_weights, T, K, E, pl.tile_rows, pl.cap, n_counters, ws,
+                         stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     mark(1);
-    if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!front) {
+        if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     mark(2);
-    if (launch_gemm(st->maps, gp, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_gemm(st->maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);
-    if (launch_reduce(topk_ids, T, K, E, D, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    // on the single-launch path the top-k sum also clears the ready word for the next call
+    if (launch_reduce(topk_ids, T, K, E, D, out, ws, front, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(4);
     if (timed) tm.recorded = true;
     return MOE_OK;
@@ -574,6 +607,26 @@ moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream
 }
 
 int moe_mxfp4_num_kernels(void) { return kNumKernels; }
+
+int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk) {
+    if (validate_shape(T, d_model, d_inter, E, topk) != MOE_OK) return -1;
+    if (T == 0) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    moe_mxfp4_plan_t pl;
+    moe::GemmParams gp;
+    shape_geometry(T, d_model, d_inter, E, topk, &pl, &gp);
+    return single_launch_for(dev, T, E, topk, gp) ? 2 : 4;
+}
+
+moe_status_t moe_mxfp4_set_single_launch(int mode) {
+    if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    g_single_launch[dev] = mode;
+    g_single_set[dev] = true;
+    return MOE_OK;
+}
 
 moe_status_t moe_mxfp4_set_kernel_timing(int mode) {
     if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;

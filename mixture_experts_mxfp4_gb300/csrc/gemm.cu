@@ -55,29 +55,314 @@
 namespace moe {
 
 struct Item {
-    int e, row0, nrows, f, ks0, ks1, unit, split, tile;
+    int e, row0, nrows, f, ks0, ks1, tile;
 };
 
-// Item `it` of a stage: route tile it / (n_ftiles * ksplits), then feature tile,
-// then K split.  The first kTileCache route tiles come from the shared-memory copy.
+// Item `it` of a stage: route tile it / n_ftiles, then feature tile; it runs
+// over the whole K extent.  The first kTileCache route tiles come from the
+// shared-memory copy.
 __device__ __forceinline__ Item decode_item(const StageGeom& q, const int4* gtiles, int it,
                                             const int4* tcache) {
     Item x;
-    const int per_tile = q.n_ftiles * q.ksplits;
-    const int tile = it / per_tile;
-    const int rem = it - tile * per_tile;
-    x.f = rem / q.ksplits;
-    x.split = rem - x.f * q.ksplits;
+    const int tile = it / q.n_ftiles;
+    x.f = it - tile * q.n_ftiles;
     const int4 t = tile < kTileCache ? tcache[tile] : __ldcg(gtiles + tile);
     x.e = t.x;
     x.row0 = t.y;
     x.nrows = t.z;
-    const int per = q.kstages / q.ksplits;
-    x.ks0 = x.split * per;
-    x.ks1 = x.ks0 + per;
-    x.unit = tile * q.n_ftiles + x.f;
+    x.ks0 = 0;
+    x.ks1 = q.kstages;
     x.tile = tile;
     return x;
+}
+
+// ---------------------------------------------------------------- front end
+//
+// Single-launch path (few routes): every CTA routes all routes in shared memory
+// with the routing kernel's deterministic order (routes of an expert in
+// ascending route id, block_m padding, sentinel slots; route_quant_reduce.cu),
+// so it knows its route tiles without waiting for another kernel.  scr (ring
+// slot 0, not yet in use): hist [NW][E], seg [E + 1], wsum [2 NW], totals [4].
+// pos [R] receives every route's slot (-1 for ids outside [0, E)); the tiles go
+// to tcache.  CTA 0 (write_global) also clears the call's error bits, writes
+// the workspace routing arrays and then stores kFrontReady to status[15] (the
+// top-k sum kernel of the same call sets it back to 0).  Returns the number of
+// route tiles.  Whole CTA; E <= kFrontMaxExperts.
+__device__ int front_route(const GemmParams& p, int* scr, int* pos, int4* tcache, bool write_global) {
+    constexpr int NW = kGemmThreads / 32;
+    const int E = p.E, R = p.T * p.K, bm = kBlockM, tr = p.tile_rows;
+    int* hist = scr;
+    int* seg = hist + NW * E;
+    int* wsum = seg + (E + 1);
+    int* totals = wsum + 2 * NW;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < NW * E; i += kGemmThreads) hist[i] = 0;
+    if (tid < 4) totals[tid] = 0;
+    if (write_global && tid < 15) p.ws.status[tid] = 0;  // this call's error bits
+    __syncthreads();
+
+    const int chunk = (R + NW - 1) / NW;
+    const int r_begin = min(warp * chunk, R);
+    const int r_end = min(r_begin + chunk, R);
+    // pass 1: per-warp histogram (one leader per distinct expert in a batch of 32)
+    for (int base = r_begin; base < r_end; base += 32) {
+        const int r = base + lane;
+        const int e = (r < r_end) ? __ldg(p.topk_ids + r) : -1;
+        const bool valid = (r < r_end) && e >= 0 && e < E;
+        const uint32_t m = __match_any_sync(0xffffffffu, valid ? e : -1);
+        if (valid && lane == __ffs(m) - 1) hist[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // per expert: prefix over warps, padded length, tiles; then exclusive scans
+    int cnt = 0, padded = 0, ntiles = 0;
+    if (tid < E) {
+        int run = 0;
+        for (int w = 0; w < NW; ++w) {
+            const int c = hist[w * E + tid];
+            hist[w * E + tid] = run;
+            run += c;
+        }
+        cnt = run;
+        padded = (cnt + bm - 1) / bm * bm;
+        ntiles = (padded + tr - 1) / tr;
+    }
+    int a = padded, b = ntiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ta = __shfl_up_sync(0xffffffffu, a, o);
+        const int tb = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) {
+            a += ta;
+            b += tb;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = a;
+        wsum[NW + warp] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int xa = lane < NW ? wsum[lane] : 0, xb = lane < NW ? wsum[NW + lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, xa, o);
+            const int tb = __shfl_up_sync(0xffffffffu, xb, o);
+            if (lane >= o) {
+                xa += ta;
+                xb += tb;
+            }
+        }
+        if (lane < NW) {
+            wsum[lane] = xa;
+            wsum[NW + lane] = xb;
+        }
+    }
+    __syncthreads();
+    if (warp > 0) {
+        a += wsum[warp - 1];
+        b += wsum[NW + warp - 1];
+    }
+    const int seg_e = a - padded, tile_e = b - ntiles;
+    if (tid < E) seg[tid] = seg_e;
+    if (tid == kGemmThreads - 1) {
+        seg[E] = a;
+        totals[0] = a;  // padded length
+        totals[1] = b;  // route tiles
+    }
+    if (tid < E && cnt > 0) atomicAdd(&totals[2], cnt);  // valid routes
+    __syncthreads();
+    const int total_padded = totals[0], total_tiles = totals[1];
+
+    if (tid < E && cnt > 0) {
+        for (int j = 0; j < ntiles; ++j) {
+            const int4 t4 = make_int4(tid, seg_e + j * tr, min(tr, padded - j * tr), 0);
+            if (tile_e + j < kTileCache) tcache[tile_e + j] = t4;
+            if (write_global) p.ws.tiles[tile_e + j] = t4;
+        }
+    }
+    if (write_global) {
+        if (tid <= E) p.ws.seg_start[tid] = seg[tid];
+        if (tid < E && cnt > 0) {
+            for (int blk = seg_e / bm; blk < (seg_e + padded) / bm; ++blk) p.ws.block_expert[blk] = tid;
+            for (int q = seg_e + cnt; q < seg_e + padded; ++q) {
+                p.ws.sorted_ids[q] = R;
+                p.ws.sorted_w[q] = 0.0f;
+            }
+        }
+        for (int q = total_padded + tid; q < p.cap; q += kGemmThreads) {
+            p.ws.sorted_ids[q] = R;
+            p.ws.sorted_w[q] = 0.0f;
+        }
+        for (int blk = total_padded / bm + tid; blk < p.cap / bm; blk += kGemmThreads)
+            p.ws.block_expert[blk] = -1;
+        if (tid == 0) {
+            p.ws.num_valid[0] = total_padded;
+            p.ws.num_valid[1] = totals[2];
+            p.ws.num_valid[2] = total_tiles;
+            p.ws.num_valid[3] = 0;
+        }
+    }
+    // pass 2: slots in the same order; rank = warp prefix + rank in the batch
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int base = r_begin; base < r_end; base += 32) {
+        const int r = base + lane;
+        const int e = (r < r_end) ? __ldg(p.topk_ids + r) : -1;
+        const bool valid = (r < r_end) && e >= 0 && e < E;
+        const uint32_t m = __match_any_sync(0xffffffffu, valid ? e : -1);
+        if (valid) {
+            const int slot = seg[e] + hist[warp * E + e] + __popc(m & lt_mask);
+            pos[r] = slot;
+            if (write_global) {
+                p.ws.sorted_ids[slot] = r;
+                p.ws.sorted_w[slot] = __ldg(p.topk_w + r);
+                p.ws.route_pos[r] = slot;
+            }
+        } else if (r < r_end) {
+            pos[r] = -1;
+            if (write_global) p.ws.route_pos[r] = -1;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(m) - 1) hist[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+    fence_proxy_async_smem();  // the scratch is ring memory that TMA copies fill next
+    __syncthreads();
+    if (write_global && tid == 0) {
+        // publish the routing arrays (the epilogues read the slots' route ids and weights)
+        __threadfence();
+        st_release_gpu(p.ws.status + 15, kFrontReady);
+    }
+    return total_tiles;
+}
+
+// MX quantisation of a 32-element block of bf16 by four lanes (lane % 4 = qd
+// holds elements 8qd .. 8qd+7 as one 16-byte load): the lanes share the block's
+// amax, and each returns its 4 code bytes (low nibble = even element); sc is the
+// block's e8m0 scale byte.  All 32 lanes of the warp call it (inactive lanes
+// with zeros: their group's result is not used).
+__device__ __forceinline__ uint32_t front_quant8(const uint4 raw, uint32_t& sc) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    sc = mx_scale_byte(amax);
+    const float inv = mx_inv_scale(sc == 255u ? 0u : sc);
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) word |= e2m1_code(v[i], sc, inv) << (4 * i);
+    return word;
+}
+
+// Blocks of 32 elements that one CTA quantises per pass (four epilogue threads each).
+constexpr int kFrontQuantBlocks = 64;
+// Stages whose weight copies a CTA issues before the quantisation is complete.
+constexpr int kFrontPreStages = 2;
+
+// First 16-byte load of an epilogue thread's quantisation share, issued before
+// the routing and before any weight copy (the copies of the first stages fill
+// the memory system's queues for microseconds), and an L2 prefetch of the
+// CTA's later passes; zeros past the end.  The hidden states are contiguous,
+// so block j of 32 elements starts at byte 64 j.
+__device__ __forceinline__ uint4 front_quant_first_load(const GemmParams& p) {
+    const int et = (int)threadIdx.x - 128;
+    const long total = (long)p.T * (p.D / 32);
+    const uint8_t* hid = static_cast<const uint8_t*>(p.hidden);
+    constexpr int kLines = kFrontQuantBlocks * 64 / 128;  // 128-byte lines per pass
+    if (et < kLines) {
+        for (long jb = (long)(blockIdx.x + gridDim.x) * kFrontQuantBlocks; jb < total;
+             jb += (long)gridDim.x * kFrontQuantBlocks)
+            if (jb * 64 + et * 128 < total * 64) prefetch_l2(hid + jb * 64 + et * 128);
+    }
+    const long j = (long)blockIdx.x * kFrontQuantBlocks + (et >> 2);
+    if (j >= total) return make_uint4(0, 0, 0, 0);
+    return ld_nc_v4_now(hid + j * 64 + (et & 3) * 16);
+}
+
+// Bounded wait (one thread) until a global word equals `want` (equal) or
+// reaches it; returns after an acquire load that saw it.  False, with the
+// status bit and the CTA's abort flag set, when the limit passes; false when
+// the CTA has already aborted.
+__device__ __forceinline__ bool poll_word(const uint32_t* word, uint32_t want, bool equal,
+                                          uint32_t* status, uint32_t err_bit,
+                                          volatile int* abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 0;; ++n) {
+        const uint32_t v = ld_relaxed_gpu(word);
+        if (equal ? v == want : v >= want) {
+            const uint32_t va = ld_acquire_gpu(word);
+            if (equal ? va == want : va >= want) return true;
+        }
+        if ((n & 63u) == 63u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(status, err_bit);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// The epilogue warps' part of the single-launch front end: quantise this CTA's
+// share of the hidden states (passes of kFrontQuantBlocks consecutive blocks of
+// 32 elements, spread over the CTAs; first16: the thread's first load) and
+// write each block to the sorted slot of every valid route of its token; then
+// count the CTA in quant_done (zero at the start of the call: the previous
+// call's top-k sum kernel, or the workspace registration, cleared it).
+// Warps 4..11 (named barrier 3).
+__device__ void front_quant(const GemmParams& p, const int* pos, uint4 first16) {
+    const int et = (int)threadIdx.x - 128;
+    const int D = p.D, K = p.K, nblk = D / 32;
+    const long total = (long)p.T * nblk;
+    const __nv_bfloat16* hidden = static_cast<const __nv_bfloat16*>(p.hidden);
+    const int qd = et & 3;
+    bool first = true;
+    for (long jb = (long)blockIdx.x * kFrontQuantBlocks; jb < total;
+         jb += (long)gridDim.x * kFrontQuantBlocks) {
+        const long j = jb + (et >> 2);
+        const bool active = j < total;
+        const int t = active ? (int)(j / nblk) : 0;
+        const int gb = active ? (int)(j - (long)t * nblk) : 0;
+        uint4 raw = first16;
+        if (!first && active)
+            raw = __ldg(reinterpret_cast<const uint4*>(hidden + (size_t)t * D) + gb * 4 + qd);
+        first = false;
+        uint32_t sc;
+        const uint32_t word = front_quant8(raw, sc);  // whole warp
+        if (active) {
+            for (int k = 0; k < K; ++k) {
+                const int ps = pos[t * K + k];
+                if (ps >= 0) {
+                    *reinterpret_cast<uint32_t*>(p.ws.a1q + (size_t)ps * (D / 2) + gb * 16 + qd * 4) = word;
+                    if (qd == 0) p.ws.a1s[(size_t)ps * p.a1s_stride + gb] = (uint8_t)sc;
+                }
+            }
+        }
+    }
+    // the stage-1 route-tile copies (async proxy) read these bytes
+    fence_proxy_async_global();
+    named_bar_sync(3, 256);
+    if (et == 0) {
+        __threadfence();
+        if (atomicAdd(p.ws.quant_done, 1u) >= gridDim.x) atomicOr(p.ws.status, kErrCounterState);
+    }
+}
+
+// Routing-array read in the epilogue: through the read-only cache when an
+// earlier kernel wrote the arrays, from L2 when CTA 0 of this kernel did.
+template <typename V>
+__device__ __forceinline__ V ld_route(bool written_here, const V* ptr) {
+    return written_here ? __ldcg(ptr) : __ldg(ptr);
 }
 
 // Scale factors in TMEM: tcgen05.cp .32x128b.warpx4 copies 32 rows x 16 bytes
@@ -165,9 +450,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* drain = tempty + kMaxAccBufs;  // one per MMA warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    // per epilogue group: 4 KB exchange buffer, then a flag word
+    // per epilogue group: a 4 KB exchange buffer (kXchgBytes apart)
     float* xchg = reinterpret_cast<float*>(smem + p.off_xchg);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + p.off_xchg + 4096);
     uint32_t* status = p.ws.status;
 
     grid_dep_launch();
@@ -200,8 +484,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Everything above overlaps the previous kernel; from here on the kernel
     // reads what earlier kernels wrote, and TMEM is free once they have exited.
     grid_dep_wait();
-    const int num_tiles = __ldcg(p.ws.num_valid + 2);
-    const int nitems[2] = {num_tiles * p.g[0].n_ftiles * p.g[0].ksplits, num_tiles * p.g[1].n_ftiles};
+    // Single-launch path: route in shared memory (the ring is not in use yet);
+    // otherwise the routing kernel's tile count.
+    const bool front = p.fused_front != 0;
+    int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
+    int* fpos = reinterpret_cast<int*>(smem + p.off_xchg);  // route -> slot (front end only)
+    uint4 qfirst = make_uint4(0, 0, 0, 0);  // epilogue threads: first hidden-state load
+    if (front && warp >= 4) qfirst = front_quant_first_load(p);
+    const int num_tiles = front ? front_route(p, reinterpret_cast<int*>(smem), fpos, tcache, blockIdx.x == 0)
+                                : __ldcg(p.ws.num_valid + 2);
+    const int nitems[2] = {num_tiles * p.g[0].n_ftiles, num_tiles * p.g[1].n_ftiles};
     const int G = (int)gridDim.x;
     const int b0 = (int)blockIdx.x;
     // stage-2 schedule: items [0, X) round-robin over the L CTAs with one stage-1
@@ -209,7 +501,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // stage-2 item (per2 stages) costs about 1.5 stage-1 stages (measured: its
     // narrower MMAs and P epilogue), so one stage-1 item is worth 2*per1/(3*per2)
     // stage-2 items.
-    const int per1 = p.g[0].kstages / p.g[0].ksplits, per2 = p.g[1].kstages;
+    const int per1 = p.g[0].kstages, per2 = p.g[1].kstages;
     const int r1 = nitems[0] % G;
     const int L = r1 > 0 ? G - r1 : 0;
     const int X = min(L * ((2 * per1) / (3 * per2)), nitems[1]);
@@ -226,10 +518,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int j = X + b0 + (m - seg1) * G;
         return j < nitems[1] ? j : -1;
     };
-    if (my_items0 == 0 && my_items1 == 0) return;
-    int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
-    for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kGemmThreads)
-        tcache[i] = __ldcg(p.ws.tiles + i);
+    if (my_items0 == 0 && my_items1 == 0) {
+        // an idle CTA still quantises its share of the hidden states
+        if (front && warp >= 4) front_quant(p, fpos, qfirst);
+        return;
+    }
+    if (!front) {
+        for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kGemmThreads)
+            tcache[i] = __ldcg(p.ws.tiles + i);
+    }
     if (warp == 2) {
         tmem_alloc(tmem_slot, p.tmem_cols);
         tmem_relinquish();
@@ -252,7 +549,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t last_ph = 0;  // bit s: parity of the last fill of stage s
             int ready_tile = -1;   // last route tile seen complete by stage 1
             const uint32_t need = (uint32_t)p.g[0].n_ftiles;
+            // Single-launch path: the CTA's first kFrontPreStages stages (stage i in
+            // slot i) get their weight copies at once and their route-tile copies
+            // once every CTA has quantised its share of the hidden states; later
+            // stages wait for that too.  (More early weight copies would fill the
+            // memory system's queues and slow the front end's own loads, stores and
+            // instruction fetches.)
+            const int defer_n = front ? min(kFrontPreStages, my_items0 * per1) : 0;
+            int n_st = 0;  // stages issued so far
+            int drow[kMaxStages], dks[kMaxStages];
+            bool resolved = !front;
+            auto resolve = [&]() {
+                const bool got =
+                    poll_word(p.ws.quant_done, (uint32_t)G, false, status, kErrTimeoutFront, abort_flag);
+                if (got)
+                    fence_proxy_async_global();
+                else
+                    ok = false;
+                // issued either way so that the deferred stages' barriers complete
+                const StageGeom& q0 = p.g[0];
+                for (int i = 0; i < min(n_st, defer_n); ++i) {
+                    uint8_t* st = smem + (size_t)i * p.slot_bytes;
+                    tma_load_2d(st + q0.off_sb, &tmSB1, q0.b_scale_x ? dks[i] * 16 : 0, drow[i], &sfull[i]);
+                    tma_load_3d(st + q0.off_b, &tmB1, 0, drow[i], dks[i] * q0.nkt, &full[i]);
+                }
+                resolved = true;
+            };
             for (int phs = 0; phs < 2 && ok; ++phs) {
+                if (phs == 1 && !resolved) resolve();
+                if (!ok) break;
                 const StageGeom& q = p.g[phs];
                 const CUtensorMap* mA = phs ? &tmA2 : &tmA1;
                 const CUtensorMap* mSA = phs ? &tmSA2 : &tmSA1;
@@ -263,6 +588,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                     const Item x = decode_item(q, p.ws.tiles, it, tcache);
                     for (int ks = x.ks0; ks < x.ks1; ++ks) {
+                        if (!resolved && n_st == defer_n) {
+                            resolve();
+                            if (!ok) break;
+                        }
                         if (!mbar_wait(&empty[s], ph ^ 1u, status, kErrTimeoutEmpty, abort_flag)) {
                             ok = false;
                             break;
@@ -292,7 +621,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 const uint64_t t0 = globaltimer_ns();
                                 bool got = false;
                                 for (uint32_t n = 0;; ++n) {
-                                    if (ld_acquire_gpu(p.ws.tile_done + x.tile) >= need) {
+                                    if (ld_relaxed_gpu(p.ws.tile_done + x.tile) >= need &&
+                                        ld_acquire_gpu(p.ws.tile_done + x.tile) >= need) {
                                         got = true;
                                         break;
                                     }
@@ -318,8 +648,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                         // route tile: tile_rows sorted slots from row0 (rows past the tile's
                         // own are read but never used; past the end they are zero-filled)
-                        tma_load_2d(st + q.off_sb, mSB, q.b_scale_x ? ks * 16 : 0, x.row0, &sfull[s]);
-                        tma_load_3d(st + q.off_b, mB, 0, x.row0, kt0, &full[s]);
+                        if (n_st < defer_n) {
+                            drow[n_st] = x.row0;
+                            dks[n_st] = ks;
+                        } else {
+                            tma_load_2d(st + q.off_sb, mSB, q.b_scale_x ? ks * 16 : 0, x.row0, &sfull[s]);
+                            tma_load_3d(st + q.off_b, mB, 0, x.row0, kt0, &full[s]);
+                        }
+                        ++n_st;
                         issued |= 1u << s;
                         last_ph = (last_ph & ~(1u << s)) | (ph << s);
                         if (++s == NS) {
@@ -330,6 +666,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
+            if (!resolved) resolve();  // (after an abort: completes the deferred stages)
             if (!ok) {
                 // Let every copy already issued land before the CTA exits: the
                 // last fill of stage i completes the phase with parity last_ph[i].
@@ -394,7 +731,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
                 for (int c = 0; c < qq.natoms; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
             };
-            const long g_phase_end = g + (long)(phs == 0 ? my_items0 : my_items1) * (q.kstages / q.ksplits);
+            const long g_phase_end = g + (long)(phs == 0 ? my_items0 : my_items1) * q.kstages;
             for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
@@ -521,7 +858,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int grp = (int)(warp - 4) >> 2;    // epilogue group
         const uint32_t bar_id = 1u + (uint32_t)grp;
         float* xg = xchg + grp * (kXchgBytes / 4);
-        volatile int* flag = last_flag + grp * (kXchgBytes / 4);
         const int R = p.R;
         const int MW = p.mma_warps;
         int local = 0;
@@ -529,9 +865,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t aph_next = 0;  // and its use parity
         int g0 = 0;             // index of the item's first stage (as the MMA warps count)
         bool ok = true;
+        if (front) {
+            front_quant(p, fpos, qfirst);
+            // the slots' route ids and weights come from CTA 0 (ready word)
+            int got = 1;
+            if (warp == 4 && lane == 0)
+                got = poll_word(p.ws.status + 15, kFrontReady, true, status, kErrTimeoutFront, abort_flag) ? 1 : 0;
+            ok = named_bar_and(3, 256, got != 0);
+        }
         for (int phs = 0; phs < 2 && ok; ++phs) {
             const StageGeom& q = p.g[phs];
-            const int per = q.kstages / q.ksplits;  // stages per item
+            const int per = q.kstages;  // stages per item
             const int MB = q.mblocks;
             for (int m = 0, it = item_of(phs, 0); it >= 0; it = item_of(phs, ++m), ++local) {
                 const int a = a_next;
@@ -546,8 +890,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 // route metadata of the tile's first 16 slots, fetched before waiting
                 const int slot0 = x.row0 + (int)(lane & 15);
-                int rid_pre = __ldg(p.ws.sorted_ids + slot0);
-                float w_pre = phs == 1 ? __ldg(p.ws.sorted_w + slot0) : 0.0f;
+                int rid_pre = ld_route(front, p.ws.sorted_ids + slot0);
+                float w_pre = phs == 1 ? ld_route(front, p.ws.sorted_w + slot0) : 0.0f;
                 if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) {
                     ok = false;
                     break;
@@ -584,52 +928,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 bool released = false;
                 if (phs == 0) {
                     const int n0 = x.f * 64;  // first feature of the tile
-                    bool have = true;
-                    if (q.ksplits > 1) {
-                        // Split-K: publish this split's partial sums, then the CTA that
-                        // completes the unit's count sums splits 0..S-1 in that order.
-                        float* part = p.ws.partial + (size_t)x.unit * q.ksplits * p.tile_rows * 128;
+                    {
                         for (int c = 0; c < nchunks; ++c) {
                             float v[16];
                             load_acc(c, v);
                             if (c + 1 == nchunks) {
                                 release();
                                 released = true;
-                            }
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                part[((size_t)x.split * p.tile_rows + 16 * c + i) * 128 + 32 * q4 + lane] = v[i];
-                        }
-                        __threadfence();
-                        named_bar_sync(bar_id, 128);
-                        if (q4 == 0 && lane == 0) {
-                            const uint32_t prev = atomicAdd(p.ws.counters + x.unit, 1u);
-                            *flag = (prev == (uint32_t)(q.ksplits - 1)) ? 1 : 0;
-                        }
-                        named_bar_sync(bar_id, 128);
-                        have = *flag != 0;
-                        if (have) __threadfence();
-                    }
-                    if (have) {
-                        const float* part = p.ws.partial + (size_t)x.unit * q.ksplits * p.tile_rows * 128;
-                        for (int c = 0; c < nchunks; ++c) {
-                            float v[16];
-                            if (q.ksplits > 1) {
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[i] = __ldcg(part + ((size_t)(16 * c + i)) * 128 + 32 * q4 + lane);
-                                for (int sp = 1; sp < q.ksplits; ++sp) {
-#pragma unroll
-                                    for (int i = 0; i < 16; ++i)
-                                        v[i] = v[i] + __ldcg(part + ((size_t)sp * p.tile_rows + 16 * c + i) * 128 +
-                                                             32 * q4 + lane);
-                                }
-                            } else {
-                                load_acc(c, v);
-                                if (c + 1 == nchunks) {
-                                    release();
-                                    released = true;
-                                }
                             }
                             if (q4 >= 2) {
 #pragma unroll
@@ -638,7 +943,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             named_bar_sync(bar_id, 128);
                             if (q4 < 2) {
                                 const int rid_l =
-                                    c == 0 ? rid_pre : __ldg(p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
+                                    c == 0 ? rid_pre : ld_route(front, p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
                                 const int feat = n0 + 32 * (int)q4;  // first feature of this warp's block
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
@@ -676,7 +981,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         named_bar_sync(bar_id, 128);
                         if (q4 == 0 && lane == 0) {
                             __threadfence();
-                            atomicAdd(p.ws.tile_done + x.tile, 1u);
+                            if (atomicAdd(p.ws.tile_done + x.tile, 1u) >= (uint32_t)q.n_ftiles)
+                                atomicOr(status, kErrCounterState);
                         }
                     }
                 } else {
@@ -695,8 +1001,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             float w_l = w_pre;
                             if (c > 0) {
                                 const int sl = x.row0 + 16 * c + (int)(lane & 15);
-                                rid_l = __ldg(p.ws.sorted_ids + sl);
-                                w_l = __ldg(p.ws.sorted_w + sl);
+                                rid_l = ld_route(front, p.ws.sorted_ids + sl);
+                                w_l = ld_route(front, p.ws.sorted_w + sl);
                             }
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
@@ -718,7 +1024,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 2) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
+                        cudaStream_t stream) {
     // Raise the dynamic shared-memory limit once per device.
     static bool limit_set[64];
     int dev = 0;

@@ -13,8 +13,8 @@ namespace moe {
 
 // Device pointers into the caller's workspace (see moe_mxfp4_plan_t).
 struct WsPtrs {
-    uint32_t* status;      // [16]
-    uint32_t* counters;    // split-K arrival counters
+    uint32_t* status;      // [kStatusWords]: [0] error bits, [15] single-launch ready word, ...
+    uint32_t* counters;    // [max_tiles]: route-tile counters of the multi-kernel path
     int32_t* sorted_ids;   // [cap]
     float* sorted_w;       // [cap]
     int32_t* block_expert; // [cap / block_m]
@@ -27,15 +27,15 @@ struct WsPtrs {
     uint8_t* a2q;          // [cap][I/2]
     uint8_t* a2s;          // [cap][a2s_stride]
     float* P;              // [R][D]
-    float* partial;        // split-K partial accumulators
-    uint32_t* tile_done;   // [max_tiles]: stage-1 feature tiles completed per route tile
+    uint32_t* tile_done;   // stage-1 feature tiles completed per route tile (counters, or the
+                           // status region's block on the single-launch path)
+    uint32_t* quant_done;  // CTAs whose share of the hidden states is quantised (single launch)
 };
 
 // Geometry of one grouped block-scaled GEMM stage (stage 1: gate_up, K = D;
 // stage 2: down, K = I) inside the fused GEMM kernel.
 struct StageGeom {
     int n_ftiles;       // stage 1: I / 64 feature tiles; stage 2: D / (128 * mblocks) output tiles
-    int ksplits;        // K splits (stage 2: 1)
     int kstages;        // K / kstage_elems
     int kstage_elems;   // K elements per pipeline stage: 128, 256 or 512
     int kb;             // bytes per row of one TMA box along K: 64 or 128
@@ -68,7 +68,23 @@ struct GemmParams {
     uint32_t smem_bytes;                    // dynamic shared memory requested
     int a2s_stride;
     int a1s_stride;
+    // Routing and quantisation inside the GEMM kernel (fused_front = 1, few
+    // routes): the inputs and the sorted-slot capacity.
+    int fused_front;
+    const int32_t* topk_ids;
+    const float* topk_w;
+    const void* hidden;
+    int T, cap;
 };
+
+// Status region (u32 words): [0] error bits, [1..14] spare, [15] ready word of
+// the single-launch path, [16] its quantisation count, [512, 1024) its route-tile
+// counters.  Words 15.. are zero between calls: the workspace registration
+// zeroes the region and the single-launch path's top-k sum kernel clears them
+// after each call.
+constexpr int kStatusWords = 1024;
+constexpr int kFrontQuantWord = 16;
+constexpr int kFrontTileWord = 512;
 
 constexpr int kBlockM = 16;          // slots per padded block
 // 12 warps: producer, MMA, second MMA / TMEM owner, scale layout, 2 x 4 epilogue
@@ -78,6 +94,9 @@ constexpr int kXchgBytes = 4352;     // per epilogue group: 4 KB exchange + flag
 constexpr int kMaxStages = 8;
 constexpr int kGemmSmemLimit = 227 * 1024;  // dynamic shared memory limit set on the GEMMs
 constexpr int kMaxAccBufs = 4;
+constexpr int kFrontMaxRoutes = 2048;  // single-launch path: routes (position table in the exchange buffer)
+constexpr int kFrontMaxExperts = 384;  // single-launch path: one expert per GEMM thread
+constexpr int kFrontAutoRoutes = 256;  // automatic mode: single launch up to this many routes
 constexpr int kTileCache = 512;      // route tiles kept in shared memory (the rest read from L2)
 
 // Host-side pieces of the forward call shared by its entry points (api.cu).
@@ -97,8 +116,9 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
                          cudaStream_t stream);
 cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride,
                          const WsPtrs& ws, cudaStream_t stream);
+// clear_ready: also clear the single-launch words of the status region (after that GEMM)
 cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
-                          const WsPtrs& ws, cudaStream_t stream);
+                          const WsPtrs& ws, bool clear_ready, cudaStream_t stream);
 // maps: stage-1 A, SA, B, SB, then stage-2 A, SA, B, SB
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream);

@@ -13,10 +13,12 @@
 // are rejected with MOE_ERR_WORKSPACE.
 //
 // The array is shared by every call on a device and keeps the previous call's
-// contents; the parts that must start at zero (split-K arrival counters and the
-// device status word) are cleared by the routing kernel at the start of every
-// call.  Calls that overlap on the GPU (different streams without ordering)
-// race on the array.
+// contents.  The parts that must start at zero are zero when the library is
+// loaded (a __device__ array is zero-initialised) and are kept so: the routing
+// kernel clears the route-tile counters and status words at the start of a
+// multi-kernel call, and a single-launch call's top-k sum kernel clears the
+// words its GEMM used.  Calls that overlap on the GPU (different streams
+// without ordering) race on the array.
 #include <cuda_runtime.h>
 
 #include <mutex>

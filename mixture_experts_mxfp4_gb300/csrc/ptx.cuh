@@ -21,7 +21,14 @@ enum : uint32_t {
     kErrTimeoutDrain = 1u << 4,    // abort path waited for outstanding copies/MMAs
     kErrSelfCheck = 1u << 5,       // moe_mxfp4_check_wait_timeout's deliberate wait ran out
     kErrTimeoutTile = 1u << 6,     // stage-2 producer waited for a stage-1 route tile
+    kErrTimeoutFront = 1u << 7,    // single-launch path waited for routing or quantisation
+    kErrCounterState = 1u << 8,    // a counter was already past its target (status region not zeroed)
 };
+
+// Status word 15 on the single-launch path: 0 between calls, kFrontReady once
+// CTA 0 of the GEMM kernel has zeroed the call's counters and written the
+// routing arrays.  (Not 1, so that stale contents are unlikely to look ready.)
+constexpr uint32_t kFrontReady = 0x4d6f4531u;
 
 // A wait gives up after this many nanoseconds of %globaltimer.  Legitimate waits
 // in these kernels last microseconds.
@@ -153,10 +160,52 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Polling load: a relaxed load does not order (or hold up) the SM's other
+// memory accesses the way an acquire load does; a poll that sees its value
+// follows up with one acquire load of the same word.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// 16-byte read-only load that the compiler keeps where it is written (issued
+// early on purpose, e.g. before a long stretch of other work).
+__device__ __forceinline__ uint4 ld_nc_v4_now(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Named barrier over nthreads threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

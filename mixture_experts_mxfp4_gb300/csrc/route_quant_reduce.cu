@@ -270,9 +270,20 @@ cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride
 
 __global__ void __launch_bounds__(256)
     moe_reduce_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int D,
-                      const float* __restrict__ P, __nv_bfloat16* __restrict__ out) {
+                      const float* __restrict__ P, __nv_bfloat16* __restrict__ out,
+                      uint32_t* front_status) {
     grid_dep_launch();
     grid_dep_wait();  // P comes from the stage-2 GEMM
+    // After the single-launch GEMM: its ready word, quantisation count and
+    // route-tile counters go back to 0 for the next call.
+    if (front_status && blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < kStatusWords - kFrontTileWord; i += blockDim.x)
+            front_status[kFrontTileWord + i] = 0u;
+        if (threadIdx.x == 0) {
+            front_status[15] = 0u;
+            front_status[kFrontQuantWord] = 0u;
+        }
+    }
     const int n4 = D / 4;
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)T * n4) return;
@@ -297,7 +308,7 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
-                          const WsPtrs& ws, cudaStream_t stream) {
+                          const WsPtrs& ws, bool clear_ready, cudaStream_t stream) {
     const long total = (long)T * (D / 4);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((total + 255) / 256));
@@ -309,7 +320,8 @@ cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, v
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, moe_reduce_kernel, topk_ids, T, K, E, D,
-                              static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out));
+                              static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out),
+                              clear_ready ? ws.status : static_cast<uint32_t*>(nullptr));
 }
 
 // ============================================================== wait self-check

@@ -35,6 +35,15 @@ def moe():
     return m
 
 
+@pytest.fixture(params=[0, 1], ids=["separate_kernels", "single_launch"])
+def launch_mode(request, moe):
+    """Both launch modes: routing and quantisation as their own kernels, or inside
+    the GEMM kernel (single launch; results must be identical)."""
+    moe.set_single_launch(request.param)
+    yield request.param
+    moe.set_single_launch(2)
+
+
 def _threads():
     return max(1, min(32, os.cpu_count() or 1))
 
@@ -174,17 +183,17 @@ def full_check(moe, w, inp, tokens=None):
 
 # ------------------------------------------------------------------ workloads
 
-def test_tiny_workload(moe):
+def test_tiny_workload(moe, launch_mode):
     w = workloads.WORKLOADS[workloads.TINY]
     full_check(moe, w, workloads.make_inputs(w))
 
 
-def test_decode_t16_full(moe):
+def test_decode_t16_full(moe, launch_mode):
     w = workloads.WORKLOADS[workloads.DECODE_T16]
     full_check(moe, w, workloads.make_inputs(w))
 
 
-def test_decode_t128_full(moe):
+def test_decode_t128_full(moe, launch_mode):
     w = workloads.WORKLOADS["decode_T128_D7168_I256_E257_K9"]
     full_check(moe, w, workloads.make_inputs(w))
 
@@ -208,18 +217,18 @@ def _small(T=16, D=256, I=128, E=9, K=3, seed=0):
     return w, workloads.make_inputs(w, seed=seed)
 
 
-def test_single_token(moe):
+def test_single_token(moe, launch_mode):
     w, inp = _small(T=1)
     full_check(moe, w, inp)
 
 
-def test_all_routes_on_one_expert(moe):
+def test_all_routes_on_one_expert(moe, launch_mode):
     w, inp = _small(T=40, E=9, K=1)
     inp["topk_ids"][:] = 4
     full_check(moe, w, inp)
 
 
-def test_exactly_full_blocks_and_duplicates(moe):
+def test_exactly_full_blocks_and_duplicates(moe, launch_mode):
     # expert 2 receives exactly 32 routes (two full blocks); token 0 repeats an expert
     w, inp = _small(T=32, E=5, K=2)
     ids = inp["topk_ids"]
@@ -231,7 +240,7 @@ def test_exactly_full_blocks_and_duplicates(moe):
     full_check(moe, w, inp)
 
 
-def test_invalid_ids_and_empty_rows(moe):
+def test_invalid_ids_and_empty_rows(moe, launch_mode):
     w, inp = _small(T=20, E=9, K=3)
     ids = inp["topk_ids"]
     ids[0, :] = -1            # a token with no valid route -> exact zero row
@@ -241,13 +250,13 @@ def test_invalid_ids_and_empty_rows(moe):
     full_check(moe, w, inp)
 
 
-def test_dense_shape_small(moe):
+def test_dense_shape_small(moe, launch_mode):
     # K = 512-multiple contraction with several pipeline stages, 128-row tiles
     w, inp = _small(T=64, D=1024, I=512, E=3, K=2)
     full_check(moe, w, inp)
 
 
-def test_large_tiles_mid_shape(moe):
+def test_large_tiles_mid_shape(moe, launch_mode):
     w, inp = _small(T=256, D=512, I=256, E=5, K=3)
     full_check(moe, w, inp)
 
@@ -260,7 +269,7 @@ def test_empty_batch(moe):
     del m
 
 
-def test_closed_form_bit_exact(moe):
+def test_closed_form_bit_exact(moe, launch_mode):
     """All-ones case from tests/golden/closed_form.txt: exact in every step."""
     D, I, E, K, T = 256, 128, 1, 1, 1
     hidden = torch.ones(T, D, dtype=torch.bfloat16)
@@ -278,7 +287,7 @@ def test_closed_form_bit_exact(moe):
     assert (out.float().cpu() == 3145728.0).all()
 
 
-def test_deterministic_repeat(moe):
+def test_deterministic_repeat(moe, launch_mode):
     w = workloads.WORKLOADS[workloads.TINY]
     inp = workloads.make_inputs(w)
     m, t, out = run_gpu(moe, inp, w)
@@ -288,6 +297,26 @@ def test_deterministic_repeat(moe):
                        t["topk_ids"], t["topk_weights"])
         torch.cuda.synchronize()
         assert torch.equal(o2.view(torch.int16), ref.view(torch.int16))
+
+
+def test_launch_modes_bitwise_identical(moe):
+    """Single-launch mode reproduces the separate-kernel output and workspace
+    routing arrays bit for bit (same routing order, same quantisation)."""
+    w = workloads.WORKLOADS[workloads.DECODE_T16]
+    inp = workloads.make_inputs(w, seed=3)
+    outs, sids = [], []
+    for mode in (0, 1):
+        moe.set_single_launch(mode)
+        try:
+            m, t, out = run_gpu(moe, inp, w)
+            torch.cuda.synchronize()
+            assert m.device_status() == 0
+            outs.append(out.view(torch.int16).cpu())
+            sids.append(m.region("sorted_ids", torch.int32, (m.plan.cap,)).cpu().clone())
+        finally:
+            moe.set_single_launch(2)
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(sids[0], sids[1])
 
 
 # ------------------------------------------------------------------ failure reporting
