@@ -99,6 +99,30 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
                                int d_inter, int E, int topk, cudaStream_t stream);
 
 /*
+ * Forward with padded weight storage (the d_hidden_pad / d_expert_pad of
+ * solution.py's _Cfg and flower_moe.py's custom_kernel: weights stored with
+ * padded dimensions, activations and output with the logical ones).
+ *   hidden   bf16 [T, d_model];  out bf16 [T, d_model]
+ *   w13      u8 [E, 2*d_inter_pad, d_model_pad/2], rows [0, d_inter_pad) gate,
+ *            [d_inter_pad, 2*d_inter_pad) up; w13_scale u8 [E, 2*d_inter_pad, d_model_pad/32]
+ *   w2       u8 [E, d_model_pad, d_inter_pad/2];  w2_scale u8 [E, d_model_pad, d_inter_pad/32]
+ * The result is the forward of the logical problem: the weights' first d_inter
+ * gate rows, first d_inter up rows, first d_model columns (w13) and the first
+ * d_model rows and d_inter columns (w2).  d_model, d_inter: multiples of 32 (one
+ * scale block), at most the padded sizes; the padded sizes as for
+ * moe_mxfp4_forward.  The padding may hold any e2m1 codes but no scale byte 255
+ * (NaN): it is multiplied by zeros.  The workspace is that of the padded shape
+ * (moe_mxfp4_workspace_size(T, d_model_pad, d_inter_pad, E, topk)).
+ * moe_mxfp4_forward(..., d_model, d_inter, ...) is this call with no padding.
+ */
+moe_status_t moe_mxfp4_forward_padded(const void* hidden, const void* w13, const void* w13_scale,
+                                      const void* w2, const void* w2_scale,
+                                      const int32_t* topk_ids, const float* topk_weights,
+                                      void* out, int T, int d_model, int d_inter,
+                                      int d_model_pad, int d_inter_pad, int E, int topk,
+                                      cudaStream_t stream);
+
+/*
  * Forward without any device allocation, for callers that cannot allocate.
  * (This entry point has no counterpart in the pages; it is a deployment aid.)
  *

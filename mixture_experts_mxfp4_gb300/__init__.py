@@ -48,6 +48,7 @@ EXPORTS = [
     "moe_mxfp4_check_wait_timeout",
     "moe_mxfp4_set_single_launch",
     "moe_mxfp4_call_launches",
+    "moe_mxfp4_forward_padded",
 ]
 
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
@@ -101,6 +102,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_set_workspace.argtypes = [P, ctypes.c_size_t]
     lib.moe_mxfp4_forward.restype = i
     lib.moe_mxfp4_forward.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P]
+    lib.moe_mxfp4_forward_padded.restype = i
+    lib.moe_mxfp4_forward_padded.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, i, i, P]
     lib.moe_mxfp4_status_string.restype = ctypes.c_char_p
     lib.moe_mxfp4_status_string.argtypes = [i]
     lib.moe_mxfp4_last_device_status.restype = i
@@ -148,6 +151,17 @@ def get_plan(T, d_model, d_inter, E, topk) -> Plan:
 def set_workspace(ptr: int, nbytes: int):
     _check(load_library().moe_mxfp4_set_workspace(ctypes.c_void_p(ptr), nbytes),
            "moe_mxfp4_set_workspace")
+
+
+def forward_padded_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out,
+                       T, d_model, d_inter, d_model_pad, d_inter_pad, E, topk,
+                       stream: int = 0) -> int:
+    """Raw-pointer call of moe_mxfp4_forward_padded; returns the status code."""
+    return int(load_library().moe_mxfp4_forward_padded(
+        ctypes.c_void_p(hidden), ctypes.c_void_p(w13), ctypes.c_void_p(w13_scale),
+        ctypes.c_void_p(w2), ctypes.c_void_p(w2_scale), ctypes.c_void_p(topk_ids),
+        ctypes.c_void_p(topk_weights), ctypes.c_void_p(out), T, d_model, d_inter,
+        d_model_pad, d_inter_pad, E, topk, ctypes.c_void_p(stream)))
 
 
 def forward_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out,
@@ -224,14 +238,18 @@ class MoeMXFP4:
     """One MoE layer shape with its own device workspace (a torch uint8 tensor).
 
     The workspace is registered for the current device on every call, so several
-    instances can coexist as long as their calls are ordered on the GPU.
+    instances can coexist as long as their calls are ordered on the GPU.  With
+    d_model_pad / d_inter_pad the weights are stored with those padded sizes
+    (moe_mxfp4_forward_padded); hidden and out keep d_model columns.
     """
 
-    def __init__(self, T, d_model, d_inter, E, topk, device="cuda"):
+    def __init__(self, T, d_model, d_inter, E, topk, device="cuda", d_model_pad=None,
+                 d_inter_pad=None):
         import torch
 
         self.shape = (T, d_model, d_inter, E, topk)
-        self.plan = get_plan(T, d_model, d_inter, E, topk)
+        self.pad = (d_model_pad or d_model, d_inter_pad or d_inter)
+        self.plan = get_plan(T, self.pad[0], self.pad[1], E, topk)
         n = max(int(self.plan.workspace_bytes), 256)
         # zero-filled: the status region must start at zero (the calls keep it so)
         self.workspace = torch.zeros(n + 256, dtype=torch.uint8, device=device)
@@ -269,10 +287,17 @@ class MoeMXFP4:
         if stream is None:
             stream = torch.cuda.current_stream(hidden.device).cuda_stream
         set_workspace(self.ws_ptr, self.ws_bytes)
-        code = forward_ptr(hidden.data_ptr(), w13.data_ptr(), w13_scale.data_ptr(), w2.data_ptr(),
-                           w2_scale.data_ptr(), topk_ids.data_ptr(), topk_weights.data_ptr(),
-                           out.data_ptr(), T, D, I, E, K, stream)
-        _check(code, "moe_mxfp4_forward")
+        if self.pad == (D, I):
+            code = forward_ptr(hidden.data_ptr(), w13.data_ptr(), w13_scale.data_ptr(),
+                               w2.data_ptr(), w2_scale.data_ptr(), topk_ids.data_ptr(),
+                               topk_weights.data_ptr(), out.data_ptr(), T, D, I, E, K, stream)
+            _check(code, "moe_mxfp4_forward")
+        else:
+            code = forward_padded_ptr(hidden.data_ptr(), w13.data_ptr(), w13_scale.data_ptr(),
+                                      w2.data_ptr(), w2_scale.data_ptr(), topk_ids.data_ptr(),
+                                      topk_weights.data_ptr(), out.data_ptr(), T, D, I,
+                                      self.pad[0], self.pad[1], E, K, stream)
+            _check(code, "moe_mxfp4_forward_padded")
         return out
 
     def device_status(self, stream=None) -> int:

@@ -394,6 +394,14 @@ moe_status_t validate_forward(const void* hidden, const void* w13, const void* w
     return MOE_OK;
 }
 
+// Logical sizes of a padded call: multiples of 32 (one scale block), at least
+// 32, at most the stored sizes.
+moe_status_t validate_padded(int D, int I, int Dl, int Il) {
+    if (Dl < 32 || Il < 32 || Dl % 32 != 0 || Il % 32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (Dl > D || Il > I) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
 // The launch sequence of one forward call on the workspace at `base` (at least
 // workspace_bytes of the shape's plan, 256-byte aligned); arguments validated.
 }  // namespace moe
@@ -508,7 +516,7 @@ namespace moe {
 moe_status_t forward_on_workspace(const void* hidden, const void* w13, const void* w13_scale,
                                   const void* w2, const void* w2_scale, const int32_t* topk_ids,
                                   const float* topk_weights, void* out, int T, int D, int I, int E,
-                                  int K, void* base, int dev, cudaStream_t stream) {
+                                  int K, int Dl, int Il, void* base, int dev, cudaStream_t stream) {
     LaunchState state;
     if (!launch_state(dev, w13, w13_scale, w2, w2_scale, T, D, I, E, K, base, &state))
         return MOE_ERR_CUDA;
@@ -535,6 +543,8 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     g.hidden = hidden;
     g.T = T;
     g.cap = pl.cap;
+    g.Dl = Dl;
+    g.Il = Il;
     if (front) g.ws.tile_done = ws.status + kFrontTileWord;  // zero between calls
     mark(0);
     if (!front) {
@@ -544,14 +554,15 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     }
     mark(1);
     if (!front) {
-        if (launch_quant(hidden, T, K, D, pl.a1s_stride, ws, stream) != cudaSuccess)
+        if (launch_quant(hidden, T, K, D, Dl, pl.a1s_stride, ws, stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     mark(2);
     if (launch_gemm(st->maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);
     // on the single-launch path the top-k sum also clears the ready word for the next call
-    if (launch_reduce(topk_ids, T, K, E, D, out, ws, front, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_reduce(topk_ids, T, K, E, D, Dl, out, ws, front, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
     mark(4);
     if (timed) tm.recorded = true;
     return MOE_OK;
@@ -571,9 +582,20 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
                                const void* w2, const void* w2_scale, const int32_t* topk_ids,
                                const float* topk_weights, void* out, int T, int d_model,
                                int d_inter, int E, int topk, cudaStream_t stream) {
-    const int D = d_model, I = d_inter, K = topk;
+    return moe_mxfp4_forward_padded(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights,
+                                    out, T, d_model, d_inter, d_model, d_inter, E, topk, stream);
+}
+
+moe_status_t moe_mxfp4_forward_padded(const void* hidden, const void* w13, const void* w13_scale,
+                                      const void* w2, const void* w2_scale,
+                                      const int32_t* topk_ids, const float* topk_weights,
+                                      void* out, int T, int d_model, int d_inter,
+                                      int d_model_pad, int d_inter_pad, int E, int topk,
+                                      cudaStream_t stream) {
+    const int D = d_model_pad, I = d_inter_pad, K = topk;
     moe_status_t st = validate_forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
                                        topk_weights, out, T, D, I, E, K);
+    if (st == MOE_OK) st = validate_padded(D, I, d_model, d_inter);
     if (st != MOE_OK || T == 0) return st;
     const size_t need = plan_workspace_bytes(T, D, I, E, K);
     int dev = 0;
@@ -587,7 +609,7 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
     }
     if (!base || ws_bytes < need) return MOE_ERR_WORKSPACE;
     return forward_on_workspace(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out,
-                                T, D, I, E, K, base, dev, stream);
+                                T, D, I, E, K, d_model, d_inter, base, dev, stream);
 }
 
 moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream) {

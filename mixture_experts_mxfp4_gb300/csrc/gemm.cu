@@ -271,21 +271,26 @@ constexpr int kFrontPreStages = 2;
 // First 16-byte load of an epilogue thread's quantisation share, issued before
 // the routing and before any weight copy (the copies of the first stages fill
 // the memory system's queues for microseconds), and an L2 prefetch of the
-// CTA's later passes; zeros past the end.  The hidden states are contiguous,
-// so block j of 32 elements starts at byte 64 j.
+// CTA's later passes; zeros past the end and for padding blocks (columns past
+// the logical d_model).  Block j = (token t, block gb) of the D/32 blocks per
+// row reads 64 bytes at t * 2 Dl + 64 gb; without padding, at 64 j.
 __device__ __forceinline__ uint4 front_quant_first_load(const GemmParams& p) {
     const int et = (int)threadIdx.x - 128;
-    const long total = (long)p.T * (p.D / 32);
+    const int nblk = p.D / 32;
+    const long total = (long)p.T * nblk;
     const uint8_t* hid = static_cast<const uint8_t*>(p.hidden);
     constexpr int kLines = kFrontQuantBlocks * 64 / 128;  // 128-byte lines per pass
-    if (et < kLines) {
+    if (et < kLines && p.Dl == p.D) {
         for (long jb = (long)(blockIdx.x + gridDim.x) * kFrontQuantBlocks; jb < total;
              jb += (long)gridDim.x * kFrontQuantBlocks)
             if (jb * 64 + et * 128 < total * 64) prefetch_l2(hid + jb * 64 + et * 128);
     }
     const long j = (long)blockIdx.x * kFrontQuantBlocks + (et >> 2);
     if (j >= total) return make_uint4(0, 0, 0, 0);
-    return ld_nc_v4_now(hid + j * 64 + (et & 3) * 16);
+    const int t = (int)(j / nblk);
+    const int gb = (int)(j - (long)t * nblk);
+    if (gb >= p.Dl / 32) return make_uint4(0, 0, 0, 0);
+    return ld_nc_v4_now(hid + (size_t)t * p.Dl * 2 + (size_t)gb * 64 + (et & 3) * 16);
 }
 
 // Bounded wait (one thread) until a global word equals `want` (equal) or
@@ -334,8 +339,11 @@ __device__ void front_quant(const GemmParams& p, const int* pos, uint4 first16) 
         const int t = active ? (int)(j / nblk) : 0;
         const int gb = active ? (int)(j - (long)t * nblk) : 0;
         uint4 raw = first16;
-        if (!first && active)
-            raw = __ldg(reinterpret_cast<const uint4*>(hidden + (size_t)t * D) + gb * 4 + qd);
+        if (!first) {
+            raw = make_uint4(0, 0, 0, 0);  // padding blocks (past the logical d_model): zero
+            if (active && gb < p.Dl / 32)
+                raw = __ldg(reinterpret_cast<const uint4*>(hidden + (size_t)t * p.Dl) + gb * 4 + qd);
+        }
         first = false;
         uint32_t sc;
         const uint32_t word = front_quant8(raw, sc);  // whole warp
@@ -952,7 +960,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                     const float gv = v[i];
                                     const float u = xg[(q4 * 16 + i) * 32 + lane];
                                     const float sg = gv / (1.0f + expf(-gv));
-                                    const float hv = __bfloat162float(__float2bfloat16_rn(sg * u));
+                                    // features past the logical d_inter (padding): zero
+                                    const float hv = feat < p.Il
+                                                         ? __bfloat162float(__float2bfloat16_rn(sg * u))
+                                                         : 0.0f;
                                     const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
                                     const uint32_t amax = __reduce_max_sync(0xffffffffu, hb);
                                     const uint32_t sbyte = mx_scale_byte(amax);

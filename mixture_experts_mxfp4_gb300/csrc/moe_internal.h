@@ -52,7 +52,8 @@ struct StageGeom {
 // its stage-2 items, through one shared-memory ring.
 struct GemmParams {
     WsPtrs ws;
-    int D, I, E, K, R;
+    int D, I, E, K, R;  // D, I: stored (padded) sizes
+    int Dl, Il;         // logical d_model, d_inter (multiples of 32, <= D, I)
     int tile_rows;      // maximum MMA N (routes per tile), multiple of 16, <= 128
     StageGeom g[2];     // stage 1, stage 2
     int num_stages;     // shared-memory ring depth
@@ -105,19 +106,23 @@ moe_status_t validate_forward(const void* hidden, const void* w13, const void* w
                               const float* topk_weights, const void* out, int T, int D, int I,
                               int E, int K);
 size_t plan_workspace_bytes(int T, int D, int I, int E, int K);
+// D, I: stored (padded) sizes; Dl, Il: logical sizes.
+moe_status_t validate_padded(int D, int I, int Dl, int Il);
 moe_status_t forward_on_workspace(const void* hidden, const void* w13, const void* w13_scale,
                                   const void* w2, const void* w2_scale, const int32_t* topk_ids,
                                   const float* topk_weights, void* out, int T, int D, int I, int E,
-                                  int K, void* base, int dev, cudaStream_t stream);
+                                  int K, int Dl, int Il, void* base, int dev, cudaStream_t stream);
 
 cudaError_t launch_check_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, int K, int E,
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream);
-cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride,
+// hidden rows hold Dl elements; quantised rows D (zero blocks past Dl)
+cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride,
                          const WsPtrs& ws, cudaStream_t stream);
 // clear_ready: also clear the single-launch words of the status region (after that GEMM)
-cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
+// P rows hold D columns; out rows Dl
+cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, int Dl, void* out,
                           const WsPtrs& ws, bool clear_ready, cudaStream_t stream);
 // maps: stage-1 A, SA, B, SB, then stage-2 A, SA, B, SB
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,

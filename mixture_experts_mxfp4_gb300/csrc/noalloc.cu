@@ -65,5 +65,6 @@ extern "C" moe_status_t moe_mxfp4_forward_noalloc(const void* hidden, const void
     void* base = static_workspace(dev);
     if (!base) return MOE_ERR_CUDA;
     return moe::forward_on_workspace(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights,
-                                     out, T, d_model, d_inter, E, topk, base, dev, stream);
+                                     out, T, d_model, d_inter, E, topk, d_model, d_inter, base,
+                                     dev, stream);
 }

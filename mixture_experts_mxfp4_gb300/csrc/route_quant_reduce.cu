@@ -202,7 +202,7 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
 constexpr int kQuantThreads = 256;
 
 __global__ void __launch_bounds__(kQuantThreads)
-    moe_quant_kernel(const __nv_bfloat16* __restrict__ hidden, int T, int K, int D,
+    moe_quant_kernel(const __nv_bfloat16* __restrict__ hidden, int T, int K, int D, int Dl,
                      int a1s_stride, WsPtrs ws) {
     grid_dep_launch();
     const int nblk = D / 32;
@@ -210,10 +210,10 @@ __global__ void __launch_bounds__(kQuantThreads)
     const bool active = gid < (long)T * nblk;
     const int t = active ? (int)(gid / nblk) : 0;
     const int g = active ? (int)(gid - (long)t * nblk) : 0;
-    uint4 codes = make_uint4(0, 0, 0, 0);
+    uint4 codes = make_uint4(0, 0, 0, 0);  // (padding blocks past Dl stay zero, scale 0)
     uint32_t s = 0;
-    if (active) {
-        const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)t * D) + g * 4;
+    if (active && g < Dl / 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)t * Dl) + g * 4;
         uint4 raw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) raw[i] = __ldg(src + i);
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
 }
 
-cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride,
+cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride,
                          const WsPtrs& ws, cudaStream_t stream) {
     const long total = (long)T * (D / 32);
     cudaLaunchConfig_t cfg = {};
@@ -258,18 +258,19 @@ cudaError_t launch_quant(const void* hidden, int T, int K, int D, int a1s_stride
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, moe_quant_kernel,
-                              reinterpret_cast<const __nv_bfloat16*>(hidden), T, K, D, a1s_stride,
-                              ws);
+                              reinterpret_cast<const __nv_bfloat16*>(hidden), T, K, D, Dl,
+                              a1s_stride, ws);
 }
 
 // ============================================================== top-k sum
 //
 // out[t, n] = bf16( sum over k ascending of P[t*K + k, n] ), skipping routes
-// whose id is outside [0, E).  P already holds w[t,k] * y (stage-2 epilogue).
-// Deterministic: one thread owns four outputs and adds in a fixed order.
+// whose id is outside [0, E), for the Dl logical columns (P rows hold D).
+// P already holds w[t,k] * y (stage-2 epilogue).  Deterministic: one thread
+// owns four outputs and adds in a fixed order.
 
 __global__ void __launch_bounds__(256)
-    moe_reduce_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int D,
+    moe_reduce_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int D, int Dl,
                       const float* __restrict__ P, __nv_bfloat16* __restrict__ out,
                       uint32_t* front_status) {
     grid_dep_launch();
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(256)
             front_status[kFrontQuantWord] = 0u;
         }
     }
-    const int n4 = D / 4;
+    const int n4 = Dl / 4;
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)T * n4) return;
     const int t = (int)(idx / n4);
@@ -304,12 +305,12 @@ __global__ void __launch_bounds__(256)
     uint2 pk;
     pk.x = *reinterpret_cast<uint32_t*>(&lo);
     pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + (size_t)t * D + 4 * c) = pk;
+    *reinterpret_cast<uint2*>(out + (size_t)t * Dl + 4 * c) = pk;
 }
 
-cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, void* out,
+cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, int Dl, void* out,
                           const WsPtrs& ws, bool clear_ready, cudaStream_t stream) {
-    const long total = (long)T * (D / 4);
+    const long total = (long)T * (Dl / 4);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((total + 255) / 256));
     cfg.blockDim = dim3(256);
@@ -319,7 +320,7 @@ cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, v
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_reduce_kernel, topk_ids, T, K, E, D,
+    return cudaLaunchKernelEx(&cfg, moe_reduce_kernel, topk_ids, T, K, E, D, Dl,
                               static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out),
                               clear_ready ? ws.status : static_cast<uint32_t*>(nullptr));
 }

@@ -113,3 +113,20 @@ def test_validation_codes_without_device(lib):
         moe.get_plan(16, 256, 100, 9, 3)
     # workspace registration checks alignment before any device call
     assert lib.moe_mxfp4_set_workspace(ctypes.c_void_p(good + 64), 1024) == 3
+
+
+def test_padded_validation_codes_without_device(lib):
+    import mixture_experts_mxfp4_gb300 as moe
+
+    good = 1 << 20
+    args = [good] * 8
+
+    def call(T=16, D=224, I=96, Dp=256, Ip=128, E=9, K=3):
+        return moe.forward_padded_ptr(*args, T, D, I, Dp, Ip, E, K, 0)
+
+    assert call(D=200) == 2       # logical size not a multiple of 32
+    assert call(I=16) == 2        # below one scale block
+    assert call(D=288) == 1       # logical size above the stored one
+    assert call(Ip=192) == 2      # stored size not 128, 256 or a multiple of 512
+    assert call(T=0) == 0
+    assert moe.call_launches(16, 255, 128, 9, 3) == -1

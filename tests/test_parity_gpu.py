@@ -299,6 +299,63 @@ def test_deterministic_repeat(moe, launch_mode):
         assert torch.equal(o2.view(torch.int16), ref.view(torch.int16))
 
 
+def _padded_weights(inp, Dp, Ip, seed=7):
+    """The logical weights inside padded storage (w13 gate rows at 0, up rows at Ip),
+    with random e2m1 codes and finite scale bytes in the padding."""
+    g = torch.Generator().manual_seed(seed)
+    E, I2, Dh = inp["w13"].shape
+    I, D = I2 // 2, Dh * 2
+    w13 = torch.randint(0, 256, (E, 2 * Ip, Dp // 2), generator=g, dtype=torch.uint8)
+    s13 = torch.randint(100, 141, (E, 2 * Ip, Dp // 32), generator=g, dtype=torch.uint8)
+    w13[:, :I, : D // 2] = inp["w13"][:, :I]
+    w13[:, Ip:Ip + I, : D // 2] = inp["w13"][:, I:]
+    s13[:, :I, : D // 32] = inp["w13_scale"][:, :I]
+    s13[:, Ip:Ip + I, : D // 32] = inp["w13_scale"][:, I:]
+    w2 = torch.randint(0, 256, (E, Dp, Ip // 2), generator=g, dtype=torch.uint8)
+    s2 = torch.randint(100, 141, (E, Dp, Ip // 32), generator=g, dtype=torch.uint8)
+    w2[:, :D, : I // 2] = inp["w2"]
+    s2[:, :D, : I // 32] = inp["w2_scale"]
+    return {**inp, "w13": w13, "w13_scale": s13, "w2": w2, "w2_scale": s2}
+
+
+@pytest.mark.parametrize("T,D,I,Dp,Ip,E,K", [
+    (24, 224, 96, 256, 128, 5, 3),      # both dims padded inside one stage
+    (40, 992, 416, 1024, 512, 9, 3),    # multi-stage contraction with a padded tail
+    (16, 7168, 224, 7168, 256, 33, 9),  # d_model unpadded, d_inter padded
+])
+def test_padded_dims(moe, launch_mode, T, D, I, Dp, Ip, E, K):
+    """Padded weight storage computes the logical problem: the oracle on the
+    unpadded weights; routing and quantised hidden rows bit-exact, padding columns
+    of the quantised rows zero."""
+    w = workloads.custom(T, D, I, E, K)
+    inp = workloads.make_inputs(w, seed=11)
+    pin = _padded_weights(inp, Dp, Ip)
+    dev = torch.device("cuda")
+    m = moe.MoeMXFP4(T, D, I, E, K, d_model_pad=Dp, d_inter_pad=Ip)
+    t = {k: v.to(dev) for k, v in pin.items()}
+    out = m.forward(t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"],
+                    t["topk_ids"], t["topk_weights"])
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    assert out.shape == (T, D)
+    npi = workloads.to_numpy(inp)
+    routing = oracle.route(npi["topk_ids"], npi["topk_weights"], E, 16, cap=m.plan.cap)
+    ref = oracle.forward(**npi, threads=_threads(), want_h=False)
+    cap = m.plan.cap
+    a1q = m.region("a1q", torch.uint8, (cap, Dp // 2)).cpu().numpy()
+    a1s = m.region("a1s", torch.uint8, (cap, m.plan.a1s_stride)).cpu().numpy()
+    a2q = m.region("a2q", torch.uint8, (cap, Ip // 2)).cpu().numpy()
+    a2s = m.region("a2s", torch.uint8, (cap, m.plan.a2s_stride)).cpu().numpy()
+    ws = {"a1q": a1q[:, : D // 2], "a1s": a1s, "a2q": a2q[:, : I // 2], "a2s": a2s}
+    check_a1(ws, ref, routing, w)
+    check_a2(ws, ref, routing, w)
+    n = int(routing["num_valid"][0])
+    valid = routing["sorted_ids"][:n] < w.R
+    assert (a1q[:n][valid, D // 2:] == 0).all()
+    assert (a2q[:n][valid, I // 2:] == 0).all()
+    check_out(out, ref)
+
+
 def test_launch_modes_bitwise_identical(moe):
     """Single-launch mode reproduces the separate-kernel output and workspace
     routing arrays bit for bit (same routing order, same quantisation)."""
