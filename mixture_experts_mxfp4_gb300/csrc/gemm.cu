@@ -937,6 +937,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (phs == 0) {
                     const int n0 = x.f * 64;  // first feature of the tile
                     {
+                        // Per chunk of 16 routes, in two halves of 8: the four warps put
+                        // their accumulator rows (gate features 0-31, 32-63, up 0-31,
+                        // 32-63) into the exchange buffer; then thread t takes route
+                        // t / 16 of the half, feature block (t / 8) % 2 and its 4 features
+                        // 4 (t % 8) .. +3, so the block's amax spans 8 lanes and every
+                        // thread does the same independent work.  A half whose 8 slots
+                        // are all padding is skipped (the same decision in every warp).
+                        const int tq = (int)(q4 * 32u + lane);
+                        const int ri = tq >> 4, bb = (tq >> 3) & 1, sub = tq & 7;
+                        const int feat0 = n0 + 32 * bb;  // first feature of this thread's block
                         for (int c = 0; c < nchunks; ++c) {
                             float v[16];
                             load_acc(c, v);
@@ -944,47 +954,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 release();
                                 released = true;
                             }
-                            if (q4 >= 2) {
+                            const int rid_l =
+                                c == 0 ? rid_pre : ld_route(front, p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
+                            const uint32_t valid = __ballot_sync(0xffffffffu, rid_l < R);
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) xg[((q4 - 2) * 16 + i) * 32 + lane] = v[i];
-                            }
-                            named_bar_sync(bar_id, 128);
-                            if (q4 < 2) {
-                                const int rid_l =
-                                    c == 0 ? rid_pre : ld_route(front, p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
-                                const int feat = n0 + 32 * (int)q4;  // first feature of this warp's block
+                            for (int hh = 0; hh < 2; ++hh) {
+                                if (((valid >> (8 * hh)) & 0xffu) == 0u) continue;  // all padding
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const int rid = __shfl_sync(0xffffffffu, rid_l, i);
-                                    if (rid >= R) continue;  // padding slot (warp-uniform)
-                                    const float gv = v[i];
-                                    const float u = xg[(q4 * 16 + i) * 32 + lane];
-                                    const float sg = gv / (1.0f + expf(-gv));
+                                for (int i = 0; i < 8; ++i) xg[(q4 * 8 + i) * 32 + lane] = v[8 * hh + i];
+                                named_bar_sync(bar_id, 128);
+                                const float4 g4 = *reinterpret_cast<const float4*>(xg + (bb * 8 + ri) * 32 + sub * 4);
+                                const float4 u4 =
+                                    *reinterpret_cast<const float4*>(xg + ((2 + bb) * 8 + ri) * 32 + sub * 4);
+                                const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+                                const float us[4] = {u4.x, u4.y, u4.z, u4.w};
+                                float hv[4];
+                                uint32_t amax = 0;
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const float sg = gs[j] / (1.0f + expf(-gs[j]));
                                     // features past the logical d_inter (padding): zero
-                                    const float hv = feat < p.Il
-                                                         ? __bfloat162float(__float2bfloat16_rn(sg * u))
-                                                         : 0.0f;
-                                    const uint32_t hb = __float_as_uint(hv) & 0x7fffffffu;
-                                    const uint32_t amax = __reduce_max_sync(0xffffffffu, hb);
-                                    const uint32_t sbyte = mx_scale_byte(amax);
-                                    const uint32_t code =
-                                        e2m1_code(hv, sbyte, mx_inv_scale(sbyte == 255u ? 0u : sbyte));
-                                    const uint32_t nb = __shfl_down_sync(0xffffffffu, code, 1);
-                                    const uint32_t byte = (code | (nb << 4)) & 0xffu;
-                                    const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
-                                    const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
-                                    const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
-                                    const int slot = x.row0 + 16 * c + i;
-                                    if ((lane & 7u) == 0) {
-                                        const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-                                        *reinterpret_cast<uint32_t*>(p.ws.a2q + (size_t)slot * (p.I / 2) +
-                                                                     feat / 2 + lane / 2) = word;
-                                    }
-                                    if (lane == 0)
-                                        p.ws.a2s[(size_t)slot * p.a2s_stride + feat / 32] = (uint8_t)sbyte;
+                                    hv[j] = feat0 < p.Il ? __bfloat162float(__float2bfloat16_rn(sg * us[j])) : 0.0f;
+                                    amax = max(amax, __float_as_uint(hv[j]) & 0x7fffffffu);
                                 }
+                                amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                                amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                                amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+                                const uint32_t sbyte = mx_scale_byte(amax);
+                                const float inv = mx_inv_scale(sbyte == 255u ? 0u : sbyte);
+                                uint32_t half16 = 0;  // 4 codes, low nibble = lower feature
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) half16 |= e2m1_code(hv[j], sbyte, inv) << (4 * j);
+                                const uint32_t next16 = __shfl_down_sync(0xffffffffu, half16, 1);
+                                const int rid = __shfl_sync(0xffffffffu, rid_l, 8 * hh + ri);
+                                const int slot = x.row0 + 16 * c + 8 * hh + ri;
+                                if (rid < R) {
+                                    if ((sub & 1) == 0)
+                                        *reinterpret_cast<uint32_t*>(p.ws.a2q + (size_t)slot * (p.I / 2) + feat0 / 2 +
+                                                                     sub * 2) = half16 | (next16 << 16);
+                                    if (sub == 0) p.ws.a2s[(size_t)slot * p.a2s_stride + feat0 / 32] = (uint8_t)sbyte;
+                                }
+                                named_bar_sync(bar_id, 128);  // the buffer is refilled next
                             }
-                            named_bar_sync(bar_id, 128);
                         }
                         // This feature tile of the route tile is written: count it for the
                         // stage-2 producers, whose TMA copies (async proxy) read it.
