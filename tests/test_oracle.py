@@ -359,6 +359,49 @@ def test_dense_fp64_brute_force(tiny, T):
     np.testing.assert_array_equal(res["out_bf16"], ref_bits)
 
 
+@pytest.mark.parametrize("T", [1, 4])
+def test_w4a16_dense_fp64_brute_force(tiny, T):
+    """The oracle's bf16-activation mode (quant_act=False: no activation quantiser,
+    the bf16 SwiGLU output feeds stage 2 directly, as in solution.py's
+    _reference_forward) against fp64 dense matrices through one-hot expert masks."""
+    w, inp = tiny
+    inp = {k: (v[:T] if k in ("hidden_bits", "topk_ids", "topk_weights") else v)
+           for k, v in inp.items()}
+    ids = inp["topk_ids"]
+    D, I, E, K = w.D, w.I, w.E, w.K
+    res = oracle.forward(**inp, quant_act=False)
+    X = oracle.bf16_bits_to_f32(inp["hidden_bits"]).astype(np.float64)  # [T, D], exact
+    W13 = np_dequant(inp["w13"], inp["w13_scale"], D)
+    W2 = np_dequant(inp["w2"], inp["w2_scale"], I)
+    M = np.zeros((T, K, E))
+    for t in range(T):
+        for k in range(K):
+            M[t, k, ids[t, k]] = 1.0
+    G = np.einsum("tke,enj,tj->tkn", M, W13[:, :I], X)
+    U = np.einsum("tke,enj,tj->tkn", M, W13[:, I:], X)
+    H = G / (1.0 + np.exp(-G)) * U
+    h_or = res["h"].reshape(T, K, I).astype(np.float64)
+    absG = np.einsum("tke,enj,tj->tkn", M, np.abs(W13[:, :I]), np.abs(X))
+    absU = np.einsum("tke,enj,tj->tkn", M, np.abs(W13[:, I:]), np.abs(X))
+    bound = 2.0 ** -8 * np.abs(H) + 4 * D * 2.0 ** -24 * (absG * np.abs(U) + absU * np.abs(G)) + 1e-30
+    assert np.all(np.abs(h_or - H) <= bound)
+    # h is already a bf16 value: widening its bf16 bits gives it back
+    hb = torch.from_numpy(res["h"]).to(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(hb, res["h"])
+    # stage 2 consumes h itself (no requantisation)
+    Y = np.einsum("tke,enj,tkj->tkn", M, W2, h_or)
+    OUT = np.einsum("tk,tkn->tn", inp["topk_weights"].astype(np.float64), Y)
+    absY = np.einsum("tke,enj,tkj->tkn", M, np.abs(W2), np.abs(h_or))
+    absO = np.einsum("tk,tkn->tn", np.abs(inp["topk_weights"].astype(np.float64)), absY)
+    tol = 4 * (I + K) * 2.0 ** -24 * absO + 1e-30
+    assert np.all(np.abs(res["out_f32"].astype(np.float64) - OUT) <= tol)
+    ref_bits = torch.from_numpy(res["out_f32"]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(res["out_bf16"], ref_bits)
+    # and it differs from the quantised path (the mode switch is live)
+    q = oracle.forward(**inp)
+    assert not np.array_equal(q["out_bf16"], res["out_bf16"])
+
+
 def test_invalid_ids_contribute_nothing(tiny):
     w, inp = tiny
     ids = inp["topk_ids"].copy()
