@@ -154,9 +154,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def alg_bytes(w, ids):
+def alg_bytes(w, ids, bf16_act=False):
     """Algorithmic bytes of one forward call and of its GEMM kernel (both stages:
-    the touched experts' weights and scales, and the quantised hidden rows)."""
+    the touched experts' weights and scales, and the quantised hidden rows, or
+    the bf16 ones for the bf16-activation forward)."""
     import workloads
 
     E_t = workloads.touched_experts(ids, w.E)
@@ -166,7 +167,7 @@ def alg_bytes(w, ids):
     out = w.T * w.D * 2                            # bf16 out
     route = w.T * w.K * 8                          # ids + weights
     total = E_t * (per_expert_w13 + per_expert_w2) + act + out + route
-    gemm = E_t * (per_expert_w13 + per_expert_w2) + w.T * w.D * 17 // 32
+    gemm = E_t * (per_expert_w13 + per_expert_w2) + (w.T * w.D * 2 if bf16_act else w.T * w.D * 17 // 32)
     return total, gemm, E_t
 
 
@@ -241,7 +242,9 @@ def run_gpu(args, w, world, rank, local):
     moe.load_library()
     inp = workloads.make_inputs(w, seed=args.seed + rank)
     t = {k: v.to(dev) for k, v in inp.items()}
-    m = moe.MoeMXFP4(w.T, w.D, w.I, w.E, w.K, device=dev)
+    bf16_act = args.activations == "bf16"
+    m = moe.MoeMXFP4(w.T, w.D, w.I, w.E, w.K, device=dev,
+                     activations="bf16" if bf16_act else "mxfp4")
     out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -250,7 +253,7 @@ def run_gpu(args, w, world, rank, local):
 
     # launch mode: the library's automatic choice unless forced
     moe.set_single_launch({"auto": 2, "single": 1, "separate": 0}[args.launch])
-    launches = moe.call_launches(w.T, w.D, w.I, w.E, w.K)
+    launches = 4 if bf16_act else moe.call_launches(w.T, w.D, w.I, w.E, w.K)
     single = launches == 2
     moe.set_kernel_timing(2)
     for _ in range(args.warmup):
@@ -336,24 +339,31 @@ def run_gpu(args, w, world, rank, local):
 
     # ---- roofline of the dominant kernel (the GEMM kernel), measured live above
     ids_np = inp["topk_ids"].numpy()
-    b_total, b_gemm, e_touched = alg_bytes(w, ids_np)
+    b_total, b_gemm, e_touched = alg_bytes(w, ids_np, bf16_act)
     peak, peak_kind = measured_peaks()
     dom = max(per_kernel, key=per_kernel.get)
     g_ms = per_kernel["gemm"] / k_steps
     achieved = b_gemm / (g_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "gemm", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "traffic": profiled_traffic(),
+                "unit": "GB/s", "frac": achieved / peak,
+                # the committed ncu summary covers the default workload and configuration
+                "traffic": profiled_traffic() if (w.name == DEFAULT_WORKLOAD and not bf16_act
+                                                  and args.launch == "auto") else None,
                 "alg_bytes_per_launch": b_gemm, "peak_kind": peak_kind}
     fwd_gbs = b_total / (us_call * 1e-6) / 1e9
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 (e2m1 x e2m1, fp32 accumulate)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 x bf16 (e2m1 weights expanded in shared memory), fp32 accumulate" if bf16_act
+        else "mxfp4 (e2m1 x e2m1, fp32 accumulate)",
         "data": "synthetic (seeded; DeepSeek-R1-shaped, random weights)",
         "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_inter": w.I, "E": w.E,
                    "topk": w.K, "touched_experts": e_touched,
                    "l2": "flushed before every step (256 MiB write, untimed)",
                    "parallelism": f"replicas x{world}",
+                   "activations": "bf16 (W4A16: weights dequantised to bf16 in shared memory)"
+                   if bf16_act else "mxfp4 (quantised per 32 elements)",
                    "launch": "single (routing + quantisation inside the GEMM kernel)"
                    if single else "separate kernels"},
         "us_per_call": us_call,
@@ -384,6 +394,8 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--activations", default="mxfp4", choices=["mxfp4", "bf16"],
+                    help="bf16: the W4A16 forward (no activation quantisation)")
     ap.add_argument("--launch", default="auto", choices=["auto", "single", "separate"],
                     help="single: route and quantise inside the GEMM kernel (2 launches per "
                          "call); separate: 4 kernels; auto: the library's choice by shape")

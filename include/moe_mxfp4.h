@@ -123,6 +123,25 @@ moe_status_t moe_mxfp4_forward_padded(const void* hidden, const void* w13, const
                                       cudaStream_t stream);
 
 /*
+ * Forward with bf16 activations (W4A16): the weights as for moe_mxfp4_forward,
+ * but the hidden states are not quantised and the SwiGLU output stays bf16
+ * (b12x moe/fused/w4a16/kernel.py, W4A16GemmKernel; flower_moe.py's
+ * bf16-activation path; solution.py, _reference_forward):
+ *   out[t] = bf16( sum_k w[t,k] * W2[e] . bf16( silu(W13g[e] . x_t) * (W13u[e] . x_t) ) )
+ * with x_t the bf16 hidden row, W = e2m1 * 2^(s-127) and fp32 accumulation.  The
+ * weights are expanded to bf16 in shared memory for bf16 tensor-core MMAs.  Same
+ * arguments, shapes and errors as moe_mxfp4_forward; the registered workspace
+ * must hold moe_mxfp4_workspace_size_w4a16 bytes (its layout:
+ * moe_mxfp4_get_plan_w4a16).  Always four launches (route, row gather, GEMM
+ * kernel, top-k sum).
+ */
+moe_status_t moe_mxfp4_forward_w4a16(const void* hidden, const void* w13, const void* w13_scale,
+                                     const void* w2, const void* w2_scale,
+                                     const int32_t* topk_ids, const float* topk_weights,
+                                     void* out, int T, int d_model, int d_inter, int E, int topk,
+                                     cudaStream_t stream);
+
+/*
  * Forward without any device allocation, for callers that cannot allocate.
  * (This entry point has no counterpart in the pages; it is a deployment aid.)
  *
@@ -193,7 +212,9 @@ typedef enum {
     MOE_WS_A2S = 12,        /* u8 [cap][a2s_stride]: its e8m0 scales                          */
     MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id    */
     MOE_WS_PARTIAL = 14,    /* unused (0 bytes): no K split of stage 1                        */
-    MOE_WS_NUM_REGIONS = 15
+    MOE_WS_A1B = 15,        /* bf16 [cap][d_model]: hidden row of each slot's token (bf16-activation plan only) */
+    MOE_WS_A2B = 16,        /* bf16 [cap][d_inter]: bf16 SwiGLU output of each slot (bf16-activation plan only) */
+    MOE_WS_NUM_REGIONS = 17
 } moe_ws_region_t;
 
 typedef struct {
@@ -204,7 +225,7 @@ typedef struct {
     int a2s_stride;     /* bytes per row of MOE_WS_A2S                                   */
     int stage1_splits;  /* K splits of the stage-1 GEMM (1)                              */
     int max_tiles;      /* capacity of MOE_WS_TILES                                      */
-    int reserved;
+    int bf16_act;       /* 1: layout of the bf16-activation forward (a1q..a2s empty, a1b/a2b used) */
     size_t offset[MOE_WS_NUM_REGIONS]; /* byte offset of each region in the workspace     */
     size_t bytes[MOE_WS_NUM_REGIONS];  /* byte size of each region                        */
     size_t workspace_bytes;            /* total (== moe_mxfp4_workspace_size)              */
@@ -214,6 +235,12 @@ typedef struct {
  * touches no device.  Returns a shape/argument status like the forward call. */
 moe_status_t moe_mxfp4_get_plan(int T, int d_model, int d_inter, int E, int topk,
                                 moe_mxfp4_plan_t* plan);
+
+/* Workspace bytes and layout of the bf16-activation forward (regions a1b, a2b
+ * instead of a1q .. a2s; bf16_act = 1). */
+size_t moe_mxfp4_workspace_size_w4a16(int T, int d_model, int d_inter, int E, int topk);
+moe_status_t moe_mxfp4_get_plan_w4a16(int T, int d_model, int d_inter, int E, int topk,
+                                      moe_mxfp4_plan_t* plan);
 
 /* Version string of the library build. */
 const char* moe_mxfp4_version(void);

@@ -29,7 +29,8 @@ STATUS = {
 MOE_OK = 0
 
 REGIONS = ["status", "counters", "sorted_ids", "sorted_w", "block_expert", "seg_start",
-           "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "partial"]
+           "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "partial",
+           "a1b", "a2b"]
 
 # Exported C symbols (kept in step with include/moe_mxfp4.h).
 EXPORTS = [
@@ -49,6 +50,9 @@ EXPORTS = [
     "moe_mxfp4_set_single_launch",
     "moe_mxfp4_call_launches",
     "moe_mxfp4_forward_padded",
+    "moe_mxfp4_forward_w4a16",
+    "moe_mxfp4_workspace_size_w4a16",
+    "moe_mxfp4_get_plan_w4a16",
 ]
 
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
@@ -72,7 +76,7 @@ class Plan(ctypes.Structure):
         ("a2s_stride", ctypes.c_int),
         ("stage1_splits", ctypes.c_int),
         ("max_tiles", ctypes.c_int),
-        ("reserved", ctypes.c_int),
+        ("bf16_act", ctypes.c_int),
         ("offset", ctypes.c_size_t * len(REGIONS)),
         ("bytes", ctypes.c_size_t * len(REGIONS)),
         ("workspace_bytes", ctypes.c_size_t),
@@ -110,6 +114,12 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_last_device_status.argtypes = [P]
     lib.moe_mxfp4_get_plan.restype = i
     lib.moe_mxfp4_get_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+    lib.moe_mxfp4_get_plan_w4a16.restype = i
+    lib.moe_mxfp4_get_plan_w4a16.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+    lib.moe_mxfp4_workspace_size_w4a16.restype = ctypes.c_size_t
+    lib.moe_mxfp4_workspace_size_w4a16.argtypes = [i, i, i, i, i]
+    lib.moe_mxfp4_forward_w4a16.restype = i
+    lib.moe_mxfp4_forward_w4a16.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P]
     lib.moe_mxfp4_version.restype = ctypes.c_char_p
     lib.moe_mxfp4_version.argtypes = []
     lib.moe_mxfp4_num_kernels.restype = i
@@ -146,6 +156,24 @@ def get_plan(T, d_model, d_inter, E, topk) -> Plan:
     _check(load_library().moe_mxfp4_get_plan(T, d_model, d_inter, E, topk, ctypes.byref(pl)),
            "moe_mxfp4_get_plan")
     return pl
+
+
+def get_plan_w4a16(T, d_model, d_inter, E, topk) -> Plan:
+    """Workspace layout of the bf16-activation (W4A16) forward."""
+    pl = Plan()
+    _check(load_library().moe_mxfp4_get_plan_w4a16(T, d_model, d_inter, E, topk, ctypes.byref(pl)),
+           "moe_mxfp4_get_plan_w4a16")
+    return pl
+
+
+def forward_w4a16_ptr(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out,
+                      T, d_model, d_inter, E, topk, stream: int = 0) -> int:
+    """Raw-pointer call of moe_mxfp4_forward_w4a16; returns the status code."""
+    return int(load_library().moe_mxfp4_forward_w4a16(
+        ctypes.c_void_p(hidden), ctypes.c_void_p(w13), ctypes.c_void_p(w13_scale),
+        ctypes.c_void_p(w2), ctypes.c_void_p(w2_scale), ctypes.c_void_p(topk_ids),
+        ctypes.c_void_p(topk_weights), ctypes.c_void_p(out), T, d_model, d_inter, E, topk,
+        ctypes.c_void_p(stream)))
 
 
 def set_workspace(ptr: int, nbytes: int):
@@ -240,16 +268,24 @@ class MoeMXFP4:
     The workspace is registered for the current device on every call, so several
     instances can coexist as long as their calls are ordered on the GPU.  With
     d_model_pad / d_inter_pad the weights are stored with those padded sizes
-    (moe_mxfp4_forward_padded); hidden and out keep d_model columns.
+    (moe_mxfp4_forward_padded); hidden and out keep d_model columns.  With
+    activations="bf16" the forward keeps the activations in bf16 (W4A16,
+    moe_mxfp4_forward_w4a16).
     """
 
     def __init__(self, T, d_model, d_inter, E, topk, device="cuda", d_model_pad=None,
-                 d_inter_pad=None):
+                 d_inter_pad=None, activations="mxfp4"):
         import torch
 
+        if activations not in ("mxfp4", "bf16"):
+            raise ValueError("activations must be 'mxfp4' or 'bf16'")
         self.shape = (T, d_model, d_inter, E, topk)
         self.pad = (d_model_pad or d_model, d_inter_pad or d_inter)
-        self.plan = get_plan(T, self.pad[0], self.pad[1], E, topk)
+        self.bf16_act = activations == "bf16"
+        if self.bf16_act and self.pad != (d_model, d_inter):
+            raise ValueError("padded storage is not available with bf16 activations")
+        self.plan = (get_plan_w4a16 if self.bf16_act else get_plan)(T, self.pad[0], self.pad[1], E,
+                                                                       topk)
         n = max(int(self.plan.workspace_bytes), 256)
         # zero-filled: the status region must start at zero (the calls keep it so)
         self.workspace = torch.zeros(n + 256, dtype=torch.uint8, device=device)
@@ -287,7 +323,12 @@ class MoeMXFP4:
         if stream is None:
             stream = torch.cuda.current_stream(hidden.device).cuda_stream
         set_workspace(self.ws_ptr, self.ws_bytes)
-        if self.pad == (D, I):
+        if self.bf16_act:
+            code = forward_w4a16_ptr(hidden.data_ptr(), w13.data_ptr(), w13_scale.data_ptr(),
+                                     w2.data_ptr(), w2_scale.data_ptr(), topk_ids.data_ptr(),
+                                     topk_weights.data_ptr(), out.data_ptr(), T, D, I, E, K, stream)
+            _check(code, "moe_mxfp4_forward_w4a16")
+        elif self.pad == (D, I):
             code = forward_ptr(hidden.data_ptr(), w13.data_ptr(), w13_scale.data_ptr(),
                                w2.data_ptr(), w2_scale.data_ptr(), topk_ids.data_ptr(),
                                topk_weights.data_ptr(), out.data_ptr(), T, D, I, E, K, stream)

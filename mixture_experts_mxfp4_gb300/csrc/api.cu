@@ -63,7 +63,9 @@ int choose_tile_rows(int T, int E, int K) {
     return 16;
 }
 
-void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
+// bf16_act: layout of the bf16-activation forward (bf16 a1/a2 rows instead of
+// the MXFP4 codes and scales).
+void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, bool bf16_act = false) {
     memset(pl, 0, sizeof(*pl));
     const long long R = (long long)T * K;
     const long long used = R < E ? R : E;
@@ -94,6 +96,14 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl) {
     b[MOE_WS_A2S] = (size_t)cap * pl->a2s_stride;
     b[MOE_WS_P] = (size_t)R * D * 4;
     b[MOE_WS_PARTIAL] = 0;  // (no K split)
+    b[MOE_WS_A1B] = 0;
+    b[MOE_WS_A2B] = 0;
+    if (bf16_act) {
+        pl->bf16_act = 1;
+        b[MOE_WS_A1Q] = b[MOE_WS_A1S] = b[MOE_WS_A2Q] = b[MOE_WS_A2S] = 0;
+        b[MOE_WS_A1B] = (size_t)cap * D * 2;
+        b[MOE_WS_A2B] = (size_t)cap * I * 2;
+    }
     size_t off = 0;
     for (int i = 0; i < MOE_WS_NUM_REGIONS; ++i) {
         pl->offset[i] = off;
@@ -122,6 +132,8 @@ WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl) {
     w.P = reinterpret_cast<float*>(b + pl.offset[MOE_WS_P]);
     w.tile_done = w.counters;
     w.quant_done = w.status + kFrontQuantWord;
+    w.a1b = reinterpret_cast<uint16_t*>(b + pl.offset[MOE_WS_A1B]);
+    w.a2b = reinterpret_cast<uint16_t*>(b + pl.offset[MOE_WS_A2B]);
     return w;
 }
 
@@ -574,6 +586,88 @@ size_t plan_workspace_bytes(int T, int D, int I, int E, int K) {
     return pl.workspace_bytes;
 }
 
+// Geometry of the bf16-activation GEMM kernel (gemm_w4a16.cu): ring slots of a
+// raw weight tile and a route tile, two dequantised bf16 weight tiles, one
+// epilogue group's exchange buffer, the route-tile cache.
+static bool w4_geometry(W4Params& g, int D, int I, int tile_rows) {
+    g.tile_rows = tile_rows;
+    g.n_ftiles1 = I / 64;
+    g.n_ftiles2 = D / 128;
+    g.kstages1 = D / kW4Kc;
+    g.kstages2 = I / kW4Kc;
+    g.slot_bytes = (uint32_t)round_up(kW4RawBytes + (size_t)tile_rows * 256, 1024);
+    const uint32_t fixed = 1024u + 2u * kW4DeqBytes + 512u + (uint32_t)kXchgBytes + (uint32_t)kTileCache * 16u;
+    int ns = (int)((uint32_t)kGemmSmemLimit - fixed) / (int)g.slot_bytes;
+    if (ns > kMaxStages) ns = kMaxStages;
+    if (ns < 2) return false;
+    g.num_stages = ns;
+    g.off_deq = (uint32_t)ns * g.slot_bytes;
+    g.off_bar = g.off_deq + 2u * kW4DeqBytes;
+    g.off_xchg = g.off_bar + 512u;
+    g.off_tiles = g.off_xchg + (uint32_t)kXchgBytes;
+    g.smem_bytes = g.off_tiles + (uint32_t)kTileCache * 16u + 1024u;
+    g.acc_bufs = 4;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(g.acc_bufs * tile_rows)) cols <<= 1;
+    g.tmem_cols = cols;
+    return cols <= 512u && g.smem_bytes <= (uint32_t)kGemmSmemLimit;
+}
+
+moe_status_t forward_w4a16_on_workspace(const void* hidden, const void* w13, const void* w13_scale,
+                                        const void* w2, const void* w2_scale,
+                                        const int32_t* topk_ids, const float* topk_weights,
+                                        void* out, int T, int D, int I, int E, int K, void* base,
+                                        int dev, cudaStream_t stream) {
+    moe_mxfp4_plan_t pl;
+    fill_plan(T, D, I, E, K, &pl, true);
+    W4Params g;
+    memset(&g, 0, sizeof(g));
+    g.ws = ws_ptrs(base, pl);
+    g.w13_scale = static_cast<const uint8_t*>(w13_scale);
+    g.w2_scale = static_cast<const uint8_t*>(w2_scale);
+    g.D = D; g.I = I; g.E = E; g.K = K; g.R = T * K;
+    if (!w4_geometry(g, D, I, pl.tile_rows)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int tr = pl.tile_rows;
+    CUtensorMap maps[4];
+    bool ok = true;
+    // raw e2m1 weights, 64 bytes (128 K elements) x 64 rows (stage 1) / 128 rows (stage 2)
+    ok = ok && make_map(&maps[0], w13, (uint64_t)D / 2, (uint64_t)E * 2 * I, (uint64_t)D / 2, 64, 64,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && make_map(&maps[2], w2, (uint64_t)I / 2, (uint64_t)E * D, (uint64_t)I / 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    // bf16 route tiles seen as {128 bytes, rows, K-boxes}: 2 K-boxes of 64 bf16 per stage
+    {
+        const uint64_t dims1[3] = {128, (uint64_t)pl.cap, (uint64_t)D * 2 / 128};
+        const uint64_t str1[2] = {(uint64_t)D * 2, 128};
+        const uint64_t dims2[3] = {128, (uint64_t)pl.cap, (uint64_t)I * 2 / 128};
+        const uint64_t str2[2] = {(uint64_t)I * 2, 128};
+        const uint32_t box[3] = {128, (uint32_t)tr, 2};
+        ok = ok && make_map_nd(&maps[1], g.ws.a1b, 3, dims1, str1, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && make_map_nd(&maps[3], g.ws.a2b, 3, dims2, str2, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (!ok) return MOE_ERR_CUDA;
+
+    const int sms = num_sms(dev);
+    Timing& tm = g_timing[dev];
+    const bool timed = tm.enabled && tm.created;
+    auto mark = [&](int i) {
+        if (timed && (tm.mode == 1 || i == 0 || i == kNumKernels)) cudaEventRecord(tm.ev[i], stream);
+    };
+    mark(0);
+    if (launch_route(topk_ids, topk_weights, T, K, E, tr, pl.cap, pl.max_tiles, g.ws, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark(1);
+    if (launch_gather_bf16(hidden, T, K, D, g.ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(2);
+    if (launch_w4a16_gemm(maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    mark(3);
+    if (launch_reduce(topk_ids, T, K, E, D, D, out, g.ws, false, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    mark(4);
+    if (timed) tm.recorded = true;
+    return MOE_OK;
+}
+
 }  // namespace moe
 
 extern "C" {
@@ -639,6 +733,45 @@ int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk) {
     moe::GemmParams gp;
     shape_geometry(T, d_model, d_inter, E, topk, &pl, &gp);
     return single_launch_for(dev, T, E, topk, gp) ? 2 : 4;
+}
+
+moe_status_t moe_mxfp4_get_plan_w4a16(int T, int d_model, int d_inter, int E, int topk,
+                                      moe_mxfp4_plan_t* plan) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = validate_shape(T, d_model, d_inter, E, topk);
+    if (st != MOE_OK) return st;
+    fill_plan(T, d_model, d_inter, E, topk, plan, true);
+    return MOE_OK;
+}
+
+size_t moe_mxfp4_workspace_size_w4a16(int T, int d_model, int d_inter, int E, int topk) {
+    moe_mxfp4_plan_t pl;
+    if (moe_mxfp4_get_plan_w4a16(T, d_model, d_inter, E, topk, &pl) != MOE_OK) return 0;
+    return pl.workspace_bytes;
+}
+
+moe_status_t moe_mxfp4_forward_w4a16(const void* hidden, const void* w13, const void* w13_scale,
+                                     const void* w2, const void* w2_scale,
+                                     const int32_t* topk_ids, const float* topk_weights,
+                                     void* out, int T, int d_model, int d_inter, int E, int topk,
+                                     cudaStream_t stream) {
+    const int D = d_model, I = d_inter, K = topk;
+    moe_status_t st = validate_forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
+                                       topk_weights, out, T, D, I, E, K);
+    if (st != MOE_OK || T == 0) return st;
+    const size_t need = moe_mxfp4_workspace_size_w4a16(T, D, I, E, K);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    void* base;
+    size_t ws_bytes;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        base = g_ws[dev].ptr;
+        ws_bytes = g_ws[dev].bytes;
+    }
+    if (!base || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    return moe::forward_w4a16_on_workspace(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
+                                           topk_weights, out, T, D, I, E, K, base, dev, stream);
 }
 
 moe_status_t moe_mxfp4_set_single_launch(int mode) {

@@ -30,6 +30,8 @@ struct WsPtrs {
     uint32_t* tile_done;   // stage-1 feature tiles completed per route tile (counters, or the
                            // status region's block on the single-launch path)
     uint32_t* quant_done;  // CTAs whose share of the hidden states is quantised (single launch)
+    uint16_t* a1b;         // bf16-activation path: [cap][D] hidden rows in sorted order
+    uint16_t* a2b;         // bf16-activation path: [cap][I] bf16 SwiGLU output in sorted order
 };
 
 // Geometry of one grouped block-scaled GEMM stage (stage 1: gate_up, K = D;
@@ -78,6 +80,28 @@ struct GemmParams {
     int T, cap;
 };
 
+// Parameters of the bf16-activation (W4A16) GEMM launch: packed e2m1 weights
+// with e8m0 scales, bf16 activations, both stages in one persistent launch.
+// Stage K chunks of 128 elements; weights dequantised to bf16 in shared memory.
+struct W4Params {
+    WsPtrs ws;
+    const uint8_t* w13_scale;  // [E][2I][D/32]
+    const uint8_t* w2_scale;   // [E][D][I/32]
+    int D, I, E, K, R;
+    int tile_rows;             // routes per tile (MMA N), multiple of 16, <= 128
+    int n_ftiles1, n_ftiles2;  // stage 1: I / 64; stage 2: D / 128
+    int kstages1, kstages2;    // D / 128, I / 128
+    int num_stages;            // TMA ring depth (raw weight tile + route tile per slot)
+    int acc_bufs;              // TMEM accumulators
+    uint32_t slot_bytes;       // raw weights (8 KB) + route tile (tile_rows x 256 B)
+    uint32_t off_deq;          // two dequantised bf16 weight tiles (32 KB each, 1024-aligned)
+    uint32_t off_bar, off_xchg, off_tiles, smem_bytes;
+    uint32_t tmem_cols;
+};
+constexpr int kW4Kc = 128;                 // K elements per stage
+constexpr uint32_t kW4RawBytes = 128 * 64;  // 128 weight rows x 64 bytes of e2m1
+constexpr uint32_t kW4DeqBytes = 128 * 256; // 128 rows x 128 bf16
+
 // Status region (u32 words): [0] error bits, [1..14] spare, [15] ready word of
 // the single-launch path, [16] its quantisation count, [512, 1024) its route-tile
 // counters.  Words 15.. are zero between calls: the workspace registration
@@ -124,6 +148,13 @@ cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1
 // P rows hold D columns; out rows Dl
 cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, int Dl, void* out,
                           const WsPtrs& ws, bool clear_ready, cudaStream_t stream);
+// bf16-activation path: copy each token's hidden row to the sorted slot of
+// every valid route (after the routing kernel)
+cudaError_t launch_gather_bf16(const void* hidden, int T, int K, int D, const WsPtrs& ws,
+                               cudaStream_t stream);
+// maps: raw w13 (64 B x 64 rows), a1b route tiles, raw w2 (64 B x 128 rows), a2b route tiles
+cudaError_t launch_w4a16_gemm(const CUtensorMap* maps, const W4Params& p, int grid,
+                              cudaStream_t stream);
 // maps: stage-1 A, SA, B, SB, then stage-2 A, SA, B, SB
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream);

@@ -364,6 +364,31 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// Instruction descriptor of tcgen05.mma .kind::f16 with bf16 operands and fp32
+// accumulation, both operands K-major:
+//   bits 4-5 D format (F32 = 1), 7-9 A format (BF16 = 1), 10-12 B format,
+//   17-22 N>>3, 24-28 M>>4.
+__device__ __forceinline__ uint32_t bf16_idesc(uint32_t M, uint32_t N) {
+    uint32_t d = 0;
+    d |= 1u << 4;
+    d |= 1u << 7;
+    d |= 1u << 10;
+    d |= ((N >> 3) & 0x3Fu) << 17;
+    d |= ((M >> 4) & 0x1Fu) << 24;
+    return d;
+}
+
+// D[tmem] (+)= A . B^T, bf16 x bf16 -> fp32, K = 16 per instruction; one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Copy a 32-row x 16-byte scale-factor block from shared memory into TMEM,
 // replicated into all four 32-lane quadrants (4 columns).
 __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {

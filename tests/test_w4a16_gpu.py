@@ -1,0 +1,174 @@
+"""GPU parity of the bf16-activation (W4A16) forward against the oracle's
+bf16-activation mode (no activation quantiser; bf16 SwiGLU output into stage 2).
+
+Bars: routing arrays bit-exact (same routing kernel); the bf16 intermediate of
+every valid route equal to the oracle's for at least 99% of elements, and every
+element that differs by more than one bf16 step within the bound the oracle's
+own pin uses against the fp64 truth (one bf16 rounding plus 4 D 2^-24 times the
+sums of absolute products: fp32 sums in another order can cancel differently);
+every output element within one bf16 step of the oracle's plus 2e-2 of the
+oracle row RMS (the bf16 intermediate can differ in a last place, so the final
+rounding of a large element can land one step away), exactly zero where the
+oracle row is zero."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+ROW_TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_mxfp4_gb300 import build
+
+    build.build()
+    import mixture_experts_mxfp4_gb300 as m
+
+    m.load_library()
+    return m
+
+
+def _threads():
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+_E2M1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6])
+
+
+def _deq_row(codes, scales):
+    """fp64 values of one packed e2m1 row with its e8m0 scales."""
+    c = np.asarray(codes, np.uint8)
+    v = _E2M1[np.stack([c & 15, c >> 4], axis=-1).reshape(-1)]
+    return v * np.repeat(np.ldexp(1.0, np.asarray(scales, np.int64) - 127), 32)
+
+
+def _h_truth(inp, w, t, e, n):
+    """fp64 G, U, H and the pin's bound for feature n of token t through expert e."""
+    x = oracle.bf16_bits_to_f32(workloads.to_numpy(inp)["hidden_bits"][t]).astype(np.float64)
+    w13, s13 = inp["w13"].numpy(), inp["w13_scale"].numpy()
+    wg = _deq_row(w13[e, n], s13[e, n])
+    wu = _deq_row(w13[e, w.I + n], s13[e, w.I + n])
+    G, U = float(wg @ x), float(wu @ x)
+    aG, aU = float(np.abs(wg) @ np.abs(x)), float(np.abs(wu) @ np.abs(x))
+    H = G / (1.0 + np.exp(-G)) * U
+    bound = 2.0 ** -8 * abs(H) + 4 * w.D * 2.0 ** -24 * (aG * abs(U) + aU * abs(G)) + 1e-30
+    return H, bound
+
+
+def run_w4a16(moe, w, inp, tokens=None):
+    dev = torch.device("cuda")
+    m = moe.MoeMXFP4(w.T, w.D, w.I, w.E, w.K, activations="bf16")
+    assert m.plan.bf16_act == 1
+    t = {k: v.to(dev) for k, v in inp.items()}
+    out = m.forward(t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"],
+                    t["topk_ids"], t["topk_weights"])
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    npi = workloads.to_numpy(inp)
+    ref = oracle.forward(**npi, tokens=tokens, quant_act=False, threads=_threads(), want_h=True)
+    routing = oracle.route(npi["topk_ids"], npi["topk_weights"], w.E, 16, cap=m.plan.cap)
+    cap = m.plan.cap
+    sid = m.region("sorted_ids", torch.int32, (cap,)).cpu().numpy()
+    np.testing.assert_array_equal(sid, routing["sorted_ids"])
+    # bf16 intermediate of each valid route (a2b rows are in sorted-slot order)
+    a2b = m.region("a2b", torch.int16, (cap, w.I)).cpu()
+    h_gpu = a2b.view(torch.bfloat16).float().numpy()
+    sel = set(range(w.T)) if tokens is None else set(int(x) for x in tokens)
+    n = int(routing["num_valid"][0])
+    total = same = 0
+    for p in range(n):
+        r = int(routing["sorted_ids"][p])
+        if r >= w.R or (r // w.K) not in sel:
+            continue
+        g, o = h_gpu[p], ref["h"][r]
+        total += w.I
+        same += int((g == o).sum())
+        tol = 2.0 ** -7 * np.maximum(np.abs(g), np.abs(o)) + 1e-30
+        for n in np.nonzero(np.abs(g - o) > tol)[0]:
+            H, bound = _h_truth(inp, w, r // w.K, int(inp["topk_ids"].reshape(-1)[r]), int(n))
+            assert abs(float(g[n]) - H) <= bound, f"h slot {p} route {r} feature {n}: {g[n]} vs {H}"
+    assert total > 0 and same >= 0.99 * total, f"{total - same} of {total} h elements differ"
+    g = out.float().cpu().numpy()
+    o = oracle.bf16_bits_to_f32(ref["out_bf16"])
+    rows = range(w.T) if tokens is None else tokens
+    for t_ in rows:
+        rms = float(np.sqrt(np.mean(o[t_].astype(np.float64) ** 2)))
+        diff = np.abs(g[t_].astype(np.float64) - o[t_])
+        if rms == 0.0:
+            assert float(diff.max()) == 0.0
+            continue
+        allow = 2.0 ** -7 * np.abs(o[t_].astype(np.float64)) + ROW_TOL * rms
+        bad = np.nonzero(diff > allow)[0]
+        assert bad.size == 0, f"row {t_} col {bad[0]}: {g[t_][bad[0]]} vs {o[t_][bad[0]]} (rms {rms})"
+    return out
+
+
+def _small(T=16, D=256, I=128, E=9, K=3, seed=0):
+    w = workloads.custom(T, D, I, E, K)
+    return w, workloads.make_inputs(w, seed=seed)
+
+
+def test_w4a16_tiny(moe):
+    w = workloads.WORKLOADS[workloads.TINY]
+    run_w4a16(moe, w, workloads.make_inputs(w))
+
+
+def test_w4a16_decode_t16(moe):
+    w = workloads.WORKLOADS[workloads.DECODE_T16]
+    run_w4a16(moe, w, workloads.make_inputs(w))
+
+
+def test_w4a16_decode_t128_sampled(moe):
+    w = workloads.WORKLOADS["decode_T128_D7168_I256_E257_K9"]
+    run_w4a16(moe, w, workloads.make_inputs(w), tokens=[0, 1, 63, 64, 100, 127])
+
+
+def test_w4a16_dense_shard_sampled(moe):
+    w = workloads.WORKLOADS["dense_T512_D7168_I2048_E33_K9"]
+    run_w4a16(moe, w, workloads.make_inputs(w), tokens=[0, 1, 255, 256, 511])
+
+
+def test_w4a16_single_token(moe):
+    w, inp = _small(T=1)
+    run_w4a16(moe, w, inp)
+
+
+def test_w4a16_invalid_ids_and_empty_rows(moe):
+    w, inp = _small(T=20, E=9, K=3)
+    ids = inp["topk_ids"]
+    ids[0, :] = -1
+    ids[3, 1] = 9
+    ids[5, 0] = 1000
+    run_w4a16(moe, w, inp)
+
+
+def test_w4a16_multi_stage_shape(moe):
+    w, inp = _small(T=64, D=1024, I=512, E=3, K=2)
+    run_w4a16(moe, w, inp)
+
+
+def test_w4a16_large_tiles(moe):
+    w, inp = _small(T=256, D=512, I=256, E=5, K=3)
+    run_w4a16(moe, w, inp)
+
+
+def test_w4a16_differs_from_mxfp4_path(moe):
+    """The two numerics paths are different computations (the activation
+    quantiser is really skipped)."""
+    w = workloads.WORKLOADS[workloads.TINY]
+    inp = workloads.make_inputs(w)
+    dev = torch.device("cuda")
+    t = {k: v.to(dev) for k, v in inp.items()}
+    args = (t["hidden"], t["w13"], t["w13_scale"], t["w2"], t["w2_scale"], t["topk_ids"],
+            t["topk_weights"])
+    a = moe.MoeMXFP4(w.T, w.D, w.I, w.E, w.K).forward(*args)
+    b = moe.MoeMXFP4(w.T, w.D, w.I, w.E, w.K, activations="bf16").forward(*args)
+    torch.cuda.synchronize()
+    assert not torch.equal(a, b)
