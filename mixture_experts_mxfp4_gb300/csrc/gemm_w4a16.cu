@@ -15,15 +15,16 @@
 //   stage 2: acc[m, j] = sum_k W2[row m, k] * h[slot j, k];  P[route] = w * acc
 // with W = e2m1 * 2^(s - 127), exact in bf16, and fp32 accumulation.
 //
-// Pipeline (one CTA per SM, 384 threads):
+// Pipeline (one CTA per SM, 512 threads):
 //   warp 0     TMA producer: per stage (128 K elements) the raw weight tile
 //              (128 rows x 64 bytes of e2m1) and the bf16 route tile
 //              (tile_rows x 256 bytes, 128-byte swizzle) -> ring slot
 //   warp 1     MMA: 8 x tcgen05.mma.kind::f16 (K = 16) per stage
 //   warp 2     allocates / frees TMEM
 //   warps 4-7  epilogue (TMEM lane quadrant = warp % 4)
-//   warps 8-11 dequantisation: thread m expands weight row m of a stage into
-//              one of two bf16 tiles (K-major, 128-byte swizzle)
+//   warps 8-15 dequantisation: two threads per weight row expand its 64-element
+//              halves of a stage into one of two bf16 tiles (K-major, 128-byte
+//              swizzle)
 // A ring slot is released when both its consumers are done (the dequantisers
 // with the raw weights, the MMAs with the route tile): its `empty` barrier
 // counts two arrivals.
@@ -40,39 +41,53 @@ struct W4Item {
     int e, row0, nrows, f, tile;
 };
 
-// fp32 value of an e8m0 scale byte: 2^(s - 127); 255 is NaN.
-__device__ __forceinline__ float w4_scale(uint32_t s) {
-    if (s == 255u) return __uint_as_float(0x7fc00000u);
-    if (s == 0u) return __uint_as_float(0x00400000u);  // 2^-127 (subnormal)
-    return __uint_as_float(s << 23);
+// bf16 bits of an e8m0 scale byte's 2^(s - 127), twice: exact for every byte
+// (s = 0: the subnormal 2^-127), 255 gives NaN.
+__device__ __forceinline__ uint32_t w4_scale2(uint32_t s) {
+    const uint32_t b = s == 255u ? 0x7fc0u : (s == 0u ? 0x0040u : (s << 7));
+    return b | (b << 16);
 }
 
-// Dequantise weight row m of one stage: 64 bytes of e2m1 (byte j: element 2j in
-// the low nibble) with 4 scale bytes (one per 32 elements) -> 128 bf16 in the
-// K-major 128-byte-swizzled tile [2 K-boxes][128 rows][128 bytes], 16-byte chunk
-// c of a row at chunk c ^ (row % 8).  lut: the 16 e2m1 values in fp32.
-__device__ __forceinline__ void w4_dequant_row(const uint8_t* raw_row, uint32_t sc4,
-                                               uint8_t* deq, int m, const float* lut) {
-    const uint4* src = reinterpret_cast<const uint4*>(raw_row);
+// Four e2m1 codes (16 bits, element i in bits 4i..4i+3) -> four bf16 (two
+// bf16x2 words), times the block scale.  The magnitude (3 bits) picks the low
+// and the high byte of the bf16 pattern from two 8-byte tables with a byte
+// permute (0, 0.5, 1, 1.5, 2, 3, 4, 6 = 0x0000 0x3F00 0x3F80 0x3FC0 0x4000
+// 0x4040 0x4080 0x40C0), the sign bit moves to bit 15, and the product with a
+// power of two is exact in bf16.
+__device__ __forceinline__ void w4_expand4(uint32_t w16, uint32_t sc2, uint32_t& o01, uint32_t& o23) {
+    const uint32_t mag = w16 & 0x7777u;
+    const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, mag);
+    const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, mag);
+    uint32_t a = __byte_perm(lo, hi, 0x5140u);
+    uint32_t b = __byte_perm(lo, hi, 0x7362u);
+    a |= ((w16 << 12) & 0x8000u) | ((w16 << 24) & 0x80000000u);
+    b |= ((w16 << 4) & 0x8000u) | ((w16 << 16) & 0x80000000u);
+    const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&sc2);
+    const __nv_bfloat162 ra = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), s2);
+    const __nv_bfloat162 rb = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b), s2);
+    o01 = *reinterpret_cast<const uint32_t*>(&ra);
+    o23 = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
+// Dequantise half hf (64 elements, K-box hf) of weight row m of one stage: 32
+// bytes of e2m1 (byte j: element 2j in the low nibble) with 2 scale bytes ->
+// 64 bf16 in the K-major 128-byte-swizzled tile [2 K-boxes][128 rows][128 bytes],
+// 16-byte chunk c of a row at chunk c ^ (row % 8).
+__device__ __forceinline__ void w4_dequant_half(const uint8_t* raw, uint32_t sc_pair, uint8_t* deq_box,
+                                                int m) {
+    const uint4* src = reinterpret_cast<const uint4*>(raw);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {  // 16 bytes = 32 elements = one scale block
+    for (int q = 0; q < 2; ++q) {  // 16 bytes = 32 elements = one scale block
         const uint4 r = src[q];
-        const float sc = w4_scale((sc4 >> (8 * q)) & 0xffu);
+        const uint32_t sc2 = w4_scale2((sc_pair >> (8 * q)) & 0xffu);
         const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {  // 4 bytes = 8 elements = one 16-byte output chunk
             uint32_t o[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const uint32_t byte = (w[h] >> (8 * b)) & 0xffu;
-                const float lo = lut[byte & 15u] * sc;
-                const float hi = lut[byte >> 4] * sc;
-                const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-                o[b] = *reinterpret_cast<const uint32_t*>(&v);
-            }
-            const int chunk = q * 4 + h;  // 0..15 along K
-            const int kbox = chunk >> 3, c8 = chunk & 7;
-            *reinterpret_cast<uint4*>(deq + kbox * (128 * 128) + m * 128 + ((c8 ^ (m & 7)) * 16)) =
+            w4_expand4(w[h] & 0xffffu, sc2, o[0], o[1]);
+            w4_expand4(w[h] >> 16, sc2, o[2], o[3]);
+            const int c8 = q * 4 + h;
+            *reinterpret_cast<uint4*>(deq_box + m * 128 + ((c8 ^ (m & 7)) * 16)) =
                 make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
@@ -123,7 +138,7 @@ cudaError_t launch_gather_bf16(const void* hidden, int T, int K, int D, const Ws
 
 // ============================================================== GEMM kernel
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kW4Threads, 1)
     moe_w4a16_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                           const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                           const W4Params p) {
@@ -147,7 +162,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* drain = tempty + kMaxAccBufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* lut = reinterpret_cast<float*>(smem + p.off_bar + 384);  // 16 e2m1 values
     float* xg = reinterpret_cast<float*>(smem + p.off_xchg);
     uint8_t* deq = smem + p.off_deq;
     uint32_t* status = p.ws.status;
@@ -170,12 +184,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (threadIdx.x < 16) {
-        // e2m1: sign, 2 exponent bits (bias 1), 1 mantissa bit
-        const uint32_t c = threadIdx.x, e = (c >> 1) & 3u, mt = c & 1u;
-        const float mag = e == 0 ? 0.5f * (float)mt : (1.0f + 0.5f * (float)mt) * (float)(1u << (e - 1));
-        lut[c] = (c & 8u) ? -mag : mag;
-    }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA1);
         tma_prefetch_desc(&tmB1);
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int b0 = (int)blockIdx.x;
     if (b0 >= nitems[0] && b0 >= nitems[1]) return;
     int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
-    for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kGemmThreads)
+    for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kW4Threads)
         tcache[i] = __ldcg(p.ws.tiles + i);
     if (warp == 2) {
         tmem_alloc(tmem_slot, p.tmem_cols);
@@ -366,7 +374,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dequantisation
-        const int m = (int)threadIdx.x - 256;  // weight row of the tile
+        const int dt = (int)threadIdx.x - 256;
+        const int m = dt & 127;   // weight row of the tile
+        const int hf = dt >> 7;   // which 64 elements (K-box) of the stage
         int s = 0, b = 0;
         uint32_t ph = 0, bph = 0;
         bool ok = true;
@@ -381,17 +391,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t* srow_p =
                     reinterpret_cast<const uint32_t*>((phs ? p.w2_scale : p.w13_scale) + rowg * srow);
                 for (int ks = 0; ks < kst; ++ks) {
-                    const uint32_t sc4 = __ldg(srow_p + ks);  // the stage's 4 scale bytes
+                    const uint32_t sc_pair = __ldg(srow_p + ks) >> (16 * hf);  // this half's 2 scales
                     if (!mbar_wait_warp(&full[s], ph, status, kErrTimeoutFull, abort_flag) ||
                         !mbar_wait_warp(&dempty[b], bph ^ 1u, status, kErrTimeoutFull, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    w4_dequant_row(smem + (size_t)s * p.slot_bytes + m * 64, sc4, deq + (size_t)b * kW4DeqBytes,
-                                   m, lut);
+                    w4_dequant_half(smem + (size_t)s * p.slot_bytes + m * 64 + hf * 32, sc_pair,
+                                    deq + (size_t)b * kW4DeqBytes + hf * (128 * 128), m);
                     fence_proxy_async_smem();  // the MMAs read the tile through the async proxy
-                    named_bar_sync(5, 128);
-                    if (m == 0) {
+                    named_bar_sync(5, 256);
+                    if (dt == 0) {
                         mbar_arrive(&dfull[b]);
                         mbar_arrive(&empty[s]);
                     }
@@ -535,7 +545,7 @@ cudaError_t launch_w4a16_gemm(const CUtensorMap* maps, const W4Params& p, int gr
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(kW4Threads);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -99,6 +99,7 @@ struct W4Params {
     uint32_t tmem_cols;
 };
 constexpr int kW4Kc = 128;                 // K elements per stage
+constexpr int kW4Threads = 512;            // 16 warps: producer, MMA, TMEM, -, 4 epilogue, 8 dequantisation
 constexpr uint32_t kW4RawBytes = 128 * 64;  // 128 weight rows x 64 bytes of e2m1
 constexpr uint32_t kW4DeqBytes = 128 * 256; // 128 rows x 128 bf16
 
