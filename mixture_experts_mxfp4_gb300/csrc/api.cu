@@ -596,13 +596,19 @@ static bool w4_geometry(W4Params& g, int D, int I, int tile_rows) {
     g.kstages1 = D / kW4Kc;
     g.kstages2 = I / kW4Kc;
     g.slot_bytes = (uint32_t)round_up(kW4RawBytes + (size_t)tile_rows * 256, 1024);
-    const uint32_t fixed = 1024u + 2u * kW4DeqBytes + 512u + (uint32_t)kXchgBytes + (uint32_t)kTileCache * 16u;
-    int ns = (int)((uint32_t)kGemmSmemLimit - fixed) / (int)g.slot_bytes;
-    if (ns > kMaxStages) ns = kMaxStages;
+    auto slots_for = [&](int nb) {
+        const uint32_t fixed = 1024u + (uint32_t)nb * kW4DeqBytes + 512u + (uint32_t)kXchgBytes +
+                               (uint32_t)kTileCache * 16u;
+        int n = (int)((uint32_t)kGemmSmemLimit - fixed) / (int)g.slot_bytes;
+        return n > kMaxStages ? kMaxStages : n;
+    };
+    // a third dequantised tile where it leaves the ring at least four slots
+    g.deq_bufs = slots_for(kW4MaxDeq) >= 4 ? kW4MaxDeq : 2;
+    const int ns = slots_for(g.deq_bufs);
     if (ns < 2) return false;
     g.num_stages = ns;
     g.off_deq = (uint32_t)ns * g.slot_bytes;
-    g.off_bar = g.off_deq + 2u * kW4DeqBytes;
+    g.off_bar = g.off_deq + (uint32_t)g.deq_bufs * kW4DeqBytes;
     g.off_xchg = g.off_bar + 512u;
     g.off_tiles = g.off_xchg + (uint32_t)kXchgBytes;
     g.smem_bytes = g.off_tiles + (uint32_t)kTileCache * 16u + 1024u;

@@ -27,7 +27,9 @@
 //              swizzle)
 // A ring slot is released when both its consumers are done (the dequantisers
 // with the raw weights, the MMAs with the route tile): its `empty` barrier
-// counts two arrivals.
+// counts two arrivals.  Two or three dequantised tiles (three where shared
+// memory leaves the ring at least four slots) let the expansion run ahead of
+// the MMAs.
 #include <cuda_bf16.h>
 
 #include "moe_internal.h"
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
     const int NS = p.num_stages;
-    constexpr int NB = 2;  // dequantised weight tiles
+    const int NB = p.deq_bufs;  // dequantised weight tiles (2 or 3)
 
     // full: raw weights + route tile landed; empty: dequantisers and MMAs done with a
     // slot (2 arrivals); dfull / dempty: a dequantised tile written / consumed;
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint64_t* empty = full + kMaxStages;
     uint64_t* dfull = empty + kMaxStages;
-    uint64_t* dempty = dfull + NB;
-    uint64_t* tfull = dempty + NB;
+    uint64_t* dempty = dfull + kW4MaxDeq;
+    uint64_t* tfull = dempty + kW4MaxDeq;
     uint64_t* tempty = tfull + kMaxAccBufs;
     uint64_t* drain = tempty + kMaxAccBufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);

@@ -93,8 +93,9 @@ struct W4Params {
     int kstages1, kstages2;    // D / 128, I / 128
     int num_stages;            // TMA ring depth (raw weight tile + route tile per slot)
     int acc_bufs;              // TMEM accumulators
+    int deq_bufs;              // dequantised bf16 weight tiles (2 or 3)
     uint32_t slot_bytes;       // raw weights (8 KB) + route tile (tile_rows x 256 B)
-    uint32_t off_deq;          // two dequantised bf16 weight tiles (32 KB each, 1024-aligned)
+    uint32_t off_deq;          // the dequantised tiles (32 KB each, 1024-aligned)
     uint32_t off_bar, off_xchg, off_tiles, smem_bytes;
     uint32_t tmem_cols;
 };
@@ -102,6 +103,7 @@ constexpr int kW4Kc = 128;                 // K elements per stage
 constexpr int kW4Threads = 512;            // 16 warps: producer, MMA, TMEM, -, 4 epilogue, 8 dequantisation
 constexpr uint32_t kW4RawBytes = 128 * 64;  // 128 weight rows x 64 bytes of e2m1
 constexpr uint32_t kW4DeqBytes = 128 * 256; // 128 rows x 128 bf16
+constexpr int kW4MaxDeq = 3;
 
 // Status region (u32 words): [0] error bits, [1..14] spare, [15] ready word of
 // the single-launch path, [16] its quantisation count, [512, 1024) its route-tile
