@@ -253,7 +253,9 @@ def run_gpu(args, w, world, rank, local):
 
     # launch mode: the library's automatic choice unless forced
     moe.set_single_launch({"auto": 2, "single": 1, "separate": 0}[args.launch])
-    launches = 4 if bf16_act else moe.call_launches(w.T, w.D, w.I, w.E, w.K)
+    # (the bf16-activation forward: separate kernels; routing in three launches from 4096 routes)
+    launches = ((6 if w.T * w.K >= 4096 else 4) if bf16_act
+                else moe.call_launches(w.T, w.D, w.I, w.E, w.K))
     single = launches == 2
     moe.set_kernel_timing(2)
     for _ in range(args.warmup):

@@ -132,8 +132,8 @@ moe_status_t moe_mxfp4_forward_padded(const void* hidden, const void* w13, const
  * weights are expanded to bf16 in shared memory for bf16 tensor-core MMAs.  Same
  * arguments, shapes and errors as moe_mxfp4_forward; the registered workspace
  * must hold moe_mxfp4_workspace_size_w4a16 bytes (its layout:
- * moe_mxfp4_get_plan_w4a16).  Always four launches (route, row gather, GEMM
- * kernel, top-k sum).
+ * moe_mxfp4_get_plan_w4a16).  Launches: routing (one kernel, or three from 4096
+ * routes), row gather, GEMM kernel, top-k sum.
  */
 moe_status_t moe_mxfp4_forward_w4a16(const void* hidden, const void* w13, const void* w13_scale,
                                      const void* w2, const void* w2_scale,
@@ -271,9 +271,10 @@ int moe_mxfp4_num_kernels(void);
 moe_status_t moe_mxfp4_set_single_launch(int mode);
 
 /* Kernels a forward call of this shape launches on the current device under its
- * launch mode: 4 (route, quant, GEMM, top-k sum), 2 (GEMM with routing and
- * quantisation inside, top-k sum), 0 for T = 0, -1 for an invalid shape or no
- * device. */
+ * launch mode: 4 (route, quant, GEMM, top-k sum), 6 when T*topk >= 4096 (routing
+ * then runs on many CTAs in three launches: chunk counts, offsets, scatter),
+ * 2 (GEMM with routing and quantisation inside, top-k sum), 0 for T = 0, -1 for
+ * an invalid shape or no device. */
 int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk);
 
 /*

@@ -738,7 +738,8 @@ int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk) {
     moe_mxfp4_plan_t pl;
     moe::GemmParams gp;
     shape_geometry(T, d_model, d_inter, E, topk, &pl, &gp);
-    return single_launch_for(dev, T, E, topk, gp) ? 2 : 4;
+    if (single_launch_for(dev, T, E, topk, gp)) return 2;
+    return (long long)T * topk >= kRouteMultiMin ? 6 : 4;  // routing in three launches
 }
 
 moe_status_t moe_mxfp4_get_plan_w4a16(int T, int d_model, int d_inter, int E, int topk,

@@ -125,6 +125,7 @@ constexpr int kMaxAccBufs = 4;
 constexpr int kFrontMaxRoutes = 2048;  // single-launch path: routes (position table in the exchange buffer)
 constexpr int kFrontMaxExperts = 384;  // single-launch path: one expert per GEMM thread
 constexpr int kFrontAutoRoutes = 256;  // automatic mode: single launch up to this many routes
+constexpr int kRouteMultiMin = 4096;  // routes from which routing runs in three launches on many CTAs
 constexpr int kTileCache = 512;      // route tiles kept in shared memory (the rest read from L2)
 
 // Host-side pieces of the forward call shared by its entry points (api.cu).

@@ -168,9 +168,217 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
 }
 
+// ============================================================== routing over many CTAs
+//
+// For large batches the same layout in three launches: per-CTA expert counts
+// of contiguous route chunks, one CTA that turns them into segment and per-chunk
+// offsets (and writes everything the one-CTA kernel writes except the routes'
+// own slots), then every CTA scatters its chunk.  The order is the one-CTA
+// kernel's: a chunk's routes precede the next chunk's, and inside a chunk the
+// per-warp ranks are as there.  The per-chunk counts live in the P region,
+// which the stage-2 GEMM overwrites later.
+
+constexpr int kRouteMaxChunks = 144;
+constexpr int kChunkThreads = 256;
+constexpr int kChunkWarps = kChunkThreads / 32;
+constexpr int kScanBatch = 12;  // per-chunk counts a scan thread loads at once
+
+// Per-warp expert histogram of routes [c0, c1) (contiguous sub-chunk per warp)
+// into hist[kChunkWarps][E] (zeroed by the caller); whole CTA.
+__device__ __forceinline__ void chunk_histogram(const int32_t* __restrict__ topk_ids, int c0, int c1,
+                                                int E, int* hist, int& r_begin, int& r_end) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wchunk = (c1 - c0 + kChunkWarps - 1) / kChunkWarps;
+    r_begin = min(c0 + warp * wchunk, c1);
+    r_end = min(r_begin + wchunk, c1);
+    for (int base = r_begin; base < r_end; base += 32) {
+        const int r = base + lane;
+        const int e = (r < r_end) ? topk_ids[r] : -1;
+        const bool valid = (r < r_end) && e >= 0 && e < E;
+        const uint32_t m = __match_any_sync(0xffffffffu, valid ? e : -1);
+        if (valid && lane == __ffs(m) - 1) hist[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+}
+
+__global__ void __launch_bounds__(kChunkThreads)
+    moe_route_count_kernel(const int32_t* __restrict__ topk_ids, int R, int E, int chunk,
+                           int* __restrict__ ccount) {
+    extern __shared__ int cs_smem[];
+    int* hist = cs_smem;  // [kChunkWarps][E]
+    grid_dep_launch();
+    for (int i = threadIdx.x; i < kChunkWarps * E; i += kChunkThreads) hist[i] = 0;
+    __syncthreads();
+    const int c0 = min((int)blockIdx.x * chunk, R), c1 = min(c0 + chunk, R);
+    int rb, re;
+    chunk_histogram(topk_ids, c0, c1, E, hist, rb, re);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kChunkThreads) {
+        int sum = 0;
+        for (int w = 0; w < kChunkWarps; ++w) sum += hist[w * E + e];
+        ccount[(size_t)blockIdx.x * E + e] = sum;
+    }
+}
+
+// One CTA of kRouteThreads: expert totals over the C chunks, the padded segment
+// layout (as moe_route_kernel), and ccount[c][e] replaced by the first slot of
+// chunk c's routes of expert e.
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    moe_route_scan_kernel(int C, int T, int K, int E, int tile_rows, int cap, int n_counters,
+                          int* __restrict__ ccount, WsPtrs ws) {
+    __shared__ int seg[1025];
+    __shared__ int wsum[64];
+    __shared__ int s_totals[2];
+    const int tid = threadIdx.x;
+    const int R = T * K;
+    const int bm = kBlockM;
+    grid_dep_launch();
+    grid_dep_wait();  // the chunk counts
+    for (int i = tid; i < n_counters; i += kRouteThreads) ws.counters[i] = 0;
+    if (tid < 16) ws.status[tid] = 0;
+
+    int cnt = 0, padded = 0, ntiles = 0;
+    if (tid < E) {
+        for (int c0 = 0; c0 < C; c0 += kScanBatch) {
+            int v[kScanBatch];
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) v[i] = (c0 + i < C) ? ccount[(size_t)(c0 + i) * E + tid] : 0;
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) cnt += v[i];
+        }
+        padded = (cnt + bm - 1) / bm * bm;
+        ntiles = (padded + tile_rows - 1) / tile_rows;
+    }
+    int seg_incl = padded, tile_incl = ntiles;
+    block_scan2(seg_incl, tile_incl, wsum, wsum + 32);
+    const int seg_e = seg_incl - padded, tile_e = tile_incl - ntiles;
+    if (tid < E) seg[tid] = seg_e;
+    if (tid == kRouteThreads - 1) {
+        seg[E] = seg_incl;
+        s_totals[0] = seg_incl;
+        s_totals[1] = tile_incl;
+    }
+    int valid_incl = cnt, dummy = 0;
+    __syncthreads();
+    block_scan2(valid_incl, dummy, wsum, wsum + 32);
+    const int total_padded = s_totals[0], total_tiles = s_totals[1];
+
+    if (tid <= E) ws.seg_start[tid] = seg[tid];
+    if (tid < E) {
+        // chunk c's routes of this expert start after the earlier chunks' ones
+        int run = seg_e;
+        for (int c0 = 0; c0 < C; c0 += kScanBatch) {
+            int v[kScanBatch];
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) v[i] = (c0 + i < C) ? ccount[(size_t)(c0 + i) * E + tid] : 0;
+#pragma unroll
+            for (int i = 0; i < kScanBatch; ++i) {
+                if (c0 + i < C) ccount[(size_t)(c0 + i) * E + tid] = run;
+                run += v[i];
+            }
+        }
+    }
+    if (tid < E && cnt > 0) {
+        for (int j = 0; j < ntiles; ++j) {
+            const int rows = min(tile_rows, padded - j * tile_rows);
+            ws.tiles[tile_e + j] = make_int4(tid, seg_e + j * tile_rows, rows, 0);
+        }
+        for (int b = seg_e / bm; b < (seg_e + padded) / bm; ++b) ws.block_expert[b] = tid;
+        for (int p = seg_e + cnt; p < seg_e + padded; ++p) {
+            ws.sorted_ids[p] = R;
+            ws.sorted_w[p] = 0.0f;
+        }
+    }
+    for (int p = total_padded + tid; p < cap; p += kRouteThreads) {
+        ws.sorted_ids[p] = R;
+        ws.sorted_w[p] = 0.0f;
+    }
+    for (int b = total_padded / bm + tid; b < cap / bm; b += kRouteThreads) ws.block_expert[b] = -1;
+    if (tid == kRouteThreads - 1) {
+        ws.num_valid[0] = total_padded;
+        ws.num_valid[1] = valid_incl;
+        ws.num_valid[2] = total_tiles;
+        ws.num_valid[3] = 0;
+    }
+}
+
+// Every CTA: its chunk's routes to their slots (ids, weights, route_pos).
+__global__ void __launch_bounds__(kChunkThreads)
+    moe_route_scatter_kernel(const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w,
+                             int R, int E, int chunk, const int* __restrict__ ccount, WsPtrs ws) {
+    extern __shared__ int cs_smem[];
+    int* hist = cs_smem;  // [kChunkWarps][E]: counts, then first slots per warp
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    grid_dep_launch();
+    for (int i = threadIdx.x; i < kChunkWarps * E; i += kChunkThreads) hist[i] = 0;
+    __syncthreads();
+    const int c0 = min((int)blockIdx.x * chunk, R), c1 = min(c0 + chunk, R);
+    int r_begin, r_end;
+    chunk_histogram(topk_ids, c0, c1, E, hist, r_begin, r_end);
+    grid_dep_wait();  // the per-chunk first slots from the scan kernel
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kChunkThreads) {
+        int run = ccount[(size_t)blockIdx.x * E + e];
+        for (int w = 0; w < kChunkWarps; ++w) {
+            const int c = hist[w * E + e];
+            hist[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int base = r_begin; base < r_end; base += 32) {
+        const int r = base + lane;
+        const int e = (r < r_end) ? topk_ids[r] : -1;
+        const bool valid = (r < r_end) && e >= 0 && e < E;
+        const uint32_t m = __match_any_sync(0xffffffffu, valid ? e : -1);
+        if (valid) {
+            const int pos = hist[warp * E + e] + __popc(m & lt_mask);
+            ws.sorted_ids[pos] = r;
+            ws.sorted_w[pos] = topk_w[r];
+            ws.route_pos[r] = pos;
+        } else if (r < r_end) {
+            ws.route_pos[r] = -1;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(m) - 1) hist[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+}
+
 cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, int K, int E,
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream) {
+    const int R = T * K;
+    if (R >= kRouteMultiMin) {
+        // count -> scan -> scatter; the per-chunk counts go to the P region
+        // (R * D floats >= C * E ints: R >= 4096, D >= 128, C <= 144, E <= 1024)
+        const int C = min(kRouteMaxChunks, (R + 1023) / 1024);
+        const int chunk = (R + C - 1) / C;
+        int* ccount = reinterpret_cast<int*>(ws.P);
+        const size_t csmem = sizeof(int) * (size_t)kChunkWarps * E;
+        moe_route_count_kernel<<<C, kChunkThreads, csmem, stream>>>(topk_ids, R, E, chunk, ccount);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.stream = stream;
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = 0;
+        err = cudaLaunchKernelEx(&cfg, moe_route_scan_kernel, C, T, K, E, tile_rows, cap, n_counters,
+                                 ccount, ws);
+        if (err != cudaSuccess) return err;
+        cfg.gridDim = dim3((unsigned)C);
+        cfg.blockDim = dim3(kChunkThreads);
+        cfg.dynamicSmemBytes = csmem;
+        return cudaLaunchKernelEx(&cfg, moe_route_scatter_kernel, topk_ids, topk_w, R, E, chunk,
+                                  static_cast<const int*>(ccount), ws);
+    }
     const size_t smem = sizeof(int) * ((size_t)kRouteWarps * E + (E + 1) + 64);
     // limit raised once per device to what E <= 1024 can need
     static bool limit_set[64];
