@@ -130,3 +130,18 @@ def test_padded_validation_codes_without_device(lib):
     assert call(Ip=192) == 2      # stored size not 128, 256 or a multiple of 512
     assert call(T=0) == 0
     assert moe.call_launches(16, 255, 128, 9, 3) == -1
+
+
+def test_w4a16_entry_and_plan_without_device(lib):
+    import mixture_experts_mxfp4_gb300 as moe
+
+    good = 1 << 20
+    args = [good] * 8
+    assert moe.forward_w4a16_ptr(*args, 16, 384, 128, 9, 3, 0) == 2   # unsupported d_model
+    assert moe.forward_w4a16_ptr(*args, 0, 256, 128, 9, 3, 0) == 0    # empty batch
+    pl = moe.get_plan_w4a16(16, 7168, 256, 257, 9)
+    ref = moe.get_plan(16, 7168, 256, 257, 9)
+    assert pl.bf16_act == 1 and ref.bf16_act == 0
+    assert pl.region("a1b")[1] == pl.cap * 7168 * 2 and pl.region("a2b")[1] == pl.cap * 256 * 2
+    assert pl.region("a1q")[1] == 0 and ref.region("a1b")[1] == 0
+    assert moe.load_library().moe_mxfp4_workspace_size_w4a16(16, 7168, 256, 257, 9) == pl.workspace_bytes
