@@ -183,7 +183,8 @@ __device__ int front_route(const GemmParams& p, int* scr, int* pos, int4* tcache
         }
     }
     if (write_global) {
-        if (tid <= E) p.ws.seg_start[tid] = seg[tid];
+        if (tid < E) p.ws.seg_start[tid] = seg[tid];
+        if (tid == 0) p.ws.seg_start[E] = seg[E];  // (E may equal the thread count)
         if (tid < E && cnt > 0) {
             for (int blk = seg_e / bm; blk < (seg_e + padded) / bm; ++blk) p.ws.block_expert[blk] = tid;
             for (int q = seg_e + cnt; q < seg_e + padded; ++q) {

@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     block_scan2(valid_incl, dummy, wsum, wsum + 32);
     const int total_padded = s_totals[0], total_tiles = s_totals[1];
 
-    if (tid <= E) ws.seg_start[tid] = seg[tid];
+    if (tid < E) ws.seg_start[tid] = seg[tid];
+    if (tid == 0) ws.seg_start[E] = seg[E];  // (E may equal the thread count)
     if (tid < E && cnt > 0) {
         for (int j = 0; j < ntiles; ++j) {
             const int rows = min(tile_rows, padded - j * tile_rows);
@@ -263,7 +264,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     block_scan2(valid_incl, dummy, wsum, wsum + 32);
     const int total_padded = s_totals[0], total_tiles = s_totals[1];
 
-    if (tid <= E) ws.seg_start[tid] = seg[tid];
+    if (tid < E) ws.seg_start[tid] = seg[tid];
+    if (tid == 0) ws.seg_start[E] = seg[E];  // (E may equal the thread count)
     if (tid < E) {
         // chunk c's routes of this expert start after the earlier chunks' ones
         int run = seg_e;

@@ -261,6 +261,19 @@ def test_large_tiles_mid_shape(moe, launch_mode):
     full_check(moe, w, inp)
 
 
+@pytest.mark.parametrize("T,D,I,E,K", [
+    (8, 128, 128, 1, 1),        # minimum dims, one expert, topk 1
+    (12, 256, 128, 40, 16),     # maximum topk
+    (24, 256, 128, 1024, 8),    # maximum E (routing histogram of 1024 experts)
+    (16, 256, 128, 384, 8),     # 384 experts: the single-launch router at its limit
+    (455, 256, 128, 33, 9),     # 4095 routes: one-CTA routing
+    (456, 256, 128, 33, 9),     # 4104 routes: routing on many CTAs
+])
+def test_limits_and_routing_threshold(moe, T, D, I, E, K):
+    w, inp = _small(T=T, D=D, I=I, E=E, K=K, seed=5)
+    full_check(moe, w, inp)
+
+
 def test_empty_batch(moe):
     m = moe.MoeMXFP4(0, 256, 128, 9, 3)
     e = torch.empty(0, device="cuda")
