@@ -339,6 +339,35 @@ def run_gpu(args, w, world, rank, local):
         s1.record(stream)
         s1.synchronize()
         e2e_ms += s0.elapsed_time(s1)
+    # ---- the same call captured in a CUDA graph and replayed (L2 flushed between
+    # replays, events around each replay); reported beside the direct calls
+    graph_us = None
+    try:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            m.forward(*fargs, out=out)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            m.forward(*fargs, out=out)
+        g_ms = 0.0
+        g_steps = max(1, min(args.steps, 200))
+        for _ in range(g_steps + 3):
+            flush.zero_()
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            graph.replay()
+            g1.record(stream)
+            g1.synchronize()
+            g_ms += g0.elapsed_time(g1) if _ >= 3 else 0.0
+        if m.device_status() != 0:
+            raise RuntimeError("device status after graph replays")
+        graph_us = 1e3 * g_ms / g_steps
+    except Exception as exc:  # reported, not fatal: the direct calls are the metric
+        print(f"graph replay not measured: {exc}", file=sys.stderr)
     e2e_max = max_over_ranks(e2e_ms / 1e3, world, dev if world > 1 else None)
     e2e_value = aggregate_value(w.T * e2e_steps, world, e2e_max)
     h2d = h_pack.numel()
@@ -374,6 +403,7 @@ def run_gpu(args, w, world, rank, local):
                    "launch": "single (routing + quantisation inside the GEMM kernel)"
                    if single else "separate kernels"},
         "us_per_call": us_call,
+        "us_per_call_graph_replay": graph_us,
         "per_kernel_us": {n: 1e3 * v / k_steps for n, v in per_kernel.items()},
         "per_kernel_note": f"{k_steps} steps with events between kernels (serialised)",
         "dominant_kernel": dom,
