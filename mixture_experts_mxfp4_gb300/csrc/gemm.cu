@@ -45,6 +45,9 @@
 //           scale-factor layout ahead of the MMA warps
 //   warps 4-11  epilogue: two groups of four warps take alternate items; the two
 //           MMA warps' partial accumulators are summed in a fixed order
+// Single-launch mode (few routes): the CTAs also route (in shared memory) and
+// quantise the hidden states before the first route-tile copies (front_route,
+// front_quant), so no routing or quantisation kernel runs before this one.
 // All waits are bounded (ptx.cuh).
 #include <cuda_bf16.h>
 
