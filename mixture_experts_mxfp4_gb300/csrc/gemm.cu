@@ -42,7 +42,8 @@
 //           with narrow (small-N) MMAs
 //   warp 2  also allocates / frees TMEM
 //   warp 3  rearranges each stage's raw scale tiles into the tcgen05
-//           scale-factor layout ahead of the MMA warps
+//           scale-factor layout ahead of the MMA warps (with one MMA warp it
+//           also copies them to TMEM and signals when the copies have run)
 //   warps 4-11  epilogue: two groups of four warps take alternate items; the two
 //           MMA warps' partial accumulators are summed in a fixed order
 // Single-launch mode (few routes): the CTAs also route (in shared memory) and
@@ -437,6 +438,9 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, ui
 }
 
 
+// kSfByLayoutWarp: warp 3 also copies the scale factors to TMEM (one MMA warp);
+// a template parameter so that each geometry's kernel carries only its scheme.
+template <bool kSfByLayoutWarp>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmSA1,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSB1,
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = sfull + kMaxStages;
     uint64_t* tempty = tfull + kMaxAccBufs;
     uint64_t* drain = tempty + kMaxAccBufs;  // one per MMA warp
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 3);  // drain[2]: scale-layout warp
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // per epilogue group: a 4 KB exchange buffer (kXchgBytes apart)
     float* xchg = reinterpret_cast<float*>(smem + p.off_xchg);
@@ -480,6 +484,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
+        mbar_init(&drain[2], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -765,7 +770,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                         if (lane == 0) {
                             tc_fence_after();
-                            copy_scales(s, q);
+                            if (!kSfByLayoutWarp) copy_scales(s, q);  // else warp 3 did
                         }
                     }
                     // this warp's next stage g + MW (its slot's previous fill, stage
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t pn = ph;
                     advance(sn, pn);
                     int rd = 0;
-                    if (lane == 0 && p.lookahead && g + MW < g_total)
+                    if (lane == 0 && p.lookahead && !kSfByLayoutWarp && g + MW < g_total)
                         rd = (mbar_test(&full[sn], pn) && mbar_test(&sfready[sn], pn)) ? 1 : 0;
                     rd = __shfl_sync(0xffffffffu, rd, 0);
                     if (rd && lane == 0) {
@@ -833,6 +838,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
     } else if (warp == 3) {
         // ------------------------------------------------------------ scale layout
+        bool copied = false;  // this warp issued scale-factor copies (drained below)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -853,7 +859,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     sf_to_atoms(st + q.off_sb, 16, q.natoms, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sfready[s]);
+                    if (lane == 0) {
+                        if (kSfByLayoutWarp) {
+                            // the scale factors to TMEM as well; sfready completes once the
+                            // copies have run (the slot's previous stage has finished: its
+                            // MMAs freed the slot before this stage's copies were issued)
+                            tc_fence_after();
+                            const uint32_t sfa = tmem_base + p.sf_col0 + (uint32_t)s * p.sf_cols;
+                            const uint32_t sfb = sfa + 4u * (uint32_t)(q.mblocks * q.natoms);
+                            const uint64_t da = smem_desc(smem_u32(st + q.off_sa), 0, 128, 0);
+                            const uint64_t db = smem_desc(smem_u32(st + q.off_sb), 0, 128, 0);
+                            for (int c = 0; c < q.mblocks * q.natoms; ++c)
+                                tmem_cp_sf(sfa + 4u * (uint32_t)c, da + (uint64_t)(32 * c));
+                            for (int c = 0; c < q.natoms; ++c)
+                                tmem_cp_sf(sfb + 4u * (uint32_t)c, db + (uint64_t)(32 * c));
+                            tc_commit(&sfready[s]);
+                            copied = true;
+                        } else {
+                            mbar_arrive(&sfready[s]);
+                        }
+                    }
                     if (++s == NS) {
                         s = 0;
                         ph ^= 1u;
@@ -861,6 +886,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
         }
+        if (lane == 0 && copied) {
+            // every copy this warp issued has run before TMEM is freed
+            tc_commit(&drain[2]);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&drain[2]), 0)) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(status, kErrTimeoutDrain);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         // Two groups of four warps take alternate items, so one item's global
@@ -1054,14 +1091,16 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream) {
     // Raise the dynamic shared-memory limit once per device.
     static bool limit_set[64];
+    auto kernel = p.sf_by_layout_warp ? moe_gemm_kernel<true> : moe_gemm_kernel<false>;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!limit_set[dev]) {
-        err = cudaFuncSetAttribute(moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kGemmSmemLimit);
-        if (err != cudaSuccess) return err;
+        for (auto k : {moe_gemm_kernel<true>, moe_gemm_kernel<false>}) {
+            err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemLimit);
+            if (err != cudaSuccess) return err;
+        }
         limit_set[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
@@ -1074,7 +1113,7 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_gemm_kernel, maps[0], maps[1], maps[2], maps[3], maps[4],
+    return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], maps[4],
                               maps[5], maps[6], maps[7], p);
 }
 

@@ -62,6 +62,7 @@ struct GemmParams {
     int mma_warps;      // MMA-issuing warps (1 or 2); warp w takes the CTA's stages g % mma_warps == w
     int acc_bufs;       // TMEM accumulator buffers (items in flight between MMA and epilogue)
     int lookahead;      // MMA warps copy the next stage's scale factors early (needs ns % mma_warps == 0)
+    int sf_by_layout_warp;  // the scale-layout warp also copies the scale factors to TMEM (one MMA warp)
     uint32_t slot_bytes;  // bytes per ring slot (the larger stage layout)
     uint32_t acc_cols;    // TMEM columns per accumulator buffer
     uint32_t sf_cols;     // TMEM scale-factor columns per ring slot
