@@ -439,8 +439,9 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, ui
 
 
 // kSfByLayoutWarp: warp 3 also copies the scale factors to TMEM (one MMA warp);
-// a template parameter so that each geometry's kernel carries only its scheme.
-template <bool kSfByLayoutWarp>
+// kFront: single launch (routing and quantisation in this kernel; p.fused_front).
+// Template parameters so that each configuration's kernel carries only its code.
+template <bool kSfByLayoutWarp, bool kFront>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmSA1,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSB1,
@@ -479,7 +480,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&sfull[s], 1);
         }
         for (int a = 0; a < p.acc_bufs; ++a) {
-            mbar_init(&tfull[a], (uint32_t)p.mma_warps);
+            mbar_init(&tfull[a], (uint32_t)(kSfByLayoutWarp ? 1 : 2));
             mbar_init(&tempty[a], 128);
         }
         mbar_init(&drain[0], 1);
@@ -503,7 +504,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     grid_dep_wait();
     // Single-launch path: route in shared memory (the ring is not in use yet);
     // otherwise the routing kernel's tile count.
-    const bool front = p.fused_front != 0;
+    constexpr bool front = kFront;
+    // MMA-issuing warps: one exactly when warp 3 copies the scale factors (the host
+    // geometry ties the two; launch_gemm checks it)
+    constexpr int kMW = kSfByLayoutWarp ? 1 : 2;
     int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
     int* fpos = reinterpret_cast<int*>(smem + p.off_xchg);  // route -> slot (front end only)
     uint4 qfirst = make_uint4(0, 0, 0, 0);  // epilogue threads: first hidden-state load
@@ -702,7 +706,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
     }
-    if (warp == 1 || (warp == 2 && p.mma_warps == 2)) {
+    if (warp == 1 || (warp == 2 && kMW == 2)) {
         // ------------------------------------------------------------ MMA
         // The CTA's stages are numbered g = 0, 1, ... in (stage, item, k-stage)
         // order; MMA warp w issues the stages with g % mma_warps == w into its
@@ -712,7 +716,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // copied before this stage's MMAs are issued.  Slot and phase indices
         // advance incrementally (no division on the per-stage path).
         const int w = (int)warp - 1;
-        const int MW = p.mma_warps;
+        constexpr int MW = kMW;
         auto advance = [&](int& ss, uint32_t& pp) {
             ss += MW;
             while (ss >= NS) {
@@ -908,7 +912,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t bar_id = 1u + (uint32_t)grp;
         float* xg = xchg + grp * (kXchgBytes / 4);
         const int R = p.R;
-        const int MW = p.mma_warps;
+        constexpr int MW = kMW;
         int local = 0;
         int a_next = 0;         // accumulator buffer of the CTA's item `local`
         uint32_t aph_next = 0;  // and its use parity
@@ -1091,13 +1095,16 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream) {
     // Raise the dynamic shared-memory limit once per device.
     static bool limit_set[64];
-    auto kernel = p.sf_by_layout_warp ? moe_gemm_kernel<true> : moe_gemm_kernel<false>;
+    if ((p.sf_by_layout_warp != 0) != (p.mma_warps == 1)) return cudaErrorInvalidValue;
+    auto kernel = p.sf_by_layout_warp ? (p.fused_front ? moe_gemm_kernel<true, true> : moe_gemm_kernel<true, false>)
+                                      : (p.fused_front ? moe_gemm_kernel<false, true> : moe_gemm_kernel<false, false>);
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!limit_set[dev]) {
-        for (auto k : {moe_gemm_kernel<true>, moe_gemm_kernel<false>}) {
+        for (auto k : {moe_gemm_kernel<true, true>, moe_gemm_kernel<true, false>, moe_gemm_kernel<false, true>,
+                       moe_gemm_kernel<false, false>}) {
             err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemLimit);
             if (err != cudaSuccess) return err;
         }
