@@ -440,8 +440,10 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, ui
 
 // kSfByLayoutWarp: warp 3 also copies the scale factors to TMEM (one MMA warp);
 // kFront: single launch (routing and quantisation in this kernel; p.fused_front).
+// kKs1, kKs2: K-steps per stage of stage 1 / stage 2, kMb2: weight blocks per
+// stage-2 item (0: read from the geometry at run time).
 // Template parameters so that each configuration's kernel carries only its code.
-template <bool kSfByLayoutWarp, bool kFront>
+template <bool kSfByLayoutWarp, bool kFront, int kKs1, int kKs2, int kMb2>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmSA1,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSB1,
@@ -508,6 +510,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // MMA-issuing warps: one exactly when warp 3 copies the scale factors (the host
     // geometry ties the two; launch_gemm checks it)
     constexpr int kMW = kSfByLayoutWarp ? 1 : 2;
+    // the generic instantiation keeps one copy of each phase loop: its shapes
+    // are small, where cold code after launch costs more than the loop
+    constexpr int kPhaseUnroll = kKs1 ? 2 : 1;
+    // per-phase K-steps per stage and weight blocks per item (constants where the
+    // instantiation fixes them; the phase loops below are unrolled)
+    auto ks_of = [&](int phs) -> int {
+        const int c = phs == 0 ? kKs1 : kKs2;
+        return c ? c : p.g[phs].kstage_elems / 64;
+    };
+    auto mb_of = [&](int phs) -> int { return phs == 0 ? 1 : (kMb2 ? kMb2 : p.g[1].mblocks); };
+    auto na_of = [&](int phs) -> int {  // scale atoms per 128-row block and stage
+        return (phs == 0 ? kKs1 : kKs2) ? ks_of(phs) / 2 : p.g[phs].natoms;
+    };
     int4* tcache = reinterpret_cast<int4*>(smem + p.off_tiles);
     int* fpos = reinterpret_cast<int*>(smem + p.off_xchg);  // route -> slot (front end only)
     uint4 qfirst = make_uint4(0, 0, 0, 0);  // epilogue threads: first hidden-state load
@@ -596,7 +611,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 resolved = true;
             };
-            for (int phs = 0; phs < 2 && ok; ++phs) {
+#pragma unroll kPhaseUnroll
+            for (int phs = 0; phs < 2; ++phs) {
+                if (!ok) break;
                 if (phs == 1 && !resolved) resolve();
                 if (!ok) break;
                 const StageGeom& q = p.g[phs];
@@ -604,8 +621,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const CUtensorMap* mSA = phs ? &tmSA2 : &tmSA1;
                 const CUtensorMap* mB = phs ? &tmB2 : &tmB1;
                 const CUtensorMap* mSB = phs ? &tmSB2 : &tmSB1;
-                const int kbytes_stage = q.kstage_elems / 2;  // bytes of one row per stage
-                const uint32_t arows = 128u * (uint32_t)q.mblocks;
+                const int kbytes_stage = ks_of(phs) * 32;  // bytes of one row per stage
+                const int MBp = mb_of(phs);
+                const uint32_t arows = 128u * (uint32_t)MBp;
                 for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                     const Item x = decode_item(q, p.ws.tiles, it, tcache);
                     for (int ks = x.ks0; ks < x.ks1; ++ks) {
@@ -620,7 +638,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         uint8_t* st = smem + (size_t)s * p.slot_bytes;
                         const int kt0 = ks * q.nkt;  // first K box of the stage
                         const int rg = phs == 0 ? x.e * 2 * p.I + x.f * 64
-                                                : x.e * p.D + x.f * 128 * q.mblocks;
+                                                : x.e * p.D + x.f * 128 * MBp;
                         // weight scales, then the weight tile: they do not depend on stage 1
                         mbar_arrive_expect_tx(&sfull[s], arows * q.sr_a + (uint32_t)p.tile_rows * 16u);
                         mbar_arrive_expect_tx(&full[s], (arows + (uint32_t)p.tile_rows) * kbytes_stage);
@@ -732,25 +750,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int a = 0;           // accumulator buffer of the current item
         uint32_t aph = 0;    // and its use parity
         bool ok = true;
-        for (int phs = 0; phs < 2 && ok; ++phs) {
+#pragma unroll kPhaseUnroll
+        for (int phs = 0; phs < 2; ++phs) {
+            if (!ok) break;
             const StageGeom& q = p.g[phs];
             const uint32_t layout = (q.kb == 128) ? 2u : 4u;  // 128-byte / 64-byte swizzle
             const uint32_t sbo = 8u * q.kb;
-            const int ksteps = q.kstage_elems / 64;
-            const int MB = q.mblocks;
+            const int ksteps = ks_of(phs);
+            const int MB = mb_of(phs);
             const uint32_t a_box = (128u * MB * q.kb) >> 4;  // descriptor units (16 B)
             const uint32_t a_blk = (128u * q.kb) >> 4;       // next 128-row block
             const uint32_t b_box = ((uint32_t)p.tile_rows * q.kb) >> 4;
             // scale copies of slot ss for this stage's layout (lane 0 only); a
             // look-ahead copy may reach into the next stage's layout
-            auto copy_scales = [&](int ss, const StageGeom& qq) {
+            auto copy_scales = [&](int ss, const StageGeom& qq, int qmb, int qna) {
                 uint8_t* st = smem + (size_t)ss * p.slot_bytes;
-                const uint32_t sfa = sf_base(ss), sfb = sfa + 4u * qq.mblocks * qq.natoms;
+                const uint32_t sfa = sf_base(ss), sfb = sfa + 4u * qmb * qna;
                 const uint64_t da = smem_desc(smem_u32(st + qq.off_sa), 0, 128, 0);
                 const uint64_t db = smem_desc(smem_u32(st + qq.off_sb), 0, 128, 0);
-                for (int c = 0; c < qq.mblocks * qq.natoms; ++c)
+                for (int c = 0; c < qmb * qna; ++c)
                     tmem_cp_sf(sfa + 4u * c, da + (uint64_t)(32 * c));
-                for (int c = 0; c < qq.natoms; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
+                for (int c = 0; c < qna; ++c) tmem_cp_sf(sfb + 4u * c, db + (uint64_t)(32 * c));
             };
             const long g_phase_end = g + (long)(phs == 0 ? my_items0 : my_items1) * q.kstages;
             for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
@@ -774,7 +794,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                         if (lane == 0) {
                             tc_fence_after();
-                            if (!kSfByLayoutWarp) copy_scales(s, q);  // else warp 3 did
+                            if (!kSfByLayoutWarp) copy_scales(s, q, MB, na_of(phs));  // else warp 3 did
                         }
                     }
                     // this warp's next stage g + MW (its slot's previous fill, stage
@@ -788,18 +808,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     rd = __shfl_sync(0xffffffffu, rd, 0);
                     if (rd && lane == 0) {
                         tc_fence_after();
-                        copy_scales(sn, g + MW < g_phase_end ? q : p.g[1]);
+                        if constexpr (kKs1 == 0) {
+                            const StageGeom& qn = g + MW < g_phase_end ? q : p.g[1];
+                            copy_scales(sn, qn, qn.mblocks, qn.natoms);
+                        } else if (g + MW < g_phase_end) {
+                            copy_scales(sn, q, MB, na_of(phs));
+                        } else {
+                            copy_scales(sn, p.g[1], mb_of(1), na_of(1));
+                        }
                     }
                     if (lane == 0) {
                         uint8_t* st = smem + (size_t)s * p.slot_bytes;
                         const uint64_t ad0 = smem_desc(smem_u32(st), 16, sbo, layout);
                         const uint64_t bd0 = smem_desc(smem_u32(st + q.off_b), 16, sbo, layout);
-                        const uint32_t sfa = sf_base(s), sfb = sfa + 4u * MB * q.natoms;
+                        const uint32_t sfa = sf_base(s), sfb = sfa + 4u * MB * na_of(phs);
                         for (int h = 0; h < MB; ++h) {
                             // block h: its own accumulator columns, A rows and weight scales
                             const uint32_t dh = d + (uint32_t)(h * p.tile_rows);
                             const uint64_t adh = ad0 + (uint64_t)(h * a_blk);
-                            const uint32_t sfah = sfa + 4u * (uint32_t)(h * q.natoms);
+                            const uint32_t sfah = sfa + 4u * (uint32_t)(h * na_of(phs));
                             if (ksteps == 8)
                                 issue_stage_mmas<8, 4>(dh, adh, bd0, a_box, b_box, idesc_even,
                                                        idesc_odd, sfah, sfb, 0, !first);
@@ -846,7 +873,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int phs = 0; phs < 2 && ok; ++phs) {
+#pragma unroll kPhaseUnroll
+        for (int phs = 0; phs < 2; ++phs) {
+            if (!ok) break;
             const StageGeom& q = p.g[phs];
             for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
@@ -858,9 +887,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint8_t* st = smem + (size_t)s * p.slot_bytes;
                     // block h's rows sit at h * 128 * sr_a; its natoms atoms replace them
                     // in place (128 * sr_a == natoms * 512)
-                    for (int h = 0; h < q.mblocks; ++h)
-                        sf_to_atoms(st + q.off_sa + h * 128 * q.sr_a, q.sr_a, q.natoms, lane);
-                    sf_to_atoms(st + q.off_sb, 16, q.natoms, lane);
+                    const int qmb = mb_of(phs), qna = na_of(phs);
+                    for (int h = 0; h < qmb; ++h)
+                        sf_to_atoms(st + q.off_sa + h * 128 * q.sr_a, q.sr_a, qna, lane);
+                    sf_to_atoms(st + q.off_sb, 16, qna, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -870,12 +900,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             // MMAs freed the slot before this stage's copies were issued)
                             tc_fence_after();
                             const uint32_t sfa = tmem_base + p.sf_col0 + (uint32_t)s * p.sf_cols;
-                            const uint32_t sfb = sfa + 4u * (uint32_t)(q.mblocks * q.natoms);
+                            const uint32_t sfb = sfa + 4u * (uint32_t)(qmb * qna);
                             const uint64_t da = smem_desc(smem_u32(st + q.off_sa), 0, 128, 0);
                             const uint64_t db = smem_desc(smem_u32(st + q.off_sb), 0, 128, 0);
-                            for (int c = 0; c < q.mblocks * q.natoms; ++c)
+                            for (int c = 0; c < qmb * qna; ++c)
                                 tmem_cp_sf(sfa + 4u * (uint32_t)c, da + (uint64_t)(32 * c));
-                            for (int c = 0; c < q.natoms; ++c)
+                            for (int c = 0; c < qna; ++c)
                                 tmem_cp_sf(sfb + 4u * (uint32_t)c, db + (uint64_t)(32 * c));
                             tc_commit(&sfready[s]);
                             copied = true;
@@ -926,10 +956,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 got = poll_word(p.ws.status + 15, kFrontReady, true, status, kErrTimeoutFront, abort_flag) ? 1 : 0;
             ok = named_bar_and(3, 256, got != 0);
         }
-        for (int phs = 0; phs < 2 && ok; ++phs) {
+#pragma unroll kPhaseUnroll
+        for (int phs = 0; phs < 2; ++phs) {
+            if (!ok) break;
             const StageGeom& q = p.g[phs];
             const int per = q.kstages;  // stages per item
-            const int MB = q.mblocks;
+            const int MB = mb_of(phs);
             for (int m = 0, it = item_of(phs, 0); it >= 0; it = item_of(phs, ++m), ++local) {
                 const int a = a_next;
                 const uint32_t aph = aph_next;
@@ -1093,22 +1125,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream) {
-    // Raise the dynamic shared-memory limit once per device.
-    static bool limit_set[64];
     if ((p.sf_by_layout_warp != 0) != (p.mma_warps == 1)) return cudaErrorInvalidValue;
-    auto kernel = p.sf_by_layout_warp ? (p.fused_front ? moe_gemm_kernel<true, true> : moe_gemm_kernel<true, false>)
-                                      : (p.fused_front ? moe_gemm_kernel<false, true> : moe_gemm_kernel<false, false>);
+    // instantiation: copy scheme, front end, and the stage shapes of the common
+    // configurations (decode-like, dense-like, prefill-like), else the generic one
+    const int ks1 = p.g[0].kstage_elems / 64, ks2 = p.g[1].kstage_elems / 64, mb2 = p.g[1].mblocks;
+    const bool f = p.fused_front != 0;
+    int spec;  // index into kernels[]
+    if (!p.sf_by_layout_warp)
+        spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 0 : 1;
+    else
+        spec = (ks1 == 8 && ks2 == 8 && mb2 == 1) ? 2 : (ks1 == 8 && ks2 == 4 && mb2 == 1) ? 3 : 4;
+    using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                              CUtensorMap, CUtensorMap, GemmParams);
+    static const KernelFn kernels[2][5] = {
+        {moe_gemm_kernel<false, false, 8, 4, 2>, moe_gemm_kernel<false, false, 0, 0, 0>,
+         moe_gemm_kernel<true, false, 8, 8, 1>, moe_gemm_kernel<true, false, 8, 4, 1>,
+         moe_gemm_kernel<true, false, 0, 0, 0>},
+        {moe_gemm_kernel<false, true, 8, 4, 2>, moe_gemm_kernel<false, true, 0, 0, 0>,
+         moe_gemm_kernel<true, true, 8, 8, 1>, moe_gemm_kernel<true, true, 8, 4, 1>,
+         moe_gemm_kernel<true, true, 0, 0, 0>}};
+    const KernelFn kernel = kernels[f ? 1 : 0][spec];
+    // Raise the dynamic shared-memory limit once per device and instantiation.
+    static bool limit_set[64][2][5];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!limit_set[dev]) {
-        for (auto k : {moe_gemm_kernel<true, true>, moe_gemm_kernel<true, false>, moe_gemm_kernel<false, true>,
-                       moe_gemm_kernel<false, false>}) {
-            err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemLimit);
-            if (err != cudaSuccess) return err;
-        }
-        limit_set[dev] = true;
+    if (!limit_set[dev][f ? 1 : 0][spec]) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemLimit);
+        if (err != cudaSuccess) return err;
+        limit_set[dev][f ? 1 : 0][spec] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
