@@ -16,9 +16,16 @@
  * An e8m0 scale byte s means 2^(s-127); one scale per 32 consecutive elements
  * along the contraction (K) dimension of a row.
  *
- * Ownership and threading: every pointer argument is device memory owned by
- * the caller; inputs are only read; the library never allocates on the call
- * path.  The scratch it needs is a caller-owned device buffer registered with
+ * Ownership and threading: every pointer argument is owned by the caller and
+ * is device memory, except that the per-call buffers of the forward entry
+ * points (hidden, topk_ids, topk_weights, out) may instead be pinned host
+ * memory mapped into the device's address space (cudaHostAlloc, or
+ * cudaHostRegister with cudaHostRegisterMapped, on a system with unified
+ * addressing): the kernels then read the inputs and write the output in place
+ * (on GB300 over NVLink-C2C) and no staging copy is made.  Weights, scales and
+ * the workspace must be device memory (tensor-memory-access copies read them).
+ * Pageable host memory is not supported (not checked).
+ * Inputs are only read; the library never allocates on the call path.  The scratch it needs is a caller-owned device buffer registered with
  * moe_mxfp4_set_workspace (one per device; calls that share it must be ordered
  * on the GPU, e.g. issued to one stream).  All work is enqueued on `stream`; the
  * call returns after enqueueing.
@@ -91,6 +98,8 @@ moe_status_t moe_mxfp4_set_workspace(void* dev_ptr, size_t bytes);
  *                 with Q the MX quantiser (shared exponent floor(log2 amax) - 2,
  *                 round to nearest even, saturate at 6), fp32 accumulation, and the
  *                 sum over k in ascending order (deterministic).
+ * hidden, topk_ids, topk_weights and out: device memory or mapped pinned host
+ * memory (see Ownership above).
  * Asynchronous on `stream`.  T == 0 returns MOE_OK and enqueues nothing.
  */
 moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* w13_scale,
@@ -244,6 +253,13 @@ moe_status_t moe_mxfp4_get_plan_w4a16(int T, int d_model, int d_inter, int E, in
 
 /* Version string of the library build. */
 const char* moe_mxfp4_version(void);
+
+/* Where a per-call buffer lives, for the host-memory case of the forward entry
+ * points: 0 device (or managed) memory; 1 host memory that the current device
+ * reads and writes at the same address (pinned and mapped); -1 neither
+ * (pageable or unknown memory: not usable as a forward argument).  A host-side
+ * query (cudaPointerGetAttributes); no device work. */
+int moe_mxfp4_pointer_kind(const void* ptr);
 
 /* ------------------------------------------------------------------ timing */
 

@@ -53,6 +53,7 @@ EXPORTS = [
     "moe_mxfp4_forward_w4a16",
     "moe_mxfp4_workspace_size_w4a16",
     "moe_mxfp4_get_plan_w4a16",
+    "moe_mxfp4_pointer_kind",
 ]
 
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
@@ -122,6 +123,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_forward_w4a16.argtypes = [P, P, P, P, P, P, P, P, i, i, i, i, i, P]
     lib.moe_mxfp4_version.restype = ctypes.c_char_p
     lib.moe_mxfp4_version.argtypes = []
+    lib.moe_mxfp4_pointer_kind.restype = i
+    lib.moe_mxfp4_pointer_kind.argtypes = [P]
     lib.moe_mxfp4_num_kernels.restype = i
     lib.moe_mxfp4_num_kernels.argtypes = []
     lib.moe_mxfp4_set_kernel_timing.restype = i
@@ -262,6 +265,23 @@ def version() -> str:
     return load_library().moe_mxfp4_version().decode()
 
 
+_MAPPED = {}
+
+
+def _host_mapped(ptr: int, device) -> bool:
+    """The device reads and writes this pinned host address at the same pointer
+    (moe_mxfp4_pointer_kind == 1); remembered per (device, address)."""
+    import torch
+
+    key = (device.index, ptr)
+    if key not in _MAPPED:
+        with torch.cuda.device(device):
+            _MAPPED[key] = load_library().moe_mxfp4_pointer_kind(ctypes.c_void_p(ptr)) == 1
+        if len(_MAPPED) > 4096:
+            _MAPPED.clear()
+    return _MAPPED[key]
+
+
 class MoeMXFP4:
     """One MoE layer shape with its own device workspace (a torch uint8 tensor).
 
@@ -270,7 +290,8 @@ class MoeMXFP4:
     d_model_pad / d_inter_pad the weights are stored with those padded sizes
     (moe_mxfp4_forward_padded); hidden and out keep d_model columns.  With
     activations="bf16" the forward keeps the activations in bf16 (W4A16,
-    moe_mxfp4_forward_w4a16).
+    moe_mxfp4_forward_w4a16).  hidden, topk_ids, topk_weights and out may be
+    pinned host tensors: the kernels read and write them in place.
     """
 
     def __init__(self, T, d_model, d_inter, E, topk, device="cuda", d_model_pad=None,
@@ -312,16 +333,28 @@ class MoeMXFP4:
 
         T, D, I, E, K = self.shape
         if out is None:
-            out = torch.empty((T, D), dtype=torch.bfloat16, device=hidden.device)
-        for t in (hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights, out):
+            out = torch.empty((T, D), dtype=torch.bfloat16, device=hidden.device,
+                              pin_memory=not hidden.is_cuda)
+        for t in (w13, w13_scale, w2, w2_scale):
             if not t.is_cuda or not t.is_contiguous():
-                raise ValueError("all tensors must be contiguous CUDA tensors")
+                raise ValueError("weights and scales must be contiguous CUDA tensors")
+        # the per-call tensors may also live in pinned host memory, which the
+        # kernels read and write in place (mapped into the device's address space)
+        for t in (hidden, topk_ids, topk_weights, out):
+            if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+                raise ValueError("hidden, topk_ids, topk_weights and out must be contiguous "
+                                 "CUDA tensors or pinned host tensors")
+            if t.is_cuda and t.device != w13.device:
+                raise ValueError("all CUDA tensors must be on the weights' device")
+            if not t.is_cuda and t.numel() and not _host_mapped(t.data_ptr(), w13.device):
+                raise ValueError("a pinned host tensor that the device cannot address at "
+                                 "the same pointer")
         if hidden.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
             raise ValueError("hidden and out must be bfloat16")
         if topk_ids.dtype != torch.int32 or topk_weights.dtype != torch.float32:
             raise ValueError("topk_ids must be int32 and topk_weights float32")
         if stream is None:
-            stream = torch.cuda.current_stream(hidden.device).cuda_stream
+            stream = torch.cuda.current_stream(w13.device).cuda_stream
         set_workspace(self.ws_ptr, self.ws_bytes)
         if self.bf16_act:
             code = forward_w4a16_ptr(hidden.data_ptr(), w13.data_ptr(), w13_scale.data_ptr(),

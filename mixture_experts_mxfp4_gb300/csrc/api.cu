@@ -335,6 +335,18 @@ extern "C" {
 
 const char* moe_mxfp4_version(void) { return "moe_mxfp4 0.1 (sm_103a, tcgen05 mxf4)"; }
 
+int moe_mxfp4_pointer_kind(const void* ptr) {
+    if (!ptr) return -1;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear the error the query may leave
+        return -1;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return 0;
+    if (a.type == cudaMemoryTypeHost && a.devicePointer == ptr) return 1;
+    return -1;
+}
+
 const char* moe_mxfp4_status_string(moe_status_t s) {
     switch (s) {
         case MOE_OK: return "ok";

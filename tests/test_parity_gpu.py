@@ -389,6 +389,44 @@ def test_launch_modes_bitwise_identical(moe):
     assert torch.equal(sids[0], sids[1])
 
 
+@pytest.mark.parametrize("shape,act", [
+    ((16, 7168, 256, 257, 9), "mxfp4"),   # decode: single launch
+    ((64, 512, 256, 17, 5), "mxfp4"),     # 320 routes: separate kernels
+    ((820, 256, 128, 9, 5), "mxfp4"),     # 4100 routes: routing on many CTAs
+    ((16, 256, 128, 9, 3), "bf16"),       # W4A16 path
+], ids=["decode_single", "separate", "multi_cta_routing", "w4a16"])
+def test_host_buffers_bitwise_identical(moe, shape, act):
+    """hidden, topk_ids, topk_weights and out in pinned host memory: the kernels
+    read and write them in place, with the same result bit for bit as with the
+    same data in device memory."""
+    T, D, I, E, K = shape
+    w = workloads.custom(T, D, I, E, K)
+    inp = workloads.make_inputs(w, seed=7)
+    dev = torch.device("cuda")
+    m = moe.MoeMXFP4(T, D, I, E, K, activations=act)
+    wts = [inp[k].to(dev) for k in ("w13", "w13_scale", "w2", "w2_scale")]
+    d_out = m.forward(inp["hidden"].to(dev), *wts, inp["topk_ids"].to(dev),
+                      inp["topk_weights"].to(dev))
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    h = {k: inp[k].contiguous().pin_memory() for k in ("hidden", "topk_ids", "topk_weights")}
+    h_out = torch.full((T, D), float("nan"), dtype=torch.bfloat16).pin_memory()
+    m.forward(h["hidden"], *wts, h["topk_ids"], h["topk_weights"], out=h_out)
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    assert torch.equal(h_out.view(torch.int16), d_out.cpu().view(torch.int16))
+
+
+def test_host_buffers_rejects_pageable(moe):
+    w = workloads.custom(16, 256, 128, 9, 3)
+    inp = workloads.make_inputs(w)
+    m = moe.MoeMXFP4(16, 256, 128, 9, 3)
+    dev = torch.device("cuda")
+    wts = [inp[k].to(dev) for k in ("w13", "w13_scale", "w2", "w2_scale")]
+    with pytest.raises(ValueError):
+        m.forward(inp["hidden"], *wts, inp["topk_ids"].to(dev), inp["topk_weights"].to(dev))
+
+
 # ------------------------------------------------------------------ failure reporting
 
 def test_bounded_wait_timeout_is_reported_and_recoverable(moe):
