@@ -145,3 +145,12 @@ def test_w4a16_entry_and_plan_without_device(lib):
     assert pl.region("a1b")[1] == pl.cap * 7168 * 2 and pl.region("a2b")[1] == pl.cap * 256 * 2
     assert pl.region("a1q")[1] == 0 and ref.region("a1b")[1] == 0
     assert moe.load_library().moe_mxfp4_workspace_size_w4a16(16, 7168, 256, 257, 9) == pl.workspace_bytes
+
+
+def test_pointer_kind_without_device(lib):
+    """Null and ordinary host memory are never usable as forward buffers; with no
+    GPU present every query answers -1 (and leaves no error behind)."""
+    assert lib.moe_mxfp4_pointer_kind(None) == -1
+    buf = ctypes.create_string_buffer(64)
+    assert lib.moe_mxfp4_pointer_kind(ctypes.cast(buf, ctypes.c_void_p)) == -1
+    assert lib.moe_mxfp4_pointer_kind(ctypes.cast(buf, ctypes.c_void_p)) == -1
