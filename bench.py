@@ -182,9 +182,17 @@ def run_reference(args, w):
 
     inp = workloads.to_numpy(workloads.make_inputs(w))
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    ntok = min(w.T, max(1, args.ref_tokens))
+    # A step is the oracle on a sample of the batch's tokens (routing over the whole
+    # batch), sized from one untimed probe call so that the W warm-up and K timed
+    # steps take about --ref-budget-s seconds (at most --ref-tokens tokens a step).
+    nmax = min(w.T, max(1, args.ref_tokens))
+    t0 = time.perf_counter()
+    oracle.forward(**inp, tokens=np.arange(nmax, dtype=np.int32), threads=threads, want_h=False)
+    per_tok = (time.perf_counter() - t0) / nmax
+    calls = max(1, args.steps) + max(0, args.warmup)
+    ntok = int(min(nmax, max(1, args.ref_budget_s / (calls * per_tok))))
     toks = np.arange(ntok, dtype=np.int32)
-    for _ in range(max(0, min(args.warmup, 1))):
+    for _ in range(max(0, args.warmup)):
         oracle.forward(**inp, tokens=toks, threads=threads, want_h=False)
     times = []
     for _ in range(max(1, args.steps)):
@@ -201,7 +209,8 @@ def run_reference(args, w):
         "config": {"workload": w.name, "T": w.T, "d_model": w.D, "d_inter": w.I, "E": w.E,
                    "topk": w.K, "sample_tokens": ntok},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{ntok} of {w.T} tokens per step, full routing"},
+                         "sample": f"{ntok} of {w.T} tokens per step (sized for a "
+                                   f"{args.ref_budget_s:g} s run), routing over the whole batch"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -475,6 +484,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--ref-budget-s", type=float, default=90.0)
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--activations", default="mxfp4", choices=["mxfp4", "bf16"],

@@ -1,0 +1,29 @@
+"""The benchmark's reference arm on CPU: `bench.py --impl reference` times the
+oracle on a sample of the workload and prints one JSON line with the contract's
+keys; it runs the requested warm-up steps and sizes its sample to the time budget."""
+import json
+import os
+import subprocess
+import sys
+
+from conftest import ROOT
+
+
+def test_reference_arm_json_line():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+           "--warmup", "3", "--ref-budget-s", "3", "--workload", "tiny_T16_D256_I128_E9_K3"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference"
+    assert line["steps"] == 3 and line["warmup"] == 3
+    assert line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "tiny_T16_D256_I128_E9_K3"
