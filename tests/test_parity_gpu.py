@@ -389,6 +389,34 @@ def test_launch_modes_bitwise_identical(moe):
     assert torch.equal(sids[0], sids[1])
 
 
+def test_quantiser_every_bf16_value(moe, launch_mode):
+    """Every finite bf16 value goes through the activation quantiser (the quant
+    kernel, or the one inside the GEMM kernel in single-launch mode): once in
+    bit-pattern order, so a block holds 32 neighbouring values (ties and
+    saturation), once shuffled (mixed magnitudes).  Codes and scales must equal
+    the oracle's bit for bit.  The GEMM outputs of such inputs overflow and are
+    not checked."""
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = ((bits >> 7) & 0xFF) != 0xFF
+    vals = bits[finite].astype(np.uint16)
+    rng = np.random.default_rng(11)
+    allv = np.concatenate([vals, rng.permutation(vals)])
+    D = 256
+    allv = np.concatenate([allv, np.zeros((-len(allv)) % D, np.uint16)])
+    T = len(allv) // D
+    w = workloads.custom(T, D, 128, 9, 1)
+    inp = workloads.make_inputs(w, seed=2)
+    inp["hidden"] = torch.from_numpy(allv.view(np.int16).reshape(T, D).copy()).view(torch.bfloat16)
+    m, t, out = run_gpu(moe, inp, w)
+    ws = ws_arrays(m, w)
+    f32 = (allv.astype(np.uint32) << 16).view(np.float32).reshape(T, D)
+    for tok in range(T):
+        pos = int(ws["route_pos"][tok])
+        codes, scales = oracle.quant_row(f32[tok])
+        np.testing.assert_array_equal(ws["a1q"][pos], codes, err_msg=f"codes of token {tok}")
+        np.testing.assert_array_equal(ws["a1s"][pos, : D // 32], scales, err_msg=f"scales of token {tok}")
+
+
 @pytest.mark.parametrize("shape,act", [
     ((16, 7168, 256, 257, 9), "mxfp4"),   # decode: single launch
     ((64, 512, 256, 17, 5), "mxfp4"),     # 320 routes: separate kernels
