@@ -366,23 +366,29 @@ def run_gpu(args, w, world, rank, local):
     hi = h_pack[hb:hb + ib].view(torch.int32).view(w.T, w.K)
     hw = h_pack[hb + ib:].view(torch.float32).view(w.T, w.K)
     h_out2 = torch.empty(w.T, w.D, dtype=torch.bfloat16).pin_memory()
-    for _ in range(3):
-        m.forward(hh, *fargs[1:5], hi, hw, out=h_out2)
-    torch.cuda.synchronize(dev)
-    e2e_host_ms = 0.0
-    for _ in range(e2e_steps):
-        flush.zero_()
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        m.forward(hh, *fargs[1:5], hi, hw, out=h_out2)
-        s1.record(stream)
-        s1.synchronize()
-        e2e_host_ms += s0.elapsed_time(s1)
-    if m.device_status() != 0:
-        raise RuntimeError("device status after the host-buffer calls")
-    if not torch.equal(h_out2.view(torch.int16), h_out.view(torch.int16)):
-        raise RuntimeError("host-buffer call differs from the device-buffer call")
+    e2e_host_ms = None
+    try:
+        for _ in range(3):
+            m.forward(hh, *fargs[1:5], hi, hw, out=h_out2)
+        torch.cuda.synchronize(dev)
+        e2e_host_ms = 0.0
+        for _ in range(e2e_steps):
+            flush.zero_()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            m.forward(hh, *fargs[1:5], hi, hw, out=h_out2)
+            s1.record(stream)
+            s1.synchronize()
+            e2e_host_ms += s0.elapsed_time(s1)
+    except ValueError as exc:  # pinned memory the device cannot address in place
+        print(f"host-buffer calls not measured: {exc}", file=sys.stderr)
+        e2e_host_ms = None
+    if e2e_host_ms is not None:
+        if m.device_status() != 0:
+            raise RuntimeError("device status after the host-buffer calls")
+        if not torch.equal(h_out2.view(torch.int16), h_out.view(torch.int16)):
+            raise RuntimeError("host-buffer call differs from the device-buffer call")
     # ---- the same call captured in a CUDA graph and replayed (L2 flushed between
     # replays, events around each replay); reported beside the direct calls
     graph_us = None
@@ -414,6 +420,9 @@ def run_gpu(args, w, world, rank, local):
         print(f"graph replay not measured: {exc}", file=sys.stderr)
     e2e_max = max_over_ranks(e2e_ms / 1e3, world, dev if world > 1 else None)
     e2e_staged = aggregate_value(w.T * e2e_steps, world, e2e_max)
+    in_place = e2e_host_ms is not None
+    if not in_place:  # report the staged path as the end-to-end number
+        e2e_host_ms = e2e_ms
     e2e_host_max = max_over_ranks(e2e_host_ms / 1e3, world, dev if world > 1 else None)
     e2e_value = aggregate_value(w.T * e2e_steps, world, e2e_host_max)
     h2d = h_pack.numel()
@@ -459,8 +468,9 @@ def run_gpu(args, w, world, rank, local):
                              "peak": peak, "unit": "GB/s", "frac": fwd_gbs / peak},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "transfer": "pinned host inputs read and pinned host output written by the "
-                            "kernels in place (mapped host memory, NVLink-C2C); no staging copy",
+                "transfer": ("pinned host inputs read and pinned host output written by the "
+                             "kernels in place (mapped host memory, NVLink-C2C); no staging copy")
+                if in_place else "staged copies (pinned host memory not addressable in place)",
                 "us_per_step": 1e3 * e2e_host_ms / e2e_steps},
         "e2e_staged": {"value": e2e_staged, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h,
