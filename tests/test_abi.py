@@ -154,3 +154,19 @@ def test_pointer_kind_without_device(lib):
     buf = ctypes.create_string_buffer(64)
     assert lib.moe_mxfp4_pointer_kind(ctypes.cast(buf, ctypes.c_void_p)) == -1
     assert lib.moe_mxfp4_pointer_kind(ctypes.cast(buf, ctypes.c_void_p)) == -1
+
+
+@pytest.mark.parametrize("shape,rows", [
+    ((16, 7168, 256, 257, 9), 16),    # decode: 0.56 routes per expert
+    ((128, 7168, 256, 257, 9), 16),   # decode batch: 4.5
+    ((64, 256, 128, 9, 3), 32),       # 21.3
+    ((64, 256, 128, 5, 3), 64),       # 38.4
+    ((512, 7168, 2048, 33, 9), 128),  # dense shard: 140
+    ((4096, 7168, 256, 257, 9), 128), # prefill: 143 on average
+])
+def test_route_tile_width_rule(lib, shape, rows):
+    """Route-tile width: the smallest of 16/32/64/128 rows above the expected
+    routes per expert (T*topk/E <= 8, 24, 48, else 128)."""
+    import mixture_experts_mxfp4_gb300 as moe
+
+    assert moe.get_plan(*shape).tile_rows == rows
