@@ -27,3 +27,24 @@ def test_reference_arm_json_line():
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == "tiny_T16_D256_I128_E9_K3"
+
+
+def test_algorithmic_bytes_of_the_decode_workload():
+    """The roofline's byte count: touched experts x 3*I*D*17/32 (e2m1 weights plus one
+    e8m0 byte per 32), plus the quantised hidden rows for the GEMM kernel; the whole
+    call adds the bf16 hidden in, the bf16 output and 8 bytes per route."""
+    import numpy as np
+
+    import bench
+    import workloads
+
+    ids = np.array([[e, e + 1, 256] for e in range(0, 32, 2)], np.int32)  # 33 experts touched
+    w = workloads.custom(16, 7168, 256, 257, 3)
+    total, gemm, touched = bench.alg_bytes(w, ids)
+    assert touched == 33
+    per_expert = 3 * 256 * 7168 * 17 // 32  # 2.92 MB
+    assert per_expert == 2_924_544
+    assert gemm == 33 * per_expert + 16 * 7168 * 17 // 32
+    assert total == 33 * per_expert + 2 * 16 * 7168 * 2 + 16 * 3 * 8
+    _, gemm_bf16, _ = bench.alg_bytes(w, ids, bf16_act=True)
+    assert gemm_bf16 == 33 * per_expert + 16 * 7168 * 2
