@@ -45,8 +45,13 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            # MOE_ORACLE_LIB: a given build of moe_oracle.c (the mutation tests load
+            # copies with a planted mistake this way); otherwise build and load ours
+            path = os.environ.get("MOE_ORACLE_LIB")
+            if not path:
+                build()
+                path = _LIB
+            lib = ctypes.CDLL(path)
             P = ctypes.c_void_p
             i = ctypes.c_int
             lib.moe_oracle_e2m1.restype = ctypes.c_float
