@@ -4,10 +4,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 One step = one moe_mxfp4_forward call (route -> quant -> stage-1 GEMM ->
-stage-2 GEMM -> top-k sum) over one batch of synthetic inputs already resident
-in HBM.  Between steps the L2 is flushed (a 256 MiB write), so every step reads
-the expert weights from HBM.  Step time is the device time between CUDA events
-the library records on its stream before its first and after its last kernel.
+stage-2 GEMM with the top-k sum) over one batch of synthetic inputs already
+resident in HBM.  The default workload is the largest one-GPU configuration,
+the skewed prefill batch (T=4096, d_model 7168, d_inter 256, E 257, topk 9).
+Between steps the L2 is flushed (a 256 MiB write), so every step reads the
+expert weights from HBM.  Step time is the device time between CUDA events the
+library records on its stream before its first and after its last kernel.
 
 Multi-GPU (torchrun, one process per GPU): replicas only -- each rank runs an
 independent forward on its own batch (the op has no exchange step); the value
@@ -34,17 +36,24 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused MoE µs/call and tokens/s; achieved HBM TB/s or MXFP4 TFLOPS vs roofline"
-DEFAULT_WORKLOAD = "decode_T16_D7168_I256_E257_K9"
+DEFAULT_WORKLOAD = "prefill_zipf_T4096_D7168_I256_E257_K9"
 # Published number for this workload on the pages (MI355X, aiter): 152.7 us/call
 # for (T=16, E=257, d_inter=256, topk=9); context only.
 PUBLISHED_US = {"decode_T16_D7168_I256_E257_K9": 152.7,
                 "decode_T128_D7168_I256_E257_K9": 239.0,
                 "dense_T512_D7168_I2048_E33_K9": 380.4}
 HBM_FALLBACK_GBS = 6800.0
+BF16_FALLBACK_TFLOPS = 1900.0
+# nominal dense fp4 : bf16 tensor rate of the part (13.5 : 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0
 L2_FLUSH_BYTES = 256 << 20
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_decode_T16_D7168_I256_E257_K9.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_mxfp4_gb300", "csrc", f)
                   for f in ("gemm.cu", "ptx.cuh", "mx.cuh", "moe_internal.h", "api.cu")]
+
+
+def profile_summary(workload: str) -> str:
+    """Committed ncu summary of the GEMM kernel on this workload."""
+    return os.path.join(ROOT, "profiles", f"gemm_{workload}.md")
 
 
 # ---------------------------------------------------------------- helpers
@@ -74,13 +83,15 @@ def aggregate_value(units_per_rank: float, world: int, max_seconds: float) -> fl
 
 
 def measured_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, kind) from MEASURED_PEAKS.json, else the
+    recipe's fallback figures."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", BF16_FALLBACK_TFLOPS)), "measured"
     except Exception:
-        return HBM_FALLBACK_GBS, "fallback"
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -91,11 +102,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(workload: str):
     """DRAM bytes per GEMM-kernel launch from the committed ncu summary, or None when
     the summary is missing or the kernel sources changed since it was taken."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(profile_summary(workload)).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
@@ -152,6 +163,45 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def alg_flops(w, ids):
+    """Algorithmic operations of one call: 6 * (valid routes) * d_model * d_inter
+    (stage 1: 2*2I*D per route, stage 2: 2*D*I per route; padding excluded)."""
+    import numpy as np
+
+    ids = np.asarray(ids).reshape(-1)
+    r_valid = int(((ids >= 0) & (ids < w.E)).sum())
+    return 6.0 * r_valid * w.D * w.I
+
+
+def tensor_peak(moe, stream, dev):
+    """Measured dense MXFP4 rate (TFLOP/s) of the library's tensor-core probe: one
+    CTA per SM issuing back-to-back M=128 N=256 K=64 mxf4 MMAs for ~20 ms, timed
+    with events on the launching stream (best of 3), plus the rate with one
+    scale-factor copy per MMA and at the decode kernels' MMA width N=16."""
+    import torch
+
+    def run(n, iters, copies, variant=0):
+        best = 0.0
+        for _ in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fl = moe.tensor_probe(n, iters, copies, variant, stream.cuda_stream)
+            e1.record(stream)
+            e1.synchronize()
+            best = max(best, fl / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+        return best
+
+    run(256, 2000, 0)  # warm-up
+    out = {"n256": run(256, 200000, 0), "n256_copy1": run(256, 100000, 1),
+           "n128": run(128, 200000, 0), "n16": run(16, 200000, 0), "n16_copy1": run(16, 100000, 1),
+           # copy shape and issuing warp (variant bits: 128x256b copies; a second warp)
+           "n16_copy1_wide": run(16, 100000, 1, 1), "n16_copy1_warp2": run(16, 100000, 1, 2),
+           "n16_copy1_wide_warp2": run(16, 100000, 1, 3), "n256_copy1_warp2": run(256, 100000, 1, 2)}
+    torch.cuda.synchronize(dev)
+    return out
 
 
 def alg_bytes(w, ids, bf16_act=False):
@@ -216,7 +266,9 @@ def run_reference(args, w):
 
 
 def cpu_baseline(w, budget_s: float):
-    """Oracle on the host cores over whole batches of the workload, ~budget_s seconds."""
+    """Oracle on the host cores over a bounded sample of the workload: whole batches
+    while one takes under budget_s, else the batch's first n tokens (routing over
+    the whole batch) with n sized from a probe call to take about budget_s."""
     import numpy as np
 
     import oracle
@@ -224,17 +276,28 @@ def cpu_baseline(w, budget_s: float):
 
     inp = workloads.to_numpy(workloads.make_inputs(w))
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    ntok = w.T
+    nprobe = min(w.T, 16)
     t0 = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.forward(**inp, threads=threads, want_h=False)
-        reps += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
+    oracle.forward(**inp, tokens=np.arange(nprobe, dtype=np.int32), threads=threads, want_h=False)
+    per_tok = (time.perf_counter() - t0) / nprobe
+    if per_tok * w.T <= budget_s:
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.forward(**inp, threads=threads, want_h=False)
+            reps += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return {"value": w.T * reps / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                "sample": f"{reps} full batches of {w.T} tokens ({w.name}), {dt:.1f} s"}
+    ntok = int(max(1, min(w.T, budget_s / per_tok)))
+    t0 = time.perf_counter()
+    oracle.forward(**inp, tokens=np.arange(ntok, dtype=np.int32), threads=threads, want_h=False)
     dt = time.perf_counter() - t0
-    return {"value": ntok * reps / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{reps} full batches of {ntok} tokens ({w.name}), {dt:.1f} s"}
+    return {"value": ntok / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"the first {ntok} of {w.T} tokens of one batch ({w.name}; routing over "
+                      f"the whole batch), {dt:.1f} s"}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -262,10 +325,11 @@ def run_gpu(args, w, world, rank, local):
 
     # launch mode: the library's automatic choice unless forced
     moe.set_single_launch({"auto": 2, "single": 1, "separate": 0}[args.launch])
-    # (the bf16-activation forward: separate kernels; routing in three launches from 4096 routes)
+    # (the bf16-activation forward: separate kernels, a separate top-k sum; routing in
+    # three launches from 4096 routes)
     launches = ((6 if w.T * w.K >= 4096 else 4) if bf16_act
                 else moe.call_launches(w.T, w.D, w.I, w.E, w.K))
-    single = launches == 2
+    single = launches == 1 and not bf16_act
     moe.set_kernel_timing(2)
     for _ in range(args.warmup):
         flush.zero_()
@@ -314,7 +378,7 @@ def run_gpu(args, w, world, rank, local):
         m.forward(*fargs, out=out)
         kt = moe.kernel_times()
         for n in names:
-            per_kernel[n] += kt[n]
+            per_kernel[n] = None if kt[n] is None else per_kernel[n] + kt[n]
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if m.device_status() != 0:
@@ -431,16 +495,33 @@ def run_gpu(args, w, world, rank, local):
     # ---- roofline of the dominant kernel (the GEMM kernel), measured live above
     ids_np = inp["topk_ids"].numpy()
     b_total, b_gemm, e_touched = alg_bytes(w, ids_np, bf16_act)
-    peak, peak_kind = measured_peaks()
-    dom = max(per_kernel, key=per_kernel.get)
+    flops = alg_flops(w, ids_np)
+    peak, bf16_peak, peak_kind = measured_peaks()
+    probe = tensor_peak(moe, stream, dev)
+    mxf4_peak = probe["n256"]
+    ran = {n: v for n, v in per_kernel.items() if v is not None}
+    dom = max(ran, key=ran.get)
     g_ms = per_kernel["gemm"] / k_steps
     achieved = b_gemm / (g_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "gemm", "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak,
-                # the committed ncu summary covers the default workload and configuration
-                "traffic": profiled_traffic() if (w.name == DEFAULT_WORKLOAD and not bf16_act
-                                                  and args.launch == "auto") else None,
-                "alg_bytes_per_launch": b_gemm, "peak_kind": peak_kind}
+    g_tflops = flops / (g_ms * 1e-3) / 1e12
+    t_hbm = b_gemm / (peak * 1e9)
+    t_fp4 = flops / (mxf4_peak * 1e12)
+    roofline = {"bound": "hbm" if t_hbm >= t_fp4 else "tensor", "kernel": "gemm",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                # the committed ncu summary of this workload's GEMM kernel (default launch
+                # mode), null once the kernel sources have changed since it was taken
+                "traffic": profiled_traffic(w.name) if (not bf16_act and args.launch == "auto")
+                else None,
+                "alg_bytes_per_launch": b_gemm, "peak_kind": peak_kind,
+                "flops_alg": flops, "achieved_tflops": g_tflops,
+                "tensor_peak_tflops": mxf4_peak,
+                "tensor_peak_kind": "measured: the library's mxf4 probe (M128 N256 K64 MMAs, one CTA "
+                                    "per SM, operands in shared memory)",
+                "tensor_frac": g_tflops / mxf4_peak,
+                "tensor_peak_from_bf16_tflops": bf16_peak * FP4_OVER_BF16,
+                "tensor_frac_vs_bf16_ratio": g_tflops / (bf16_peak * FP4_OVER_BF16),
+                "t_hbm_us": t_hbm * 1e6, "t_fp4_us": t_fp4 * 1e6,
+                "probe_tflops": probe}
     fwd_gbs = b_total / (us_call * 1e-6) / 1e9
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -460,8 +541,10 @@ def run_gpu(args, w, world, rank, local):
         "us_per_call": us_call,
         "us_per_call_graph_replay": graph_us,
         "us_per_call_l2_not_flushed": warm_us,
-        "per_kernel_us": {n: 1e3 * v / k_steps for n, v in per_kernel.items()},
-        "per_kernel_note": f"{k_steps} steps with events between kernels (serialised)",
+        "per_kernel_us": {n: (None if v is None else 1e3 * v / k_steps) for n, v in per_kernel.items()},
+        "per_kernel_note": f"{k_steps} steps with events between kernels (serialised); null: "
+                           "nothing launched in that slot (top-k sum inside the GEMM kernel; "
+                           "routing and quantisation too in single-launch mode)",
         "dominant_kernel": dom,
         "roofline": roofline,
         "roofline_forward": {"bound": "hbm", "alg_bytes": b_total, "achieved": fwd_gbs,
@@ -479,6 +562,7 @@ def run_gpu(args, w, world, rank, local):
                        "us_per_step": 1e3 * e2e_ms / e2e_steps},
         "gpu_launches": launches * args.steps,
         "clocks": clk,
+        "us_per_call_x_sm_mhz": (us_call * clk["sm_mhz"]) if clk else None,
     }
     if w.name in PUBLISHED_US:
         res["vs_baseline"] = value / (w.T / (PUBLISHED_US[w.name] * 1e-6))

@@ -166,13 +166,16 @@ moe_status_t moe_mxfp4_forward_w4a16(const void* hidden, const void* w13, const 
  *   - Shapes whose workspace (moe_mxfp4_workspace_size) exceeds the array are
  *     rejected with MOE_ERR_WORKSPACE; other errors as for moe_mxfp4_forward.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) for that device; make that first call before any
- *     stream capture.
+ *     (cudaGetSymbolAddress) for that device.  With CUDA's lazy module loading
+ *     that lookup is also when the array's device memory is committed.  A call
+ *     with T = 0 (any supported shape; the pointers are not used) does only this
+ *     set-up and enqueues nothing: make it once per device at start-up, before
+ *     a memory pool takes the free device memory and before any stream capture.
  *   - Every call on a device shares the array and leaves its contents behind;
  *     the parts that must start at zero are cleared by each call.  Calls that
  *     overlap on the GPU (unordered streams) race on the array.
- *   - moe_mxfp4_last_device_status reports on the registered workspace, not on
- *     this array.
+ *   - moe_mxfp4_last_device_status after such a call reads this array's status
+ *     word (bounded-wait timeouts of the call are reported there).
  */
 #define MOE_MXFP4_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
 moe_status_t moe_mxfp4_forward_noalloc(const void* hidden, const void* w13, const void* w13_scale,
@@ -185,10 +188,12 @@ moe_status_t moe_mxfp4_forward_noalloc(const void* hidden, const void* w13, cons
 const char* moe_mxfp4_status_string(moe_status_t status);
 
 /*
- * Synchronise `stream`, then read the device status word of the current
- * device's workspace.  Returns MOE_ERR_DEVICE_TIMEOUT when a kernel of the last
- * forward call gave up on a bounded wait, MOE_OK otherwise.  Meant for tests and
- * checked runs (it synchronises).
+ * Synchronise `stream`, then read the device status word of the workspace the
+ * last forward call on the current device used (the registered workspace, or
+ * the static array of moe_mxfp4_forward_noalloc; before any forward call, the
+ * registered workspace).  Returns MOE_ERR_DEVICE_TIMEOUT when a kernel of that
+ * call gave up on a bounded wait or found a counter in an impossible state,
+ * MOE_OK otherwise.  Meant for tests and checked runs (it synchronises).
  */
 moe_status_t moe_mxfp4_last_device_status(cudaStream_t stream);
 
@@ -206,7 +211,7 @@ moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream
 
 /* Workspace regions, for tests and tools that inspect intermediate results. */
 typedef enum {
-    MOE_WS_STATUS = 0,      /* u32 [1024]: [0] error bits; [15], [16], [512..1024) the single-launch path's ready word, quantisation count and route-tile counters (zero between calls) */
+    MOE_WS_STATUS = 0,      /* u32 [1024]: [0] error bits; [15], [16], [17], [512..1024) the single-launch path's ready word, quantisation count, exit count and route-tile counters (zero between calls) */
     MOE_WS_COUNTERS = 1,    /* u32 [max_tiles]: finished stage-1 feature tiles per route tile (multi-kernel path; zeroed per call) */
     MOE_WS_SORTED_IDS = 2,  /* i32 [cap]: route id t*topk+k per sorted slot, T*topk = padding */
     MOE_WS_SORTED_W = 3,    /* f32 [cap]: topk weight of the slot's route, 0 for padding      */
@@ -219,8 +224,8 @@ typedef enum {
     MOE_WS_A1S = 10,        /* u8 [cap][a1s_stride]: its e8m0 scales                          */
     MOE_WS_A2Q = 11,        /* u8 [cap][d_inter/2]: quantised SwiGLU output of each slot      */
     MOE_WS_A2S = 12,        /* u8 [cap][a2s_stride]: its e8m0 scales                          */
-    MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id    */
-    MOE_WS_PARTIAL = 14,    /* unused (0 bytes): no K split of stage 1                        */
+    MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id (scratch of the top-k sum; summed rows are dropped from L2 and read back as unspecified data) */
+    MOE_WS_TOKENS = 14,     /* i32 [T] valid routes per token (padded to 16 bytes), then u32 [T][d_model/128] the top-k sum's arrival counters per output block */
     MOE_WS_A1B = 15,        /* bf16 [cap][d_model]: hidden row of each slot's token (bf16-activation plan only) */
     MOE_WS_A2B = 16,        /* bf16 [cap][d_inter]: bf16 SwiGLU output of each slot (bf16-activation plan only) */
     MOE_WS_NUM_REGIONS = 17
@@ -264,8 +269,11 @@ int moe_mxfp4_pointer_kind(const void* ptr);
 /* ------------------------------------------------------------------ timing */
 
 /* Number of kernel slots of a forward call (route, quant, the GEMM kernel that
- * runs both grouped GEMMs, top-k sum).  In single-launch mode the route and
- * quant slots are empty: routing and quantisation run inside the GEMM kernel. */
+ * runs both grouped GEMMs, top-k sum).  Where the MXFP4 forward sums in the GEMM
+ * kernel's stage-2 epilogue (moe_mxfp4_set_tuning) its last slot is empty; in
+ * single-launch mode the route and quant slots are empty too (routing and
+ * quantisation run inside the GEMM kernel).  The bf16-activation forward always
+ * launches a separate top-k sum. */
 int moe_mxfp4_num_kernels(void);
 
 /*
@@ -275,8 +283,9 @@ int moe_mxfp4_num_kernels(void);
  * T*topk <= 2048 and E <= 384 route and quantise inside the GEMM kernel: every
  * CTA sorts all routes in shared memory and quantises a share of the hidden
  * states, and the stage-1 route-tile copies wait (bounded) until all CTAs have
- * counted their share; only the GEMM kernel and the top-k sum are launched.
- * Otherwise: routing kernel, quantisation kernel, GEMM kernel, top-k sum.
+ * counted their share; the GEMM kernel is the call's only launch.  Otherwise:
+ * routing kernel, quantisation kernel, GEMM kernel (which also does the top-k
+ * sum in either mode).
  *   mode 0: always separate kernels;
  *   mode 1: single launch wherever the shape allows;
  *   mode 2 (default): single launch for decode-sized calls (T*topk <= 256),
@@ -287,10 +296,10 @@ int moe_mxfp4_num_kernels(void);
 moe_status_t moe_mxfp4_set_single_launch(int mode);
 
 /* Kernels a forward call of this shape launches on the current device under its
- * launch mode: 4 (route, quant, GEMM, top-k sum), 6 when T*topk >= 4096 (routing
- * then runs on many CTAs in three launches: chunk counts, offsets, scatter),
- * 2 (GEMM with routing and quantisation inside, top-k sum), 0 for T = 0, -1 for
- * an invalid shape or no device. */
+ * launch mode: 3 (route, quant, GEMM), 5 when T*topk >= 4096 (routing then runs
+ * on many CTAs in three launches: chunk counts, offsets, scatter), 1 (the GEMM
+ * kernel with routing and quantisation inside); one more where the top-k sum
+ * runs as a separate kernel; 0 for T = 0, -1 for an invalid shape or no device. */
 int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk);
 
 /*
@@ -304,10 +313,46 @@ int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk);
  *   mode 2: events only before the first and after the last kernel.
  * moe_mxfp4_kernel_times (mode 1) waits for the last event and writes each
  * kernel's duration of the most recent call, in ms, to ms[0 .. min(n, num_kernels)-1]
- * and returns the count, or -1.  moe_mxfp4_last_call_ms (modes 1 and 2) returns
+ * (a negative value for a slot in which that call launched nothing) and returns
+ * the count, or -1.  moe_mxfp4_last_call_ms (modes 1 and 2) returns
  * the device time of the most recent call in ms, or a negative value.
  */
 moe_status_t moe_mxfp4_set_kernel_timing(int mode);
+
+/*
+ * Tuning override for measurements (process-wide; results do not change, only
+ * speed).  tile_rows: the GEMM route-tile width (maximum MMA N, routes per
+ * tile): 16, 32, 64 or 128, or 0 for the library's choice by shape (the
+ * per-shape block_m / tile table of flower_moe.py is the pages' counterpart).
+ * s2_order: order of the stage-2 items: 1 route-tile-major, 2 output-block-major
+ * (a fused top-k sum then finds each block's P rows in L2), 0 the library's
+ * choice.  topk_sum: 1 in the GEMM kernel's stage-2 epilogue (the item that
+ * writes a token's last P rows of an output block sums them; no separate
+ * kernel), 2 a separate kernel after it, 0 the library's choice (the separate
+ * kernel, measured faster).  Affects calls made after it
+ * (their plan, moe_mxfp4_get_plan, follows it); the workspace size does not
+ * depend on it.  MOE_ERR_INVALID_ARG for other values.
+ */
+moe_status_t moe_mxfp4_set_tuning(int tile_rows, int s2_order, int topk_sum);
+
+/*
+ * Measurement aid for the roofline's compute term (no counterpart in the pages):
+ * enqueue on `stream` one kernel with one CTA per SM, each issuing `iters`
+ * block-scaled MXFP4 MMAs (tcgen05.mma .kind::mxf4 .scale_vec::2X, M = 128,
+ * N = n, K = 64, operands in shared memory, zero values) into one tensor-memory
+ * accumulator, and copies_per_mma scale-factor copies to tensor memory per MMA
+ * (the GEMM kernel's per-stage mix).  variant bit 0: the copies are
+ * tcgen05.cp .128x256b (else .32x128b.warpx4, the GEMM kernel's); bit 1: a second
+ * warp issues the copies (else the MMA thread, before each MMA); bits 2-3: the
+ * MMAs rotate over 2^bits independent accumulators (n * 2^bits <= 256).  *flops
+ * receives the dense operation count (2*128*n*64 per MMA); time the kernel with
+ * events on `stream`.  n: 16..256, multiple of 16; iters: 1..1e7;
+ * copies_per_mma: 0..8; variant: 0..15.  Needs a registered workspace (its
+ * status word records a timed-out final wait; moe_mxfp4_last_device_status
+ * reads it).  Overwrites nothing else.
+ */
+moe_status_t moe_mxfp4_tensor_probe(int n, int iters, int copies_per_mma, int variant,
+                                    double* flops, cudaStream_t stream);
 int moe_mxfp4_kernel_times(float* ms, int n);
 float moe_mxfp4_last_call_ms(void);
 

@@ -29,7 +29,7 @@ STATUS = {
 MOE_OK = 0
 
 REGIONS = ["status", "counters", "sorted_ids", "sorted_w", "block_expert", "seg_start",
-           "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "partial",
+           "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "tokens",
            "a1b", "a2b"]
 
 # Exported C symbols (kept in step with include/moe_mxfp4.h).
@@ -54,11 +54,15 @@ EXPORTS = [
     "moe_mxfp4_workspace_size_w4a16",
     "moe_mxfp4_get_plan_w4a16",
     "moe_mxfp4_pointer_kind",
+    "moe_mxfp4_set_tuning",
+    "moe_mxfp4_tensor_probe",
 ]
 
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
 STATIC_WORKSPACE_BYTES = 64 << 20
 
+# kernel slots of a forward call; the MXFP4 forward sums over the top k inside
+# the GEMM kernel (its topk_sum slot is empty), the bf16-activation one separately
 KERNEL_NAMES = ["route", "quant", "gemm", "topk_sum"]
 
 
@@ -131,6 +135,10 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_set_kernel_timing.argtypes = [i]
     lib.moe_mxfp4_set_single_launch.restype = i
     lib.moe_mxfp4_set_single_launch.argtypes = [i]
+    lib.moe_mxfp4_set_tuning.restype = i
+    lib.moe_mxfp4_set_tuning.argtypes = [i, i, i]
+    lib.moe_mxfp4_tensor_probe.restype = i
+    lib.moe_mxfp4_tensor_probe.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_double), P]
     lib.moe_mxfp4_call_launches.restype = i
     lib.moe_mxfp4_call_launches.argtypes = [i, i, i, i, i]
     lib.moe_mxfp4_kernel_times.restype = i
@@ -232,6 +240,25 @@ def set_single_launch(mode):
     _check(load_library().moe_mxfp4_set_single_launch(int(mode)), "moe_mxfp4_set_single_launch")
 
 
+def set_tuning(tile_rows=0, s2_order=0, topk_sum=0):
+    """Tuning override: route-tile width (16/32/64/128, 0 automatic), stage-2 item
+    order (1 route-tile-major, 2 output-block-major, 0 automatic) and where the
+    top-k sum runs (1 GEMM epilogue, 2 separate kernel, 0 automatic)."""
+    _check(load_library().moe_mxfp4_set_tuning(int(tile_rows), int(s2_order), int(topk_sum)),
+           "moe_mxfp4_set_tuning")
+
+
+def tensor_probe(n, iters, copies_per_mma=0, variant=0, stream: int = 0) -> float:
+    """Enqueue the MXFP4 tensor-core throughput probe (needs a registered
+    workspace); returns the operation count of the enqueued kernel."""
+    fl = ctypes.c_double(0.0)
+    _check(load_library().moe_mxfp4_tensor_probe(int(n), int(iters), int(copies_per_mma),
+                                                  int(variant), ctypes.byref(fl),
+                                                  ctypes.c_void_p(stream)),
+           "moe_mxfp4_tensor_probe")
+    return float(fl.value)
+
+
 def call_launches(T, d_model, d_inter, E, topk) -> int:
     """Kernels one forward call of this shape launches under the current launch mode."""
     return int(load_library().moe_mxfp4_call_launches(T, d_model, d_inter, E, topk))
@@ -251,14 +278,15 @@ def last_call_ms() -> float:
 
 
 def kernel_times():
-    """Per-kernel durations (ms) of the last forward call on this device, by name."""
+    """Per-kernel durations (ms) of the last forward call on this device, by name
+    (None for a slot in which the call launched nothing)."""
     lib = load_library()
     n = lib.moe_mxfp4_num_kernels()
     buf = (ctypes.c_float * n)()
     got = lib.moe_mxfp4_kernel_times(buf, n)
     if got < 0:
         raise MoeError(5, "moe_mxfp4_kernel_times")
-    return {KERNEL_NAMES[i]: float(buf[i]) for i in range(got)}
+    return {KERNEL_NAMES[i]: (float(buf[i]) if buf[i] >= 0 else None) for i in range(got)}
 
 
 def version() -> str:

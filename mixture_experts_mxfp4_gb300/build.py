@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmoe_mxfp4.so")
-SOURCES = ["api.cu", "route_quant_reduce.cu", "gemm.cu", "gemm_w4a16.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "route_quant_reduce.cu", "gemm.cu", "gemm_w4a16.cu", "noalloc.cu", "probe.cu"]
 HEADERS = ["moe_internal.h", "ptx.cuh", "mx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

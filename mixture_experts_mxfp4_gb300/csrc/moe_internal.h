@@ -26,12 +26,15 @@ struct WsPtrs {
     uint8_t* a1s;          // [cap][a1s_stride]
     uint8_t* a2q;          // [cap][I/2]
     uint8_t* a2s;          // [cap][a2s_stride]
-    float* P;              // [R][D]
+    float* P;              // [R][D]: w[route] * stage-2 output row of each route
     uint32_t* tile_done;   // stage-1 feature tiles completed per route tile (counters, or the
                            // status region's block on the single-launch path)
     uint32_t* quant_done;  // CTAs whose share of the hidden states is quantised (single launch)
     uint16_t* a1b;         // bf16-activation path: [cap][D] hidden rows in sorted order
     uint16_t* a2b;         // bf16-activation path: [cap][I] bf16 SwiGLU output in sorted order
+    int32_t* tok_nvalid;   // [T]: routes of each token with an expert id in [0, E)
+    uint32_t* tok_cnt;     // [T][n_fb]: stage-2 items that have written a token's P rows of
+                           // one output block (the fused top-k sum's arrival counters)
 };
 
 // Geometry of one grouped block-scaled GEMM stage (stage 1: gate_up, K = D;
@@ -79,6 +82,12 @@ struct GemmParams {
     const float* topk_w;
     const void* hidden;
     int T, cap;
+    // Fused top-k sum: the stage-2 epilogue counts each route's output block and
+    // the item that completes a token's count sums its P rows into out.
+    void* out;        // bf16 [T][Dl]
+    int n_fb;         // output blocks (stage-2 feature tiles) per token = g[1].n_ftiles
+    int s2_fmajor;    // stage-2 items in output-block-major order (P stays in L2)
+    int fused_sum;    // 1: the top-k sum runs in the stage-2 epilogue; 0: a separate kernel
 };
 
 // Parameters of the bf16-activation (W4A16) GEMM launch: packed e2m1 weights
@@ -107,12 +116,13 @@ constexpr uint32_t kW4DeqBytes = 128 * 256; // 128 rows x 128 bf16
 constexpr int kW4MaxDeq = 3;
 
 // Status region (u32 words): [0] error bits, [1..14] spare, [15] ready word of
-// the single-launch path, [16] its quantisation count, [512, 1024) its route-tile
-// counters.  Words 15.. are zero between calls: the workspace registration
-// zeroes the region and the single-launch path's top-k sum kernel clears them
-// after each call.
+// the single-launch path, [16] its quantisation count, [17] its count of exited
+// CTAs, [512, 1024) its route-tile counters.  Words 15.. are zero between calls:
+// the region is zero when the workspace is first used and the last CTA of every
+// single-launch GEMM kernel clears them before it exits.
 constexpr int kStatusWords = 1024;
 constexpr int kFrontQuantWord = 16;
+constexpr int kFrontExitWord = 17;
 constexpr int kFrontTileWord = 512;
 
 constexpr int kBlockM = 16;          // slots per padded block
@@ -128,6 +138,9 @@ constexpr int kFrontMaxExperts = 384;  // single-launch path: one expert per GEM
 constexpr int kFrontAutoRoutes = 256;  // automatic mode: single launch up to this many routes
 constexpr int kRouteMultiMin = 4096;  // routes from which routing runs in three launches on many CTAs
 constexpr int kTileCache = 512;      // route tiles kept in shared memory (the rest read from L2)
+// Byte offset, within the GEMM kernel's 512-byte barrier block, of the
+// producer's bitmap of route tiles known to be complete (kTileCache bits).
+constexpr int kReadyBitsOff = 384;
 
 // Host-side pieces of the forward call shared by its entry points (api.cu).
 moe_status_t validate_forward(const void* hidden, const void* w13, const void* w13_scale,
@@ -147,12 +160,13 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream);
 // hidden rows hold Dl elements; quantised rows D (zero blocks past Dl)
+// Also per token: the valid-route count, the zeroed arrival counters of its n_fb
+// output blocks, and a zero out row when no route of the token is valid.
 cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride,
-                         const WsPtrs& ws, cudaStream_t stream);
-// clear_ready: also clear the single-launch words of the status region (after that GEMM)
-// P rows hold D columns; out rows Dl
+                         int n_fb, void* out, const WsPtrs& ws, cudaStream_t stream);
+// Separate top-k sum (bf16-activation path): P rows hold D columns; out rows Dl.
 cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, int Dl, void* out,
-                          const WsPtrs& ws, bool clear_ready, cudaStream_t stream);
+                          const WsPtrs& ws, cudaStream_t stream);
 // bf16-activation path: copy each token's hidden row to the sorted slot of
 // every valid route (after the routing kernel)
 cudaError_t launch_gather_bf16(const void* hidden, int T, int K, int D, const WsPtrs& ws,
@@ -163,5 +177,10 @@ cudaError_t launch_w4a16_gemm(const CUtensorMap* maps, const W4Params& p, int gr
 // maps: stage-1 A, SA, B, SB, then stage-2 A, SA, B, SB
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream);
+// Tensor-core throughput probe (probe.cu): grid CTAs, each issuing `iters`
+// M = 128, N = n, K = 64 mxf4 MMAs and copies_per_mma scale-factor copies per MMA
+// (variant bit 0: 128x256b copies; bit 1: copies from a second warp).
+cudaError_t launch_mxf4_probe(int n, int iters, int copies_per_mma, int variant, int grid,
+                              uint32_t* status, cudaStream_t stream);
 
 }  // namespace moe

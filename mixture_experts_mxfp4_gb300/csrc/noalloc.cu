@@ -13,12 +13,20 @@
 // are rejected with MOE_ERR_WORKSPACE.
 //
 // The array is shared by every call on a device and keeps the previous call's
-// contents.  The parts that must start at zero are zero when the library is
-// loaded (a __device__ array is zero-initialised) and are kept so: the routing
-// kernel clears the route-tile counters and status words at the start of a
-// multi-kernel call, and a single-launch call's top-k sum kernel clears the
-// words its GEMM used.  Calls that overlap on the GPU (different streams
-// without ordering) race on the array.
+// contents.  The parts that must start at zero are zero when the library's
+// module is loaded (a __device__ array is zero-initialised) and are kept so: the
+// routing kernel clears the route-tile counters and status words at the start
+// of a multi-kernel call, the quantisation step clears the per-token counters
+// of the top-k sum, and the last CTA of a single-launch GEMM kernel clears the
+// words that kernel shares across CTAs.  Calls that overlap on the GPU
+// (different streams without ordering) race on the array.
+//
+// The array's device memory is committed when the module that holds it is
+// loaded, which with CUDA's lazy module loading is the first address lookup.
+// The entry point does that lookup on its first call on a device; a call with
+// T = 0 does only that (it enqueues nothing), so a caller makes it at start-up,
+// before its own pool takes the free device memory and before any stream
+// capture.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -57,13 +65,14 @@ extern "C" moe_status_t moe_mxfp4_forward_noalloc(const void* hidden, const void
                                                   cudaStream_t stream) {
     const moe_status_t st = moe::validate_forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
                                                   topk_weights, out, T, d_model, d_inter, E, topk);
-    if (st != MOE_OK || T == 0) return st;
+    if (st != MOE_OK) return st;
     if (moe::plan_workspace_bytes(T, d_model, d_inter, E, topk) > kStaticWorkspaceBytes)
         return MOE_ERR_WORKSPACE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MOE_ERR_CUDA;
-    void* base = static_workspace(dev);
+    void* base = static_workspace(dev);  // (the set-up; all a T = 0 call does)
     if (!base) return MOE_ERR_CUDA;
+    if (T == 0) return MOE_OK;
     return moe::forward_on_workspace(hidden, w13, w13_scale, w2, w2_scale, topk_ids, topk_weights,
                                      out, T, d_model, d_inter, E, topk, d_model, d_inter, base,
                                      dev, stream);

@@ -194,6 +194,13 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Drop the 128-byte L2 line at p (128-byte aligned) without writing it back:
+// for scratch whose contents are dead (read for the last time), so that its
+// dirty lines never cost a DRAM write.  The memory then holds unspecified data.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Named barrier over nthreads threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
     uint32_t r;
@@ -394,6 +401,12 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
 __device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
+}
+
+// Copy a 128-row x 32-byte block from shared memory into TMEM lanes 0..127,
+// 8 columns (row r -> lane r).
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Load 16 consecutive fp32 columns of this warp's 32 TMEM lanes.

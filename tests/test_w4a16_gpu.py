@@ -125,14 +125,14 @@ def test_w4a16_decode_t16(moe):
     run_w4a16(moe, w, workloads.make_inputs(w))
 
 
-def test_w4a16_decode_t128_sampled(moe):
+def test_w4a16_decode_t128_full(moe):
     w = workloads.WORKLOADS["decode_T128_D7168_I256_E257_K9"]
-    run_w4a16(moe, w, workloads.make_inputs(w), tokens=[0, 1, 63, 64, 100, 127])
+    run_w4a16(moe, w, workloads.make_inputs(w))
 
 
-def test_w4a16_dense_shard_sampled(moe):
+def test_w4a16_dense_shard_full(moe):
     w = workloads.WORKLOADS["dense_T512_D7168_I2048_E33_K9"]
-    run_w4a16(moe, w, workloads.make_inputs(w), tokens=[0, 1, 255, 256, 511])
+    run_w4a16(moe, w, workloads.make_inputs(w))
 
 
 def test_w4a16_single_token(moe):
