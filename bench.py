@@ -199,7 +199,7 @@ def tensor_peak(moe, stream, dev):
            "n128": run(128, 200000, 0), "n16": run(16, 200000, 0), "n16_copy1": run(16, 100000, 1),
            # copy shape and issuing warp (variant bits: 128x256b copies; a second warp)
            "n16_copy1_wide": run(16, 100000, 1, 1), "n16_copy1_warp2": run(16, 100000, 1, 2),
-           "n16_copy1_wide_warp2": run(16, 100000, 1, 3), "n256_copy1_warp2": run(256, 100000, 1, 2)}
+           "n256_copy1_warp2": run(256, 100000, 1, 2)}
     torch.cuda.synchronize(dev)
     return out
 

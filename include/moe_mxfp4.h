@@ -224,8 +224,8 @@ typedef enum {
     MOE_WS_A1S = 10,        /* u8 [cap][a1s_stride]: its e8m0 scales                          */
     MOE_WS_A2Q = 11,        /* u8 [cap][d_inter/2]: quantised SwiGLU output of each slot      */
     MOE_WS_A2S = 12,        /* u8 [cap][a2s_stride]: its e8m0 scales                          */
-    MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id (scratch of the top-k sum; summed rows are dropped from L2 and read back as unspecified data) */
-    MOE_WS_TOKENS = 14,     /* i32 [T] valid routes per token (padded to 16 bytes), then u32 [T][d_model/128] the top-k sum's arrival counters per output block */
+    MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id    */
+    MOE_WS_PARTIAL = 14,    /* unused (0 bytes): no K split of stage 1                        */
     MOE_WS_A1B = 15,        /* bf16 [cap][d_model]: hidden row of each slot's token (bf16-activation plan only) */
     MOE_WS_A2B = 16,        /* bf16 [cap][d_inter]: bf16 SwiGLU output of each slot (bf16-activation plan only) */
     MOE_WS_NUM_REGIONS = 17
@@ -269,11 +269,8 @@ int moe_mxfp4_pointer_kind(const void* ptr);
 /* ------------------------------------------------------------------ timing */
 
 /* Number of kernel slots of a forward call (route, quant, the GEMM kernel that
- * runs both grouped GEMMs, top-k sum).  Where the MXFP4 forward sums in the GEMM
- * kernel's stage-2 epilogue (moe_mxfp4_set_tuning) its last slot is empty; in
- * single-launch mode the route and quant slots are empty too (routing and
- * quantisation run inside the GEMM kernel).  The bf16-activation forward always
- * launches a separate top-k sum. */
+ * runs both grouped GEMMs, top-k sum).  In single-launch mode the route and
+ * quant slots are empty: routing and quantisation run inside the GEMM kernel. */
 int moe_mxfp4_num_kernels(void);
 
 /*
@@ -283,9 +280,8 @@ int moe_mxfp4_num_kernels(void);
  * T*topk <= 2048 and E <= 384 route and quantise inside the GEMM kernel: every
  * CTA sorts all routes in shared memory and quantises a share of the hidden
  * states, and the stage-1 route-tile copies wait (bounded) until all CTAs have
- * counted their share; the GEMM kernel is the call's only launch.  Otherwise:
- * routing kernel, quantisation kernel, GEMM kernel (which also does the top-k
- * sum in either mode).
+ * counted their share; only the GEMM kernel and the top-k sum are launched.
+ * Otherwise: routing kernel, quantisation kernel, GEMM kernel, top-k sum.
  *   mode 0: always separate kernels;
  *   mode 1: single launch wherever the shape allows;
  *   mode 2 (default): single launch for decode-sized calls (T*topk <= 256),
@@ -296,10 +292,10 @@ int moe_mxfp4_num_kernels(void);
 moe_status_t moe_mxfp4_set_single_launch(int mode);
 
 /* Kernels a forward call of this shape launches on the current device under its
- * launch mode: 3 (route, quant, GEMM), 5 when T*topk >= 4096 (routing then runs
- * on many CTAs in three launches: chunk counts, offsets, scatter), 1 (the GEMM
- * kernel with routing and quantisation inside); one more where the top-k sum
- * runs as a separate kernel; 0 for T = 0, -1 for an invalid shape or no device. */
+ * launch mode: 4 (route, quant, GEMM, top-k sum), 6 when T*topk >= 4096 (routing
+ * then runs on many CTAs in three launches: chunk counts, offsets, scatter),
+ * 2 (GEMM with routing and quantisation inside, top-k sum), 0 for T = 0, -1 for
+ * an invalid shape or no device. */
 int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk);
 
 /*
@@ -321,19 +317,13 @@ moe_status_t moe_mxfp4_set_kernel_timing(int mode);
 
 /*
  * Tuning override for measurements (process-wide; results do not change, only
- * speed).  tile_rows: the GEMM route-tile width (maximum MMA N, routes per
+ * speed): tile_rows is the GEMM route-tile width (maximum MMA N, routes per
  * tile): 16, 32, 64 or 128, or 0 for the library's choice by shape (the
- * per-shape block_m / tile table of flower_moe.py is the pages' counterpart).
- * s2_order: order of the stage-2 items: 1 route-tile-major, 2 output-block-major
- * (a fused top-k sum then finds each block's P rows in L2), 0 the library's
- * choice.  topk_sum: 1 in the GEMM kernel's stage-2 epilogue (the item that
- * writes a token's last P rows of an output block sums them; no separate
- * kernel), 2 a separate kernel after it, 0 the library's choice (the separate
- * kernel, measured faster).  Affects calls made after it
- * (their plan, moe_mxfp4_get_plan, follows it); the workspace size does not
- * depend on it.  MOE_ERR_INVALID_ARG for other values.
+ * per-shape block_m table of flower_moe.py is the pages' counterpart).  Affects
+ * calls made after it (their plan, moe_mxfp4_get_plan, follows it); the
+ * workspace size does not depend on it.  MOE_ERR_INVALID_ARG for other values.
  */
-moe_status_t moe_mxfp4_set_tuning(int tile_rows, int s2_order, int topk_sum);
+moe_status_t moe_mxfp4_set_tuning(int tile_rows);
 
 /*
  * Measurement aid for the roofline's compute term (no counterpart in the pages):

@@ -29,7 +29,7 @@ STATUS = {
 MOE_OK = 0
 
 REGIONS = ["status", "counters", "sorted_ids", "sorted_w", "block_expert", "seg_start",
-           "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "tokens",
+           "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "partial",
            "a1b", "a2b"]
 
 # Exported C symbols (kept in step with include/moe_mxfp4.h).
@@ -61,8 +61,6 @@ EXPORTS = [
 # Size of the library's static scratch array used by moe_mxfp4_forward_noalloc.
 STATIC_WORKSPACE_BYTES = 64 << 20
 
-# kernel slots of a forward call; the MXFP4 forward sums over the top k inside
-# the GEMM kernel (its topk_sum slot is empty), the bf16-activation one separately
 KERNEL_NAMES = ["route", "quant", "gemm", "topk_sum"]
 
 
@@ -136,7 +134,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_set_single_launch.restype = i
     lib.moe_mxfp4_set_single_launch.argtypes = [i]
     lib.moe_mxfp4_set_tuning.restype = i
-    lib.moe_mxfp4_set_tuning.argtypes = [i, i, i]
+    lib.moe_mxfp4_set_tuning.argtypes = [i]
     lib.moe_mxfp4_tensor_probe.restype = i
     lib.moe_mxfp4_tensor_probe.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_double), P]
     lib.moe_mxfp4_call_launches.restype = i
@@ -240,12 +238,9 @@ def set_single_launch(mode):
     _check(load_library().moe_mxfp4_set_single_launch(int(mode)), "moe_mxfp4_set_single_launch")
 
 
-def set_tuning(tile_rows=0, s2_order=0, topk_sum=0):
-    """Tuning override: route-tile width (16/32/64/128, 0 automatic), stage-2 item
-    order (1 route-tile-major, 2 output-block-major, 0 automatic) and where the
-    top-k sum runs (1 GEMM epilogue, 2 separate kernel, 0 automatic)."""
-    _check(load_library().moe_mxfp4_set_tuning(int(tile_rows), int(s2_order), int(topk_sum)),
-           "moe_mxfp4_set_tuning")
+def set_tuning(tile_rows=0):
+    """Tuning override: route-tile width (16/32/64/128; 0 the library's choice)."""
+    _check(load_library().moe_mxfp4_set_tuning(int(tile_rows)), "moe_mxfp4_set_tuning")
 
 
 def tensor_probe(n, iters, copies_per_mma=0, variant=0, stream: int = 0) -> float:

@@ -59,17 +59,9 @@ moe_status_t validate_shape(int T, int D, int I, int E, int K) {
     return MOE_OK;
 }
 
-// Tuning override (moe_mxfp4_set_tuning): forced route-tile width and stage-2
-// item order; 0 = the library's choice.  Process-wide.
+// Tuning override (moe_mxfp4_set_tuning): forced route-tile width; 0 = the
+// library's choice.  Process-wide.
 std::atomic<int> g_force_tile_rows{0};
-std::atomic<int> g_force_s2_order{0};
-std::atomic<int> g_force_sum_mode{0};
-
-// Largest P (T * topk * d_model * 4 bytes) for which output-block-major stage-2
-// items are the default under a fused top-k sum.  (By default the top-k sum is a
-// separate kernel: the fused sum measured slower on every workload, decode
-// T=16 103.5 vs 87.2 us, prefill T=4096 1151 vs 858 us.)
-constexpr long long kFusedSumMaxP = 64LL << 20;
 
 // Maximum routes per GEMM tile: small tiles when experts see few routes
 // (decode), full 128-row tiles when they see many (prefill, dense shards).
@@ -115,9 +107,7 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, bool bf1
     b[MOE_WS_A2Q] = (size_t)cap * (I / 2);
     b[MOE_WS_A2S] = (size_t)cap * pl->a2s_stride;
     b[MOE_WS_P] = (size_t)R * D * 4;
-    // per token: valid-route count (i32, padded to 16 bytes), then the arrival
-    // counters of its output blocks (u32 [T][D/128]: enough for any block width)
-    b[MOE_WS_TOKENS] = round_up((size_t)T * 4, 16) + (size_t)T * (D / 128) * 4;
+    b[MOE_WS_PARTIAL] = 0;  // (no K split)
     b[MOE_WS_A1B] = 0;
     b[MOE_WS_A2B] = 0;
     if (bf16_act) {
@@ -135,7 +125,7 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, bool bf1
     pl->workspace_bytes = off;
 }
 
-WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl, int T) {
+WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl) {
     uint8_t* b = static_cast<uint8_t*>(base);
     WsPtrs w;
     w.status = reinterpret_cast<uint32_t*>(b + pl.offset[MOE_WS_STATUS]);
@@ -156,9 +146,6 @@ WsPtrs ws_ptrs(void* base, const moe_mxfp4_plan_t& pl, int T) {
     w.quant_done = w.status + kFrontQuantWord;
     w.a1b = reinterpret_cast<uint16_t*>(b + pl.offset[MOE_WS_A1B]);
     w.a2b = reinterpret_cast<uint16_t*>(b + pl.offset[MOE_WS_A2B]);
-    uint8_t* tok = b + pl.offset[MOE_WS_TOKENS];
-    w.tok_nvalid = reinterpret_cast<int32_t*>(tok);
-    w.tok_cnt = reinterpret_cast<uint32_t*>(tok + round_up((size_t)T * 4, 16));
     return w;
 }
 
@@ -470,7 +457,7 @@ struct LaunchState {
     moe::GemmParams gp;
     moe_mxfp4_plan_t pl;
     const void* key_ptr[5];
-    int key_shape[8];  // T, D, I, E, K, forced tile width, stage-2 order, top-k sum mode
+    int key_shape[6];  // T, D, I, E, K, forced tile width
     bool valid;
 };
 
@@ -488,15 +475,6 @@ void shape_geometry(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, Gem
     // stage 2 on narrow tiles: two 128-row blocks of w2 per item share the route tile
     const int mb2 = (pl->tile_rows <= 64 && D % 256 == 0) ? 2 : 1;
     gemm_geometry(*gp, D, I, pl->tile_rows, mb2);
-    gp->n_fb = gp->g[1].n_ftiles;
-    // Stage-2 items output-block-major where the P rows of the whole call would not
-    // stay in L2 (the fused top-k sum then finds each block's rows there); route-
-    // tile-major otherwise (stage 2 can start on the first finished route tiles).
-    const long long pbytes = (long long)T * K * D * 4;
-    const int sum_mode = g_force_sum_mode.load(std::memory_order_relaxed);
-    gp->fused_sum = sum_mode == 1 ? 1 : 0;
-    const int order = g_force_s2_order.load(std::memory_order_relaxed);
-    gp->s2_fmajor = order ? (order == 2 ? 1 : 0) : ((gp->fused_sum && pbytes > kFusedSumMaxP) ? 1 : 0);
 }
 
 // Whether a call of this shape routes and quantises inside the GEMM kernel under
@@ -520,7 +498,7 @@ bool build_state(LaunchState& st, const void* w13, const void* w13_scale, const 
     moe_mxfp4_plan_t& pl = st.pl;
     GemmParams& gp = st.gp;
     shape_geometry(T, D, I, E, K, &pl, &gp);
-    const WsPtrs ws = ws_ptrs(base, pl, T);
+    const WsPtrs ws = ws_ptrs(base, pl);
     gp.ws = ws;
     const StageGeom& q1 = gp.g[0];
     const StageGeom& q2 = gp.g[1];
@@ -550,8 +528,7 @@ bool launch_state(int dev, const void* w13, const void* w13_scale, const void* w
                   const void* w2_scale, int T, int D, int I, int E, int K, void* base,
                   LaunchState* out) {
     const void* kp[5] = {w13, w13_scale, w2, w2_scale, base};
-    const int ks[8] = {T, D, I, E, K, g_force_tile_rows.load(), g_force_s2_order.load(),
-                       g_force_sum_mode.load()};
+    const int ks[6] = {T, D, I, E, K, g_force_tile_rows.load()};
     std::lock_guard<std::mutex> lk(g_mu);
     for (int w = 0; w < kCacheWays; ++w) {
         const LaunchState& c = g_cache[dev][w];
@@ -596,9 +573,8 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     auto mark = [&](int i) {
         if (timed && (tm.mode == 1 || i == 0 || i == kNumKernels)) cudaEventRecord(tm.ev[i], stream);
     };
-    // Single launch: routing and quantisation run inside the GEMM kernel, which is
-    // then the call's only kernel; otherwise route -> quant -> GEMM.  The top-k sum
-    // runs in the GEMM kernel's stage-2 epilogue either way.
+    // Single launch: routing and quantisation run inside the GEMM kernel (one
+    // launch before the top-k sum); otherwise route -> quant -> GEMM.
     const bool front = single_launch_for(dev, T, E, K, gp);
     GemmParams g = gp;
     g.fused_front = front ? 1 : 0;
@@ -609,7 +585,6 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     g.cap = pl.cap;
     g.Dl = Dl;
     g.Il = Il;
-    g.out = out;
     if (front) g.ws.tile_done = ws.status + kFrontTileWord;  // zero between calls
     {
         std::lock_guard<std::mutex> lk(g_mu);
@@ -623,18 +598,17 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     }
     mark(1);
     if (!front) {
-        if (launch_quant(hidden, T, K, D, Dl, pl.a1s_stride, g.n_fb, out, ws, stream) != cudaSuccess)
+        if (launch_quant(hidden, T, K, D, Dl, pl.a1s_stride, ws, stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     mark(2);
     if (launch_gemm(st->maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);
-    if (!g.fused_sum && launch_reduce(topk_ids, T, K, E, D, Dl, out, ws, stream) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (launch_reduce(T, K, D, Dl, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(4);
     if (timed) {
         tm.recorded = true;
-        tm.launched = (front ? 0x4u : 0x7u) | (g.fused_sum ? 0u : 0x8u);
+        tm.launched = front ? 0xcu : 0xfu;
     }
     return MOE_OK;
 }
@@ -687,7 +661,7 @@ moe_status_t forward_w4a16_on_workspace(const void* hidden, const void* w13, con
     fill_plan(T, D, I, E, K, &pl, true);
     W4Params g;
     memset(&g, 0, sizeof(g));
-    g.ws = ws_ptrs(base, pl, T);
+    g.ws = ws_ptrs(base, pl);
     g.w13_scale = static_cast<const uint8_t*>(w13_scale);
     g.w2_scale = static_cast<const uint8_t*>(w2_scale);
     g.D = D; g.I = I; g.E = E; g.K = K; g.R = T * K;
@@ -726,8 +700,7 @@ moe_status_t forward_w4a16_on_workspace(const void* hidden, const void* w13, con
     mark(2);
     if (launch_w4a16_gemm(maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(3);
-    if (launch_reduce(topk_ids, T, K, E, D, D, out, g.ws, stream) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    if (launch_reduce(T, K, D, D, out, g.ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
     mark(4);
     if (timed) {
         tm.recorded = true;
@@ -804,9 +777,8 @@ int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk) {
     moe_mxfp4_plan_t pl;
     moe::GemmParams gp;
     shape_geometry(T, d_model, d_inter, E, topk, &pl, &gp);
-    const int sum = gp.fused_sum ? 0 : 1;  // a separate top-k sum kernel
-    if (single_launch_for(dev, T, E, topk, gp)) return 1 + sum;
-    return ((long long)T * topk >= kRouteMultiMin ? 5 : 3) + sum;  // routing in three launches
+    if (single_launch_for(dev, T, E, topk, gp)) return 2;
+    return (long long)T * topk >= kRouteMultiMin ? 6 : 4;  // routing in three launches
 }
 
 moe_status_t moe_mxfp4_get_plan_w4a16(int T, int d_model, int d_inter, int E, int topk,
@@ -880,13 +852,10 @@ moe_status_t moe_mxfp4_tensor_probe(int n, int iters, int copies_per_mma, int va
     return MOE_OK;
 }
 
-moe_status_t moe_mxfp4_set_tuning(int tile_rows, int s2_order, int topk_sum) {
+moe_status_t moe_mxfp4_set_tuning(int tile_rows) {
     if (!(tile_rows == 0 || tile_rows == 16 || tile_rows == 32 || tile_rows == 64 || tile_rows == 128))
         return MOE_ERR_INVALID_ARG;
-    if (s2_order < 0 || s2_order > 2 || topk_sum < 0 || topk_sum > 2) return MOE_ERR_INVALID_ARG;
     g_force_tile_rows.store(tile_rows);
-    g_force_s2_order.store(s2_order);
-    g_force_sum_mode.store(topk_sum);
     return MOE_OK;
 }
 

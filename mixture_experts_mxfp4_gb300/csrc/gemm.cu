@@ -17,10 +17,7 @@
 //
 // Stage 2 (solution.py, kernel_stage2: down projection, weight applied to the
 // output; flower_moe.py passes sorted_weights to stage 2): A = 128 rows of w2,
-// the epilogue writes w[route] * y into P[route, :] and then does the per-token
-// top-k sum for the tokens whose last route it wrote (epilogue_topk_sum: ordered
-// fp32 sum over k, one bf16 rounding, no waiting; b12x moe/fused/w4a16/kernel.py
-// sums in its FC2 epilogue with atomics instead, which is not deterministic).
+// the epilogue writes w[route] * y into P[route, :] (fp32) for the per-token sum.
 //
 // One launch runs both stages: every CTA takes its stage-1 items, then its
 // stage-2 items, through the same shared-memory ring, so stage-2 weight tiles
@@ -65,23 +62,14 @@ struct Item {
     int e, row0, nrows, f, ks0, ks1, tile;
 };
 
-// Item `it` of a stage: route tile it / n_ftiles, then feature tile (tile-major),
-// or, with fmajor, feature tile it / ntiles, then route tile (every route tile
-// of one output block before the next block: the stage-2 epilogue's P rows of a
-// block are then written, summed and dropped while they are still in L2).  An
-// item runs over the whole K extent.  The first kTileCache route tiles come
-// from the shared-memory copy.
+// Item `it` of a stage: route tile it / n_ftiles, then feature tile; it runs
+// over the whole K extent.  The first kTileCache route tiles come from the
+// shared-memory copy.
 __device__ __forceinline__ Item decode_item(const StageGeom& q, const int4* gtiles, int it,
-                                            const int4* tcache, bool fmajor, int ntiles) {
+                                            const int4* tcache) {
     Item x;
-    int tile;
-    if (fmajor) {
-        x.f = it / ntiles;
-        tile = it - x.f * ntiles;
-    } else {
-        tile = it / q.n_ftiles;
-        x.f = it - tile * q.n_ftiles;
-    }
+    const int tile = it / q.n_ftiles;
+    x.f = it - tile * q.n_ftiles;
     const int4 t = tile < kTileCache ? tcache[tile] : __ldcg(gtiles + tile);
     x.e = t.x;
     x.row0 = t.y;
@@ -340,10 +328,8 @@ __device__ __forceinline__ bool poll_word(const uint32_t* word, uint32_t want, b
 // 32 elements, spread over the CTAs; first16: the thread's first load) and
 // write each block to the sorted slot of every valid route of its token; then
 // count the CTA in quant_done (zero at the start of the call: the last CTA of
-// the previous single-launch call cleared it, or it was never used).  Also
-// prepares the fused top-k sum per token, as the quant kernel does on the
-// multi-kernel path: valid-route count, zeroed arrival counters, and a zero
-// output row for a token without a valid route.  Warps 4..11 (named barrier 3).
+// the previous single-launch call cleared it, or it was never used).
+// Warps 4..11 (named barrier 3).
 __device__ void front_quant(const GemmParams& p, const int* pos, uint4 first16) {
     const int et = (int)threadIdx.x - 128;
     const int D = p.D, K = p.K, nblk = D / 32;
@@ -367,21 +353,13 @@ __device__ void front_quant(const GemmParams& p, const int* pos, uint4 first16) 
         uint32_t sc;
         const uint32_t word = front_quant8(raw, sc);  // whole warp
         if (active) {
-            int nvalid = 0;
             for (int k = 0; k < K; ++k) {
                 const int ps = pos[t * K + k];
                 if (ps >= 0) {
-                    ++nvalid;
                     *reinterpret_cast<uint32_t*>(p.ws.a1q + (size_t)ps * (D / 2) + gb * 16 + qd * 4) = word;
                     if (qd == 0) p.ws.a1s[(size_t)ps * p.a1s_stride + gb] = (uint8_t)sc;
                 }
             }
-            // the fused top-k sum's per-token state (as the quant kernel prepares it)
-            if (qd == 0 && gb == 0) p.ws.tok_nvalid[t] = nvalid;
-            if (qd == 0 && gb < p.n_fb) p.ws.tok_cnt[(size_t)t * p.n_fb + gb] = 0u;
-            if (nvalid == 0 && gb < p.Dl / 32)
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (size_t)t * p.Dl + gb * 32 + qd * 8) =
-                    make_uint4(0, 0, 0, 0);
         }
     }
     // the stage-1 route-tile copies (async proxy) read these bytes
@@ -459,101 +437,6 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint64_t adesc0, ui
     }
 }
 
-
-// Fused top-k sum (stage-2 epilogue, one epilogue group of 128 threads, after
-// the group has written the item's P rows: w[route] * y for the item's routes
-// and its MB*128 output features).  Deterministic without waiting:
-//  - every route of the item counts one arrival for (its token, the item's
-//    output block x.f); a token's count reaches its number of valid routes
-//    exactly once, in the item that writes the token's last P rows of the block;
-//  - the threads whose arrivals complete a count put those tokens (and their
-//    valid-route masks) on the group's list in shared memory;
-//  - the whole group then sums the listed tokens' P rows of the block: one
-//    thread per (token, 4 features), every route's row loaded before the sum,
-//    which runs over k in ascending order in fp32 from zero (the oracle's
-//    order), then one bf16 rounding;
-//  - the summed P lines are dead and are dropped from L2 (no write-back).
-// Writers fence before the group barrier that precedes the arrivals; a thread
-// whose arrival completes a count fences before the barrier after which the
-// group reads P (through L2).  sx: the group's exchange buffer ([0] count,
-// [4, 132) tokens, [132, 260) masks); free in stage 2.
-constexpr int kSumBatch = 12;  // route rows a thread loads before adding them
-
-__device__ __forceinline__ void epilogue_topk_sum(const GemmParams& p, const Item& x, bool front,
-                                                  uint32_t q4, uint32_t lane, uint32_t bar_id,
-                                                  int MB, uint32_t* status, int* sx) {
-    const int K = p.K;
-    const int tq = (int)(q4 * 32u + lane);
-    if (tq == 0) sx[0] = 0;
-    __threadfence();  // this thread's P stores, before the arrivals
-    named_bar_sync(bar_id, 128);
-    if (tq < x.nrows) {
-        const int rid = ld_route(front, p.ws.sorted_ids + x.row0 + tq);
-        if (rid < p.R) {
-            const int t = rid / K;
-            const uint32_t target = (uint32_t)__ldcg(p.ws.tok_nvalid + t);
-            const uint32_t old = atomicAdd(p.ws.tok_cnt + (size_t)t * p.n_fb + x.f, 1u);
-            if (old + 1u == target) {
-                __threadfence();  // the token's other P rows were fenced before their arrivals
-                uint32_t vm = 0;
-                for (int k = 0; k < K; ++k)
-                    vm |= (__ldcg(p.ws.route_pos + t * K + k) >= 0 ? 1u : 0u) << k;
-                const int slot = atomicAdd(sx, 1);
-                sx[4 + slot] = t;
-                sx[4 + 128 + slot] = (int)vm;
-            } else if (old + 1u > target) {
-                atomicOr(status, kErrCounterState);
-            }
-        }
-    }
-    named_bar_sync(bar_id, 128);
-    const int F = sx[0];
-    if (F == 0) return;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    const int units = F * MB * 32;  // (token, block h, 4 features); a multiple of 32: warp-uniform loop
-    for (int u = tq; u < units; u += 128) {
-        const int li = u / (MB * 32);
-        const int h = (u / 32) - li * MB;
-        const int c = u & 31;
-        const int t = sx[4 + li];
-        const uint32_t vm = (uint32_t)sx[4 + 128 + li];
-        const int blk = (x.f * MB + h) * 128;
-        const int n = blk + 4 * c;
-        const float* prow = p.ws.P + (size_t)t * K * p.D + n;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < K; k0 += kSumBatch) {
-            float4 v[kSumBatch];
-#pragma unroll
-            for (int i = 0; i < kSumBatch; ++i)
-                if (k0 + i < K && ((vm >> (k0 + i)) & 1u))
-                    v[i] = __ldcg(reinterpret_cast<const float4*>(prow + (size_t)(k0 + i) * p.D));
-#pragma unroll
-            for (int i = 0; i < kSumBatch; ++i) {
-                if (k0 + i < K && ((vm >> (k0 + i)) & 1u)) {
-                    acc.x = acc.x + v[i].x;
-                    acc.y = acc.y + v[i].y;
-                    acc.z = acc.z + v[i].z;
-                    acc.w = acc.w + v[i].w;
-                }
-            }
-        }
-        if (n < p.Dl) {
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-            uint2 pk;
-            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(out + (size_t)t * p.Dl + n) = pk;
-        }
-        // the 8 lanes that read a 128-byte line are this lane's neighbours in the
-        // warp; once they have all consumed their loads, the first drops the line
-        __syncwarp();
-        if ((c & 7) == 0) {
-            for (int k = 0; k < K; ++k)
-                if ((vm >> k) & 1u) discard_l2_line(prow + (size_t)k * p.D);
-        }
-    }
-}
 
 // Single-launch path, once per CTA after all its work: count the CTA out; the
 // last CTA clears the words the path shares across CTAs (ready word,
@@ -764,7 +647,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int MBp = mb_of(phs);
                 const uint32_t arows = 128u * (uint32_t)MBp;
                 for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
-                    const Item x = decode_item(q, p.ws.tiles, it, tcache, phs == 1 && p.s2_fmajor, num_tiles);
+                    const Item x = decode_item(q, p.ws.tiles, it, tcache);
                     for (int ks = x.ks0; ks < x.ks1; ++ks) {
                         if (!resolved && n_st == defer_n) {
                             resolve();
@@ -914,7 +797,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             };
             const long g_phase_end = g + (long)(phs == 0 ? my_items0 : my_items1) * q.kstages;
             for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
-                const Item x = decode_item(q, p.ws.tiles, it, tcache, phs == 1 && p.s2_fmajor, num_tiles);
+                const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
                     ok = false;
                     break;
@@ -1018,7 +901,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!ok) break;
             const StageGeom& q = p.g[phs];
             for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
-                const Item x = decode_item(q, p.ws.tiles, it, tcache, phs == 1 && p.s2_fmajor, num_tiles);
+                const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 for (int ks = x.ks0; ks < x.ks1; ++ks) {
                     if (!mbar_wait_warp(&sfull[s], ph, status, kErrTimeoutFull, abort_flag)) {
                         ok = false;
@@ -1112,7 +995,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int gbeg = g0;
                 g0 += per;
                 if ((local & (kEpiGroups - 1)) != grp) continue;
-                const Item x = decode_item(q, p.ws.tiles, it, tcache, phs == 1 && p.s2_fmajor, num_tiles);
+                const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 // route metadata of the tile's first 16 slots, fetched before waiting
                 const int slot0 = x.row0 + (int)(lane & 15);
                 int rid_pre = ld_route(front, p.ws.sorted_ids + slot0);
@@ -1251,9 +1134,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             }
                         }
                     }
-                    if (p.fused_sum)
-                        epilogue_topk_sum(p, x, front, q4, lane, bar_id, MB, status,
-                                          reinterpret_cast<int*>(xg));
                 }
                 if (!released) release();
             }

@@ -26,15 +26,12 @@ struct WsPtrs {
     uint8_t* a1s;          // [cap][a1s_stride]
     uint8_t* a2q;          // [cap][I/2]
     uint8_t* a2s;          // [cap][a2s_stride]
-    float* P;              // [R][D]: w[route] * stage-2 output row of each route
+    float* P;              // [R][D]: w[route] * stage-2 output of each route, by route id
     uint32_t* tile_done;   // stage-1 feature tiles completed per route tile (counters, or the
                            // status region's block on the single-launch path)
     uint32_t* quant_done;  // CTAs whose share of the hidden states is quantised (single launch)
     uint16_t* a1b;         // bf16-activation path: [cap][D] hidden rows in sorted order
     uint16_t* a2b;         // bf16-activation path: [cap][I] bf16 SwiGLU output in sorted order
-    int32_t* tok_nvalid;   // [T]: routes of each token with an expert id in [0, E)
-    uint32_t* tok_cnt;     // [T][n_fb]: stage-2 items that have written a token's P rows of
-                           // one output block (the fused top-k sum's arrival counters)
 };
 
 // Geometry of one grouped block-scaled GEMM stage (stage 1: gate_up, K = D;
@@ -82,12 +79,6 @@ struct GemmParams {
     const float* topk_w;
     const void* hidden;
     int T, cap;
-    // Fused top-k sum: the stage-2 epilogue counts each route's output block and
-    // the item that completes a token's count sums its P rows into out.
-    void* out;        // bf16 [T][Dl]
-    int n_fb;         // output blocks (stage-2 feature tiles) per token = g[1].n_ftiles
-    int s2_fmajor;    // stage-2 items in output-block-major order (P stays in L2)
-    int fused_sum;    // 1: the top-k sum runs in the stage-2 epilogue; 0: a separate kernel
 };
 
 // Parameters of the bf16-activation (W4A16) GEMM launch: packed e2m1 weights
@@ -160,13 +151,12 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream);
 // hidden rows hold Dl elements; quantised rows D (zero blocks past Dl)
-// Also per token: the valid-route count, the zeroed arrival counters of its n_fb
-// output blocks, and a zero out row when no route of the token is valid.
 cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride,
-                         int n_fb, void* out, const WsPtrs& ws, cudaStream_t stream);
-// Separate top-k sum (bf16-activation path): P rows hold D columns; out rows Dl.
-cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, int Dl, void* out,
-                          const WsPtrs& ws, cudaStream_t stream);
+                         const WsPtrs& ws, cudaStream_t stream);
+// Top-k sum: P rows by route id hold D columns, out rows Dl; a route counts where
+// route_pos >= 0 (its expert id is in [0, E)).
+cudaError_t launch_reduce(int T, int K, int D, int Dl, void* out, const WsPtrs& ws,
+                          cudaStream_t stream);
 // bf16-activation path: copy each token's hidden row to the sorted slot of
 // every valid route (after the routing kernel)
 cudaError_t launch_gather_bf16(const void* hidden, int T, int K, int D, const WsPtrs& ws,

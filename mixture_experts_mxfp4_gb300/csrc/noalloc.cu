@@ -16,9 +16,8 @@
 // contents.  The parts that must start at zero are zero when the library's
 // module is loaded (a __device__ array is zero-initialised) and are kept so: the
 // routing kernel clears the route-tile counters and status words at the start
-// of a multi-kernel call, the quantisation step clears the per-token counters
-// of the top-k sum, and the last CTA of a single-launch GEMM kernel clears the
-// words that kernel shares across CTAs.  Calls that overlap on the GPU
+// of a multi-kernel call, and the last CTA of a single-launch GEMM kernel clears
+// the words that kernel shares across CTAs.  Calls that overlap on the GPU
 // (different streams without ordering) race on the array.
 //
 // The array's device memory is committed when the module that holds it is

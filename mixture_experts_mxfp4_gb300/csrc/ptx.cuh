@@ -194,13 +194,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Drop the 128-byte L2 line at p (128-byte aligned) without writing it back:
-// for scratch whose contents are dead (read for the last time), so that its
-// dirty lines never cost a DRAM write.  The memory then holds unspecified data.
-__device__ __forceinline__ void discard_l2_line(const void* p) {
-    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
 // Named barrier over nthreads threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
     uint32_t r;

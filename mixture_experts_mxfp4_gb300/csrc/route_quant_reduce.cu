@@ -408,10 +408,6 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
 // activation is quantised once per token, as flower_moe.py does with topk=1
 // for the hidden states).  The loads and the quantisation run before the
 // routing kernel has finished (dependent launch); only the scatter waits.
-// The same threads prepare the top-k sum that the GEMM kernel's stage-2
-// epilogue runs: block 0 of a token stores the token's valid-route count,
-// blocks below n_fb zero the token's arrival counters, and a token without a
-// valid route gets a zero output row here (no stage-2 item ever reaches it).
 
 constexpr int kQuantThreads = 256;
 
@@ -430,7 +426,7 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float hi, float lo) {
 
 __global__ void __launch_bounds__(kQuantThreads)
     moe_quant_kernel(const __nv_bfloat16* __restrict__ hidden, int T, int K, int D, int Dl,
-                     int a1s_stride, int n_fb, __nv_bfloat16* __restrict__ out, WsPtrs ws) {
+                     int a1s_stride, WsPtrs ws) {
     grid_dep_launch();
     const int nblk = D / 32;
     const long gid = (long)blockIdx.x * kQuantThreads + threadIdx.x;
@@ -470,26 +466,17 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
     grid_dep_wait();  // route_pos comes from the routing kernel
     if (!active) return;
-    int nvalid = 0;
     for (int k = 0; k < K; ++k) {
         const int pos = ws.route_pos[t * K + k];
         if (pos >= 0) {
-            ++nvalid;
             *reinterpret_cast<uint4*>(ws.a1q + (size_t)pos * (D / 2) + g * 16) = codes;
             ws.a1s[(size_t)pos * a1s_stride + g] = (uint8_t)s;
         }
     }
-    if (g == 0) ws.tok_nvalid[t] = nvalid;
-    if (g < n_fb) ws.tok_cnt[(size_t)t * n_fb + g] = 0u;
-    if (nvalid == 0 && g < Dl / 32) {
-        uint4* o = reinterpret_cast<uint4*>(out + (size_t)t * Dl + g * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = make_uint4(0, 0, 0, 0);
-    }
 }
 
 cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride,
-                         int n_fb, void* out, const WsPtrs& ws, cudaStream_t stream) {
+                         const WsPtrs& ws, cudaStream_t stream) {
     const long total = (long)T * (D / 32);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((total + kQuantThreads - 1) / kQuantThreads));
@@ -502,32 +489,31 @@ cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, moe_quant_kernel,
                               reinterpret_cast<const __nv_bfloat16*>(hidden), T, K, D, Dl,
-                              a1s_stride, n_fb, reinterpret_cast<__nv_bfloat16*>(out), ws);
+                              a1s_stride, ws);
 }
 
 // ============================================================== top-k sum
 //
-// Separate top-k sum of the bf16-activation forward (the MXFP4 forward sums in
-// its GEMM kernel's stage-2 epilogue instead):
-// out[t, n] = bf16( sum over k ascending of P[t*K + k, n] ), skipping routes
-// whose id is outside [0, E), for the Dl logical columns (P rows hold D).
-// P already holds w[t,k] * y (stage-2 epilogue).  Deterministic: one thread
-// owns four outputs and adds in a fixed order.
+// out[t, n] = bf16( sum over k ascending of P[t*K + k, n] ) over the routes of
+// token t whose expert id is in [0, E) (route_pos >= 0: the routing kernel's map,
+// so the ids are not read again), for the Dl logical columns (P rows hold D).
+// P already holds w[t,k] * y (stage-2 epilogue).  Deterministic: one thread owns
+// four outputs and adds the routes' values in k order in fp32 from zero, rounded
+// once.  A token without a valid route gets a zero row.
 
 __global__ void __launch_bounds__(256)
-    moe_reduce_kernel(const int32_t* __restrict__ topk_ids, int T, int K, int E, int D, int Dl,
+    moe_reduce_kernel(const int32_t* __restrict__ route_pos, int T, int K, int D, int Dl,
                       const float* __restrict__ P, __nv_bfloat16* __restrict__ out) {
     grid_dep_launch();
-    grid_dep_wait();  // P comes from the stage-2 GEMM
+    grid_dep_wait();  // P comes from the stage-2 GEMM, route_pos from routing
     const int n4 = Dl / 4;
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)T * n4) return;
     const int t = (int)(idx / n4);
-    const int c = (int)(idx % n4);
+    const int c = (int)(idx - (long)t * n4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < K; ++k) {
-        const int e = __ldg(topk_ids + t * K + k);
-        if (e < 0 || e >= E) continue;
+        if (__ldg(route_pos + t * K + k) < 0) continue;
         const float4 v = __ldcs(reinterpret_cast<const float4*>(P + ((size_t)t * K + k) * D) + c);
         acc.x = acc.x + v.x;
         acc.y = acc.y + v.y;
@@ -542,8 +528,8 @@ __global__ void __launch_bounds__(256)
     *reinterpret_cast<uint2*>(out + (size_t)t * Dl + 4 * c) = pk;
 }
 
-cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, int Dl, void* out,
-                          const WsPtrs& ws, cudaStream_t stream) {
+cudaError_t launch_reduce(int T, int K, int D, int Dl, void* out, const WsPtrs& ws,
+                          cudaStream_t stream) {
     const long total = (long)T * (Dl / 4);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((total + 255) / 256));
@@ -554,8 +540,8 @@ cudaError_t launch_reduce(const int32_t* topk_ids, int T, int K, int E, int D, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_reduce_kernel, topk_ids, T, K, E, D, Dl,
-                              static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out));
+    return cudaLaunchKernelEx(&cfg, moe_reduce_kernel, static_cast<const int32_t*>(ws.route_pos), T, K,
+                              D, Dl, static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 // ============================================================== wait self-check
