@@ -317,13 +317,17 @@ moe_status_t moe_mxfp4_set_kernel_timing(int mode);
 
 /*
  * Tuning override for measurements (process-wide; results do not change, only
- * speed): tile_rows is the GEMM route-tile width (maximum MMA N, routes per
+ * speed).  tile_rows: the GEMM route-tile width (maximum MMA N, routes per
  * tile): 16, 32, 64 or 128, or 0 for the library's choice by shape (the
- * per-shape block_m table of flower_moe.py is the pages' counterpart).  Affects
+ * per-shape block_m table of flower_moe.py is the pages' counterpart).
+ * sf_copies: who copies the block scales to tensor memory: 1 the MMA-issuing
+ * warps (two of them), 2 a separate warp, one 128-element chunk per copy, 3 a
+ * separate warp, two chunks per copy where shared memory allows (else as 2),
+ * 0 the library's choice (2, measured fastest).  Affects
  * calls made after it (their plan, moe_mxfp4_get_plan, follows it); the
  * workspace size does not depend on it.  MOE_ERR_INVALID_ARG for other values.
  */
-moe_status_t moe_mxfp4_set_tuning(int tile_rows);
+moe_status_t moe_mxfp4_set_tuning(int tile_rows, int sf_copies);
 
 /*
  * Measurement aid for the roofline's compute term (no counterpart in the pages):

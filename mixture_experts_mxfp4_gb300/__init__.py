@@ -134,7 +134,7 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_set_single_launch.restype = i
     lib.moe_mxfp4_set_single_launch.argtypes = [i]
     lib.moe_mxfp4_set_tuning.restype = i
-    lib.moe_mxfp4_set_tuning.argtypes = [i]
+    lib.moe_mxfp4_set_tuning.argtypes = [i, i]
     lib.moe_mxfp4_tensor_probe.restype = i
     lib.moe_mxfp4_tensor_probe.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_double), P]
     lib.moe_mxfp4_call_launches.restype = i
@@ -238,9 +238,11 @@ def set_single_launch(mode):
     _check(load_library().moe_mxfp4_set_single_launch(int(mode)), "moe_mxfp4_set_single_launch")
 
 
-def set_tuning(tile_rows=0):
-    """Tuning override: route-tile width (16/32/64/128; 0 the library's choice)."""
-    _check(load_library().moe_mxfp4_set_tuning(int(tile_rows)), "moe_mxfp4_set_tuning")
+def set_tuning(tile_rows=0, sf_copies=0):
+    """Tuning override: route-tile width (16/32/64/128) and scale-factor copy
+    scheme (1 MMA warps, 2 separate warp, 3 separate warp with two-chunk copies);
+    0 the library's choice."""
+    _check(load_library().moe_mxfp4_set_tuning(int(tile_rows), int(sf_copies)), "moe_mxfp4_set_tuning")
 
 
 def tensor_probe(n, iters, copies_per_mma=0, variant=0, stream: int = 0) -> float:

@@ -59,9 +59,10 @@ moe_status_t validate_shape(int T, int D, int I, int E, int K) {
     return MOE_OK;
 }
 
-// Tuning override (moe_mxfp4_set_tuning): forced route-tile width; 0 = the
-// library's choice.  Process-wide.
+// Tuning override (moe_mxfp4_set_tuning): forced route-tile width and scale-factor
+// copy scheme; 0 = the library's choice.  Process-wide.
 std::atomic<int> g_force_tile_rows{0};
+std::atomic<int> g_force_sf_copies{0};
 
 // Maximum routes per GEMM tile: small tiles when experts see few routes
 // (decode), full 128-row tiles when they see many (prefill, dense shards).
@@ -277,7 +278,7 @@ uint32_t stage_geometry(StageGeom& q, int Kc, int tile_rows, int mblocks) {
 // hold either stage's layout.  Narrow route tiles (decode) use two MMA-issuing
 // warps: a single stream of scale-factor copies and narrow MMAs leaves the
 // tensor pipe idle between instructions, and a second stream fills it.
-void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2) {
+void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int sf_copies) {
     g.tile_rows = tile_rows;
     const uint32_t b1 = stage_geometry(g.g[0], D, tile_rows, 1);
     const uint32_t b2 = stage_geometry(g.g[1], I, tile_rows, mblocks2);
@@ -287,11 +288,37 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2) {
     const uint32_t xchg = (uint32_t)(kEpiGroups * kXchgBytes);  // stage-1 epilogue
     const uint32_t tcache = (uint32_t)kTileCache * 16u;
     const uint32_t fixed = 1024 /*align slack*/ + 512 /*barriers*/ + xchg + tcache;
-    const uint32_t budget = 227u * 1024u - fixed;
+    uint32_t budget = 227u * 1024u - fixed;
+    // Scale-factor copies (sf_copies, 0 = by shape): 1, each of two MMA warps
+    // copies its own stages' (narrow route tiles); 2, the scale-layout warp copies
+    // one 128-element chunk per instruction (.32x128b.warpx4) and one MMA warp
+    // issues only MMAs (128-route tiles); 3, as 2 but two chunks per instruction
+    // (.128x256b, the same cost per instruction) from two staging buffers of
+    // (mblocks + 1) * natoms / 2 blocks of 4 KB, where they leave the ring at least
+    // 4 slots (else as 2).  Measured (same GB300, alternating processes, trimmed
+    // means of 400/300 calls): decode T=16 85.1 / 83.9 / 89.0 us for schemes
+    // 1 / 2 / 3, decode T=128 169.5 / 168.9 / 184.6 us; dense T=512 291 us in
+    // every scheme (there 3 falls back to 2).  Scheme 2 is the default.
+    int mode = sf_copies ? sf_copies : 2;
+    auto wide_of = [](const StageGeom& q) {
+        return q.natoms % 2 == 0 ? (uint32_t)((q.mblocks + 1) * (q.natoms / 2)) * 4096u : 0u;
+    };
+    const uint32_t sfw = wide_of(g.g[0]) > wide_of(g.g[1]) ? wide_of(g.g[0]) : wide_of(g.g[1]);
+    g.wide_sf = 0;
+    g.sfw_bytes = 0;
+    if (mode == 3) {
+        if (sfw > 0 && (budget - 2 * sfw) / g.slot_bytes >= 4) {
+            g.wide_sf = 1;
+            g.sfw_bytes = sfw;
+            budget -= 2 * sfw;
+        } else {
+            mode = 2;
+        }
+    }
     int ns = (int)(budget / g.slot_bytes);
     if (ns > kMaxStages) ns = kMaxStages;
     const int mbmax = mblocks2 > 1 ? mblocks2 : 1;
-    int mw = tile_rows <= 64 ? 2 : 1;
+    int mw = mode == 1 ? 2 : 1;
     // TMEM: acc_bufs accumulator buffers of one N-column accumulator per MMA warp
     // and weight block, plus each ring slot's scale factors ((mblocks + 1) atoms
     // of 4 columns per 128-element chunk).
@@ -321,7 +348,8 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2) {
     g.off_bar = (uint32_t)ns * g.slot_bytes;
     g.off_xchg = g.off_bar + 512;  // barriers, TMEM slot and abort flag fit in 512 bytes
     g.off_tiles = g.off_xchg + xchg;
-    g.smem_bytes = g.off_tiles + tcache + 1024u;
+    g.off_sfw = g.off_tiles + tcache;  // (1024-aligned: every term above is)
+    g.smem_bytes = g.off_sfw + 2 * g.sfw_bytes + 1024u;
     const uint32_t cols = cols_for(nb, mw, ns);
     uint32_t alloc = 32;
     while (alloc < cols) alloc <<= 1;
@@ -457,7 +485,7 @@ struct LaunchState {
     moe::GemmParams gp;
     moe_mxfp4_plan_t pl;
     const void* key_ptr[5];
-    int key_shape[6];  // T, D, I, E, K, forced tile width
+    int key_shape[7];  // T, D, I, E, K, forced tile width, forced copy scheme
     bool valid;
 };
 
@@ -474,7 +502,7 @@ void shape_geometry(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, Gem
     gp->a2s_stride = pl->a2s_stride;
     // stage 2 on narrow tiles: two 128-row blocks of w2 per item share the route tile
     const int mb2 = (pl->tile_rows <= 64 && D % 256 == 0) ? 2 : 1;
-    gemm_geometry(*gp, D, I, pl->tile_rows, mb2);
+    gemm_geometry(*gp, D, I, pl->tile_rows, mb2, g_force_sf_copies.load(std::memory_order_relaxed));
 }
 
 // Whether a call of this shape routes and quantises inside the GEMM kernel under
@@ -528,7 +556,7 @@ bool launch_state(int dev, const void* w13, const void* w13_scale, const void* w
                   const void* w2_scale, int T, int D, int I, int E, int K, void* base,
                   LaunchState* out) {
     const void* kp[5] = {w13, w13_scale, w2, w2_scale, base};
-    const int ks[6] = {T, D, I, E, K, g_force_tile_rows.load()};
+    const int ks[7] = {T, D, I, E, K, g_force_tile_rows.load(), g_force_sf_copies.load()};
     std::lock_guard<std::mutex> lk(g_mu);
     for (int w = 0; w < kCacheWays; ++w) {
         const LaunchState& c = g_cache[dev][w];
@@ -852,10 +880,12 @@ moe_status_t moe_mxfp4_tensor_probe(int n, int iters, int copies_per_mma, int va
     return MOE_OK;
 }
 
-moe_status_t moe_mxfp4_set_tuning(int tile_rows) {
+moe_status_t moe_mxfp4_set_tuning(int tile_rows, int sf_copies) {
     if (!(tile_rows == 0 || tile_rows == 16 || tile_rows == 32 || tile_rows == 64 || tile_rows == 128))
         return MOE_ERR_INVALID_ARG;
+    if (sf_copies < 0 || sf_copies > 3) return MOE_ERR_INVALID_ARG;
     g_force_tile_rows.store(tile_rows);
+    g_force_sf_copies.store(sf_copies);
     return MOE_OK;
 }
 

@@ -416,6 +416,51 @@ __device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, ui
     }
 }
 
+// Two-atom scale-factor copies (tcgen05.cp .128x256b: 128 source rows of 32
+// bytes -> TMEM lanes 0..127, 8 columns).  Atom c's layout above repeats in each
+// 32-lane quadrant, so source row L = 32q + r (q = 0..3) holds atom c's row r
+// then atom c+1's row r; one copy fills atoms c and c+1.  The source is stored as
+// 16 groups of 8 rows, each group two 128-byte core matrices (the rows' first
+// and second 16 bytes): row L, half j at (L / 8) * 256 + j * 128 + (L % 8) * 16.
+// wide_sf_rows: read raw rows lane, lane+32, lane+64, lane+96 (sr bytes each:
+// 4 scale bytes per 128-element chunk) and write the natoms / 2 atom pairs of
+// this 128-row block, 4 KB each, from dst.  Whole warp.
+__device__ __forceinline__ uint32_t wide_sf_off(uint32_t L, uint32_t half) {
+    return (L >> 3) * 256u + half * 128u + (L & 7u) * 16u;
+}
+
+__device__ __forceinline__ void wide_sf_rows(const uint8_t* raw, int sr, int natoms, uint8_t* dst,
+                                             uint32_t lane) {
+    uint32_t v[4][4];
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1) {
+        const uint8_t* row = raw + (m1 * 32 + lane) * sr;
+        if (sr == 16) {
+            const uint4 r = *reinterpret_cast<const uint4*>(row);
+            v[m1][0] = r.x;
+            v[m1][1] = r.y;
+            v[m1][2] = r.z;
+            v[m1][3] = r.w;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[m1][c] = (c < natoms) ? reinterpret_cast<const uint32_t*>(row)[c] : 0u;
+        }
+    }
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+        if (2 * pp + 1 >= natoms) break;
+        uint8_t* d = dst + pp * 4096;
+        const uint4 lo = make_uint4(v[0][2 * pp], v[1][2 * pp], v[2][2 * pp], v[3][2 * pp]);
+        const uint4 hi = make_uint4(v[0][2 * pp + 1], v[1][2 * pp + 1], v[2][2 * pp + 1], v[3][2 * pp + 1]);
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q) {
+            const uint32_t L = 32u * q + lane;
+            *reinterpret_cast<uint4*>(d + wide_sf_off(L, 0)) = lo;
+            *reinterpret_cast<uint4*>(d + wide_sf_off(L, 1)) = hi;
+        }
+    }
+}
+
 // Issue KSTEPS of a stage's K-steps of 64, starting at K-step j0 (one thread).
 // SPB = K-steps per TMA box row (4 for 128-byte rows, 2 for 64-byte rows).
 // Descriptors advance by constant offsets: +32 bytes per K-step inside a
@@ -455,18 +500,23 @@ __device__ __forceinline__ void front_exit(const GemmParams& p, int num_tiles) {
     }
 }
 
-// kSfByLayoutWarp: warp 3 also copies the scale factors to TMEM (one MMA warp);
+// kSfMode: who copies the scale factors to TMEM: 0 the two MMA warps, each for
+// its own stages; 1 warp 3 (one MMA warp), one 128-element chunk per copy;
+// 2 warp 3 (one MMA warp), two chunks per copy where the stage holds an even
+// number of chunks (p.wide_sf; staging buffers outside the ring);
 // kFront: single launch (routing and quantisation in this kernel; p.fused_front).
 // kKs1, kKs2: K-steps per stage of stage 1 / stage 2, kMb2: weight blocks per
 // stage-2 item (0: read from the geometry at run time).
 // Template parameters so that each configuration's kernel carries only its code.
-template <bool kSfByLayoutWarp, bool kFront, int kKs1, int kKs2, int kMb2>
+template <int kSfMode, bool kFront, int kKs1, int kKs2, int kMb2>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmSA1,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSB1,
                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmSA2,
                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmSB2,
                     const GemmParams p) {
+    constexpr bool kSfByLayoutWarp = kSfMode != 0;
+    constexpr bool kWide = kSfMode == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -485,6 +535,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tempty = tfull + kMaxAccBufs;
     uint64_t* drain = tempty + kMaxAccBufs;  // one per MMA warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 3);  // drain[2]: scale-layout warp
+    // sbuf[b]: the scale-factor copies from staging buffer b have run (wide copies)
+    uint64_t* sbuf = reinterpret_cast<uint64_t*>(smem + p.off_bar + kSbufBarOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // per epilogue group: a 4 KB exchange buffer (kXchgBytes apart)
     float* xchg = reinterpret_cast<float*>(smem + p.off_xchg);
@@ -505,6 +557,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
         mbar_init(&drain[2], 1);
+        mbar_init(&sbuf[0], 1);
+        mbar_init(&sbuf[1], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -893,6 +947,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 3) {
         // ------------------------------------------------------------ scale layout
         bool copied = false;  // this warp issued scale-factor copies (drained below)
+        int gw = 0;           // stages that used the two-atom staging buffers so far
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -908,9 +963,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     uint8_t* st = smem + (size_t)s * p.slot_bytes;
+                    const int qmb = mb_of(phs), qna = na_of(phs);
+                    if (kWide && p.wide_sf && (qna & 1) == 0) {
+                        // Two-atom copies from staging buffer b = gw % 2: first wait
+                        // until the copies that read it two stages ago have run.
+                        const int b = gw & 1;
+                        if (gw >= 2 && !mbar_wait_warp(&sbuf[b], (uint32_t)((gw >> 1) - 1) & 1u, status,
+                                                       kErrTimeoutFull, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* wb = smem + p.off_sfw + (uint32_t)b * p.sfw_bytes;
+                        const int pairs = qna / 2;
+                        for (int h = 0; h < qmb; ++h)
+                            wide_sf_rows(st + q.off_sa + h * 128 * q.sr_a, q.sr_a, qna, wb + h * pairs * 4096, lane);
+                        wide_sf_rows(st + q.off_sb, 16, qna, wb + qmb * pairs * 4096, lane);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tc_fence_after();
+                            const uint32_t sfa = tmem_base + p.sf_col0 + (uint32_t)s * p.sf_cols;
+                            const uint32_t sfb = sfa + 4u * (uint32_t)(qmb * qna);
+                            for (int i = 0; i < (qmb + 1) * pairs; ++i) {
+                                // block i / pairs (qmb: the route tile), atom pair i % pairs
+                                const int h = i / pairs, pp = i - h * pairs;
+                                const uint32_t col = (h < qmb ? sfa + 4u * (uint32_t)(h * qna) : sfb) + 8u * (uint32_t)pp;
+                                tmem_cp_128x256b(col, smem_desc(smem_u32(wb + i * 4096), 128, 256, 0));
+                            }
+                            tc_commit(&sfready[s]);
+                            tc_commit(&sbuf[b]);
+                            copied = true;
+                        }
+                        __syncwarp();
+                        ++gw;
+                        if (++s == NS) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
+                    }
                     // block h's rows sit at h * 128 * sr_a; its natoms atoms replace them
                     // in place (128 * sr_a == natoms * 512)
-                    const int qmb = mb_of(phs), qna = na_of(phs);
                     for (int h = 0; h < qmb; ++h)
                         sf_to_atoms(st + q.off_sa + h * 128 * q.sr_a, q.sr_a, qna, lane);
                     sf_to_atoms(st + q.off_sb, 16, qna, lane);
@@ -1108,31 +1201,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                     }
                 } else {
-                    for (int h = 0; h < MB; ++h) {
+                    // chunk qi = (block h, 16 routes c); the next chunk's route ids and
+                    // weights (lanes & 15) are loaded while this chunk is stored
+                    int rid_l = rid_pre;
+                    float w_l = w_pre;
+                    const int total = MB * nchunks;
+                    for (int qi = 0; qi < total; ++qi) {
+                        const int h = qi / nchunks, c = qi - h * nchunks;
                         tacc = tacc_item + (uint32_t)(h * p.tile_rows);
                         // output feature of this lane in block h
                         const int n = (x.f * MB + h) * 128 + 32 * (int)q4 + (int)lane;
-                        for (int c = 0; c < nchunks; ++c) {
-                            float v[16];
-                            load_acc(c, v);
-                            if (h + 1 == MB && c + 1 == nchunks) {
-                                release();
-                                released = true;
-                            }
-                            int rid_l = rid_pre;
-                            float w_l = w_pre;
-                            if (c > 0) {
-                                const int sl = x.row0 + 16 * c + (int)(lane & 15);
-                                rid_l = ld_route(front, p.ws.sorted_ids + sl);
-                                w_l = ld_route(front, p.ws.sorted_w + sl);
-                            }
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int rid = __shfl_sync(0xffffffffu, rid_l, i);
-                                const float wv = __shfl_sync(0xffffffffu, w_l, i);
-                                if (rid < R) p.ws.P[(size_t)rid * p.D + n] = wv * v[i];
-                            }
+                        int rid_n = 0;
+                        float w_n = 0.0f;
+                        if (qi + 1 < total) {
+                            const int cn = c + 1 < nchunks ? c + 1 : 0;
+                            const int sl = x.row0 + 16 * cn + (int)(lane & 15);
+                            rid_n = ld_route(front, p.ws.sorted_ids + sl);
+                            w_n = ld_route(front, p.ws.sorted_w + sl);
                         }
+                        float v[16];
+                        load_acc(c, v);
+                        if (qi + 1 == total) {
+                            release();
+                            released = true;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int rid = __shfl_sync(0xffffffffu, rid_l, i);
+                            const float wv = __shfl_sync(0xffffffffu, w_l, i);
+                            if (rid < R) p.ws.P[(size_t)rid * p.D + n] = wv * v[i];
+                        }
+                        rid_l = rid_n;
+                        w_l = w_n;
                     }
                 }
                 if (!released) release();
@@ -1150,27 +1250,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream) {
     if ((p.sf_by_layout_warp != 0) != (p.mma_warps == 1)) return cudaErrorInvalidValue;
+    if (p.wide_sf && !p.sf_by_layout_warp) return cudaErrorInvalidValue;
     // instantiation: copy scheme, front end, and the stage shapes of the common
     // configurations (decode-like, dense-like, prefill-like), else the generic one
     const int ks1 = p.g[0].kstage_elems / 64, ks2 = p.g[1].kstage_elems / 64, mb2 = p.g[1].mblocks;
     const bool f = p.fused_front != 0;
+    const bool decode = ks1 == 8 && ks2 == 4 && mb2 == 2;
     int spec;  // index into kernels[]
     if (!p.sf_by_layout_warp)
-        spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 0 : 1;
+        spec = decode ? 0 : 1;
+    else if (p.wide_sf)
+        spec = decode ? 6 : 7;
     else
-        spec = (ks1 == 8 && ks2 == 8 && mb2 == 1) ? 2 : (ks1 == 8 && ks2 == 4 && mb2 == 1) ? 3 : 4;
+        spec = (ks1 == 8 && ks2 == 8 && mb2 == 1)   ? 2
+               : (ks1 == 8 && ks2 == 4 && mb2 == 1) ? 3
+               : decode                             ? 5
+                                                    : 4;
     using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                               CUtensorMap, CUtensorMap, GemmParams);
-    static const KernelFn kernels[2][5] = {
-        {moe_gemm_kernel<false, false, 8, 4, 2>, moe_gemm_kernel<false, false, 0, 0, 0>,
-         moe_gemm_kernel<true, false, 8, 8, 1>, moe_gemm_kernel<true, false, 8, 4, 1>,
-         moe_gemm_kernel<true, false, 0, 0, 0>},
-        {moe_gemm_kernel<false, true, 8, 4, 2>, moe_gemm_kernel<false, true, 0, 0, 0>,
-         moe_gemm_kernel<true, true, 8, 8, 1>, moe_gemm_kernel<true, true, 8, 4, 1>,
-         moe_gemm_kernel<true, true, 0, 0, 0>}};
+    static const KernelFn kernels[2][8] = {
+        {moe_gemm_kernel<0, false, 8, 4, 2>, moe_gemm_kernel<0, false, 0, 0, 0>,
+         moe_gemm_kernel<1, false, 8, 8, 1>, moe_gemm_kernel<1, false, 8, 4, 1>,
+         moe_gemm_kernel<1, false, 0, 0, 0>, moe_gemm_kernel<1, false, 8, 4, 2>,
+         moe_gemm_kernel<2, false, 8, 4, 2>, moe_gemm_kernel<2, false, 0, 0, 0>},
+        {moe_gemm_kernel<0, true, 8, 4, 2>, moe_gemm_kernel<0, true, 0, 0, 0>,
+         moe_gemm_kernel<1, true, 8, 8, 1>, moe_gemm_kernel<1, true, 8, 4, 1>,
+         moe_gemm_kernel<1, true, 0, 0, 0>, moe_gemm_kernel<1, true, 8, 4, 2>,
+         moe_gemm_kernel<2, true, 8, 4, 2>, moe_gemm_kernel<2, true, 0, 0, 0>}};
     const KernelFn kernel = kernels[f ? 1 : 0][spec];
     // Raise the dynamic shared-memory limit once per device and instantiation.
-    static bool limit_set[64][2][5];
+    static bool limit_set[64][2][8];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;

@@ -70,6 +70,11 @@ struct GemmParams {
     uint32_t sf_col0;     // first TMEM column of the per-slot scale-factor regions
     uint32_t off_bar, off_xchg, off_tiles;  // barriers, epilogue exchange buffer, tile cache
     uint32_t smem_bytes;                    // dynamic shared memory requested
+    // Two-atom scale-factor copies (tcgen05.cp .128x256b) from two staging buffers
+    // of sfw_bytes at off_sfw, for the phases whose stages hold an even number of
+    // 128-element chunks; otherwise one-atom copies from the ring slot.
+    int wide_sf;
+    uint32_t off_sfw, sfw_bytes;
     int a2s_stride;
     int a1s_stride;
     // Routing and quantisation inside the GEMM kernel (fused_front = 1, few
@@ -129,9 +134,12 @@ constexpr int kFrontMaxExperts = 384;  // single-launch path: one expert per GEM
 constexpr int kFrontAutoRoutes = 256;  // automatic mode: single launch up to this many routes
 constexpr int kRouteMultiMin = 4096;  // routes from which routing runs in three launches on many CTAs
 constexpr int kTileCache = 512;      // route tiles kept in shared memory (the rest read from L2)
-// Byte offset, within the GEMM kernel's 512-byte barrier block, of the
-// producer's bitmap of route tiles known to be complete (kTileCache bits).
+// Byte offsets, within the GEMM kernel's 512-byte barrier block, of the
+// producer's bitmap of route tiles known to be complete (kTileCache bits) and of
+// the two staging-buffer barriers of the scale-factor copies.
 constexpr int kReadyBitsOff = 384;
+constexpr int kSbufBarOff = kReadyBitsOff + kTileCache / 8;
+static_assert(kSbufBarOff + 16 <= 512, "barrier block");
 
 // Host-side pieces of the forward call shared by its entry points (api.cu).
 moe_status_t validate_forward(const void* hidden, const void* w13, const void* w13_scale,

@@ -290,23 +290,29 @@ def test_limits_and_routing_threshold(moe, T, D, I, E, K):
 
 
 @pytest.mark.parametrize("shape", [(16, 7168, 256, 257, 9), (256, 512, 256, 5, 3),
-                                   (96, 1024, 512, 3, 2)])
-def test_forced_tile_widths(moe, shape):
-    """Every forced route-tile width passes the parity checks; widths 16, 32 and
-    64 (two MMA-issuing warps) give equal outputs bit for bit."""
+                                   (96, 1024, 512, 3, 2), (16, 256, 128, 9, 3)])
+def test_forced_tile_widths_and_copy_schemes(moe, shape):
+    """Every forced route-tile width and scale-factor copy scheme passes the
+    parity checks.  With one MMA-issuing warp (copy schemes 2 and 3) the output
+    does not depend on the width or the scheme, bit for bit; with two (scheme 1)
+    it does not depend on the width."""
     w = workloads.custom(*shape)
     inp = workloads.make_inputs(w, seed=9)
     outs = {}
     try:
         for rows in (16, 32, 64, 128):
-            moe.set_tuning(rows)
-            m, _, out, _ = full_check(moe, w, inp)
-            assert m.plan.tile_rows == rows
-            outs[rows] = out.view(torch.int16).cpu()
+            for copies in (1, 2, 3):
+                moe.set_tuning(rows, copies)
+                m, _, out, _ = full_check(moe, w, inp)
+                assert m.plan.tile_rows == rows
+                outs[(rows, copies)] = out.view(torch.int16).cpu()
     finally:
-        moe.set_tuning(0)
+        moe.set_tuning(0, 0)
+    one_warp = [k for k in outs if k[1] in (2, 3)]
+    for k in one_warp:
+        assert torch.equal(outs[k], outs[one_warp[0]]), k
     for rows in (32, 64):
-        assert torch.equal(outs[rows], outs[16]), rows
+        assert torch.equal(outs[(rows, 1)], outs[(16, 1)]), rows
 
 
 def test_empty_batch(moe):
