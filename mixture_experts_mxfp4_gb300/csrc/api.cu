@@ -249,6 +249,9 @@ bool make_scale_map(CUtensorMap* m, const void* base, uint64_t rows, int S, int 
 
 // Layout of one GEMM stage for contraction length Kc inside a ring slot.
 // Returns the bytes one stage of it occupies.
+// Stages of up to 512 elements along K.  (Stages of 256 elements with twice as
+// many ring slots measured much slower: dense T=512 280 -> 392 us, decode T=16
+// 84 -> 155 us; the per-stage hand-offs between the roles set the pace.)
 uint32_t stage_geometry(StageGeom& q, int Kc, int tile_rows, int mblocks) {
     q.mblocks = mblocks;
     q.kstage_elems = Kc >= 512 ? 512 : Kc;
@@ -285,7 +288,10 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int
     g.g[0].n_ftiles = I / 64;
     g.g[1].n_ftiles = D / (128 * mblocks2);
     g.slot_bytes = b1 > b2 ? b1 : b2;
-    const uint32_t xchg = (uint32_t)(kEpiGroups * kXchgBytes);  // stage-1 epilogue
+    // epilogue groups: three for 128-route tiles whose stage-2 items are a single
+    // stage (the stage-2 epilogue bounds those, see kMaxEpiGroups), else two
+    g.epi_groups = (tile_rows == 128 && g.g[1].kstages == 1) ? 3 : 2;
+    const uint32_t xchg = (uint32_t)(g.epi_groups * kXchgBytes);  // epilogue exchange buffers
     const uint32_t tcache = (uint32_t)kTileCache * 16u;
     const uint32_t fixed = 1024 /*align slack*/ + 512 /*barriers*/ + xchg + tcache;
     uint32_t budget = 227u * 1024u - fixed;
@@ -327,7 +333,10 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int
     auto cols_for = [&](int b, int m, int n) {
         return (uint32_t)(b * m * mbmax * tile_rows) + (uint32_t)n * sfc;
     };
+    // accumulator buffers: as many as fit, up to 4 (128-route tiles: 3, measured
+    // dense T=512 290.7 -> 279.8 us and prefill T=4096 814 -> 802.6 us against 2)
     int nb = 4;
+    if (cols_for(nb, mw, ns) > 512u) nb = 3;
     if (cols_for(nb, mw, ns) > 512u) nb = 2;
     if (cols_for(nb, mw, ns) > 512u) mw = 1;
     while (ns > 1 && cols_for(nb, mw, ns) > 512u) --ns;

@@ -44,7 +44,7 @@
 //   warp 3  rearranges each stage's raw scale tiles into the tcgen05
 //           scale-factor layout ahead of the MMA warps (with one MMA warp it
 //           also copies them to TMEM and signals when the copies have run)
-//   warps 4-11  epilogue: two groups of four warps take alternate items; the two
+//   warps 4-11 (4-15)  epilogue: two (three) groups of four warps take items in turn; the two
 //           MMA warps' partial accumulators are summed in a fixed order
 // Single-launch mode (few routes): the CTAs also route (in shared memory) and
 // quantise the hidden states before the first route-tile copies (front_route,
@@ -383,16 +383,18 @@ __device__ __forceinline__ V ld_route(bool written_here, const V* ptr) {
 // 128 rows occupies an "atom" of 4 columns, and the MMA's scale-factor address
 // must be the first (4-aligned) column of an atom.
 //
-// Rearrange a raw scale tile (row m at m*sr bytes, 4-byte chunk c = scales of
-// K elements [128c, 128c+128)) into natoms scale-factor atoms in place: atom c
-// holds 128 rows as [m % 32][m / 32][4 bytes], the layout tcgen05.cp .32x128b
-// .warpx4 expects.  Whole warp; rows >= 128 are not touched.
-__device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, uint32_t lane) {
+// Rearrange a raw scale tile (row m at src + m*sr bytes, 4-byte chunk c =
+// scales of K elements [128c, 128c+128)) into natoms scale-factor atoms at dst:
+// atom c holds 128 rows as [m % 32][m / 32][4 bytes], the layout tcgen05.cp
+// .32x128b.warpx4 expects.  dst may overlap src (every row is read before any
+// write).  Whole warp; rows >= 128 are not touched.
+__device__ __forceinline__ void sf_to_atoms(const uint8_t* src, int sr, int natoms, uint8_t* dst,
+                                            uint32_t lane) {
     uint32_t v[4][4];
-    if (sr == 16) {  // whole 16-byte rows: conflict-free vector loads
+    if (sr == 16 && natoms == 4) {  // whole 16-byte rows: conflict-free vector loads
 #pragma unroll
         for (int m1 = 0; m1 < 4; ++m1) {
-            const uint4 r = *reinterpret_cast<const uint4*>(buf + (m1 * 32 + lane) * 16);
+            const uint4 r = *reinterpret_cast<const uint4*>(src + (m1 * 32 + lane) * 16);
             v[m1][0] = r.x;
             v[m1][1] = r.y;
             v[m1][2] = r.z;
@@ -401,7 +403,7 @@ __device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, ui
     } else {
 #pragma unroll
         for (int m1 = 0; m1 < 4; ++m1) {
-            const uint32_t* row = reinterpret_cast<const uint32_t*>(buf + (m1 * 32 + lane) * sr);
+            const uint32_t* row = reinterpret_cast<const uint32_t*>(src + (m1 * 32 + lane) * sr);
 #pragma unroll
             for (int c = 0; c < 4; ++c) v[m1][c] = (c < natoms) ? row[c] : 0u;
         }
@@ -411,7 +413,7 @@ __device__ __forceinline__ void sf_to_atoms(uint8_t* buf, int sr, int natoms, ui
     for (int c = 0; c < 4; ++c) {
         if (c < natoms) {
             uint4 w = make_uint4(v[0][c], v[1][c], v[2][c], v[3][c]);
-            *reinterpret_cast<uint4*>(buf + c * 512 + lane * 16) = w;
+            *reinterpret_cast<uint4*>(dst + c * 512 + lane * 16) = w;
         }
     }
 }
@@ -435,7 +437,7 @@ __device__ __forceinline__ void wide_sf_rows(const uint8_t* raw, int sr, int nat
 #pragma unroll
     for (int m1 = 0; m1 < 4; ++m1) {
         const uint8_t* row = raw + (m1 * 32 + lane) * sr;
-        if (sr == 16) {
+        if (sr == 16 && natoms == 4) {
             const uint4 r = *reinterpret_cast<const uint4*>(row);
             v[m1][0] = r.x;
             v[m1][1] = r.y;
@@ -508,8 +510,8 @@ __device__ __forceinline__ void front_exit(const GemmParams& p, int num_tiles) {
 // kKs1, kKs2: K-steps per stage of stage 1 / stage 2, kMb2: weight blocks per
 // stage-2 item (0: read from the geometry at run time).
 // Template parameters so that each configuration's kernel carries only its code.
-template <int kSfMode, bool kFront, int kKs1, int kKs2, int kMb2>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int kSfMode, bool kFront, int kKs1, int kKs2, int kMb2, int kEpi>
+__global__ void __launch_bounds__(128 + 128 * kEpi, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmSA1,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmSB1,
                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmSA2,
@@ -517,6 +519,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const GemmParams p) {
     constexpr bool kSfByLayoutWarp = kSfMode != 0;
     constexpr bool kWide = kSfMode == 2;
+    constexpr int kThreads = 128 + 128 * kEpi;  // kEpi epilogue groups
+    static_assert(!kFront || kThreads == kGemmThreads, "the front end assumes the 12-warp layout");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -634,7 +638,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         return;
     }
     if (!front) {
-        for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kGemmThreads)
+        for (int i = (int)threadIdx.x; i < num_tiles && i < kTileCache; i += kThreads)
             tcache[i] = __ldcg(p.ws.tiles + i);
     }
     if (warp == 2) {
@@ -1005,8 +1009,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // block h's rows sit at h * 128 * sr_a; its natoms atoms replace them
                     // in place (128 * sr_a == natoms * 512)
                     for (int h = 0; h < qmb; ++h)
-                        sf_to_atoms(st + q.off_sa + h * 128 * q.sr_a, q.sr_a, qna, lane);
-                    sf_to_atoms(st + q.off_sb, 16, qna, lane);
+                        sf_to_atoms(st + q.off_sa + h * 128 * q.sr_a, q.sr_a, qna, st + q.off_sa + h * qna * 512,
+                                    lane);
+                    sf_to_atoms(st + q.off_sb, 16, qna, st + q.off_sb, lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -1087,7 +1092,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 const int gbeg = g0;
                 g0 += per;
-                if ((local & (kEpiGroups - 1)) != grp) continue;
+                if (local % kEpi != grp) continue;
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
                 // route metadata of the tile's first 16 slots, fetched before waiting
                 const int slot0 = x.row0 + (int)(lane & 15);
@@ -1140,15 +1145,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const int tq = (int)(q4 * 32u + lane);
                         const int ri = tq >> 4, bb = (tq >> 3) & 1, sub = tq & 7;
                         const int feat0 = n0 + 32 * bb;  // first feature of this thread's block
+                        int rid_nx = rid_pre;  // the next chunk's route ids, loaded a chunk ahead
                         for (int c = 0; c < nchunks; ++c) {
+                            const int rid_l = rid_nx;
+                            if (c + 1 < nchunks)
+                                rid_nx = ld_route(front, p.ws.sorted_ids + x.row0 + 16 * (c + 1) + (int)(lane & 15));
                             float v[16];
                             load_acc(c, v);
                             if (c + 1 == nchunks) {
                                 release();
                                 released = true;
                             }
-                            const int rid_l =
-                                c == 0 ? rid_pre : ld_route(front, p.ws.sorted_ids + x.row0 + 16 * c + (int)(lane & 15));
                             const uint32_t valid = __ballot_sync(0xffffffffu, rid_l < R);
 #pragma unroll
                             for (int hh = 0; hh < 2; ++hh) {
@@ -1251,35 +1258,41 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream) {
     if ((p.sf_by_layout_warp != 0) != (p.mma_warps == 1)) return cudaErrorInvalidValue;
     if (p.wide_sf && !p.sf_by_layout_warp) return cudaErrorInvalidValue;
-    // instantiation: copy scheme, front end, and the stage shapes of the common
-    // configurations (decode-like, dense-like, prefill-like), else the generic one
+    // instantiation: copy scheme, front end, the stage shapes of the common
+    // configurations (decode-like, dense-like, prefill-like) and the epilogue
+    // groups, else a generic one with two epilogue groups
     const int ks1 = p.g[0].kstage_elems / 64, ks2 = p.g[1].kstage_elems / 64, mb2 = p.g[1].mblocks;
     const bool f = p.fused_front != 0;
-    const bool decode = ks1 == 8 && ks2 == 4 && mb2 == 2;
-    int spec;  // index into kernels[]
-    if (!p.sf_by_layout_warp)
-        spec = decode ? 0 : 1;
-    else if (p.wide_sf)
-        spec = decode ? 6 : 7;
-    else
-        spec = (ks1 == 8 && ks2 == 8 && mb2 == 1)   ? 2
-               : (ks1 == 8 && ks2 == 4 && mb2 == 1) ? 3
-               : decode                             ? 5
-                                                    : 4;
+    const int mode = !p.sf_by_layout_warp ? 0 : p.wide_sf ? 2 : 1;
+    const bool three = p.epi_groups == 3 && !f;
     using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                               CUtensorMap, CUtensorMap, GemmParams);
-    static const KernelFn kernels[2][8] = {
-        {moe_gemm_kernel<0, false, 8, 4, 2>, moe_gemm_kernel<0, false, 0, 0, 0>,
-         moe_gemm_kernel<1, false, 8, 8, 1>, moe_gemm_kernel<1, false, 8, 4, 1>,
-         moe_gemm_kernel<1, false, 0, 0, 0>, moe_gemm_kernel<1, false, 8, 4, 2>,
-         moe_gemm_kernel<2, false, 8, 4, 2>, moe_gemm_kernel<2, false, 0, 0, 0>},
-        {moe_gemm_kernel<0, true, 8, 4, 2>, moe_gemm_kernel<0, true, 0, 0, 0>,
-         moe_gemm_kernel<1, true, 8, 8, 1>, moe_gemm_kernel<1, true, 8, 4, 1>,
-         moe_gemm_kernel<1, true, 0, 0, 0>, moe_gemm_kernel<1, true, 8, 4, 2>,
-         moe_gemm_kernel<2, true, 8, 4, 2>, moe_gemm_kernel<2, true, 0, 0, 0>}};
+    // spec = the index into the table below (per front-end variant)
+    int spec;
+    if (mode == 0)
+        spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 0 : 1;
+    else if (mode == 1)
+        spec = (ks1 == 8 && ks2 == 8 && mb2 == 1)   ? 2
+               : (ks1 == 8 && ks2 == 4 && mb2 == 1) ? (three ? 8 : 3)
+               : (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 5
+                                                    : 4;
+    else
+        spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 6 : 7;
+    static const KernelFn kernels[2][9] = {
+        {moe_gemm_kernel<0, false, 8, 4, 2, 2>, moe_gemm_kernel<0, false, 0, 0, 0, 2>,
+         moe_gemm_kernel<1, false, 8, 8, 1, 2>, moe_gemm_kernel<1, false, 8, 4, 1, 2>,
+         moe_gemm_kernel<1, false, 0, 0, 0, 2>, moe_gemm_kernel<1, false, 8, 4, 2, 2>,
+         moe_gemm_kernel<2, false, 8, 4, 2, 2>, moe_gemm_kernel<2, false, 0, 0, 0, 2>,
+         moe_gemm_kernel<1, false, 8, 4, 1, 3>},
+        {moe_gemm_kernel<0, true, 8, 4, 2, 2>, moe_gemm_kernel<0, true, 0, 0, 0, 2>,
+         moe_gemm_kernel<1, true, 8, 8, 1, 2>, moe_gemm_kernel<1, true, 8, 4, 1, 2>,
+         moe_gemm_kernel<1, true, 0, 0, 0, 2>, moe_gemm_kernel<1, true, 8, 4, 2, 2>,
+         moe_gemm_kernel<2, true, 8, 4, 2, 2>, moe_gemm_kernel<2, true, 0, 0, 0, 2>,
+         moe_gemm_kernel<1, true, 8, 4, 1, 2>}};
+    const int epi = (spec == 8 && !f) ? 3 : 2;  // the instantiation's epilogue groups
     const KernelFn kernel = kernels[f ? 1 : 0][spec];
     // Raise the dynamic shared-memory limit once per device and instantiation.
-    static bool limit_set[64][2][8];
+    static bool limit_set[64][2][9];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -1291,7 +1304,7 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(128 + 128 * epi);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -75,6 +75,7 @@ struct GemmParams {
     // 128-element chunks; otherwise one-atom copies from the ring slot.
     int wide_sf;
     uint32_t off_sfw, sfw_bytes;
+    int epi_groups;  // epilogue groups of four warps (2 or 3): 128 + 128 * epi_groups threads
     int a2s_stride;
     int a1s_stride;
     // Routing and quantisation inside the GEMM kernel (fused_front = 1, few
@@ -123,8 +124,15 @@ constexpr int kFrontTileWord = 512;
 
 constexpr int kBlockM = 16;          // slots per padded block
 // 12 warps: producer, MMA, second MMA / TMEM owner, scale layout, 2 x 4 epilogue
+// (the single-launch front end assumes this layout)
 constexpr int kGemmThreads = 384;
 constexpr int kEpiGroups = 2;
+// 128-route tiles whose stage-2 items are one stage long (prefill-like: d_inter
+// 256) run a third epilogue group (16 warps): there the stage-2 epilogue bounds
+// the kernel (measured prefill T=4096 804 -> 728 us; dense T=512 and decode
+// shapes were slower with it, so they keep two).  Not with the single-launch
+// front end, which assumes two.
+constexpr int kMaxEpiGroups = 3;
 constexpr int kXchgBytes = 4352;     // per epilogue group: 4 KB exchange + flag
 constexpr int kMaxStages = 8;
 constexpr int kGemmSmemLimit = 227 * 1024;  // dynamic shared memory limit set on the GEMMs

@@ -290,7 +290,8 @@ def test_limits_and_routing_threshold(moe, T, D, I, E, K):
 
 
 @pytest.mark.parametrize("shape", [(16, 7168, 256, 257, 9), (256, 512, 256, 5, 3),
-                                   (96, 1024, 512, 3, 2), (16, 256, 128, 9, 3)])
+                                   (96, 1024, 512, 3, 2), (16, 256, 128, 9, 3),
+                                   (200, 2048, 1024, 4, 3)])
 def test_forced_tile_widths_and_copy_schemes(moe, shape):
     """Every forced route-tile width and scale-factor copy scheme passes the
     parity checks.  With one MMA-issuing warp (copy schemes 2 and 3) the output
