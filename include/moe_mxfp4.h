@@ -338,10 +338,12 @@ moe_status_t moe_mxfp4_set_tuning(int tile_rows, int sf_copies);
  * (the GEMM kernel's per-stage mix).  variant bit 0: the copies are
  * tcgen05.cp .128x256b (else .32x128b.warpx4, the GEMM kernel's); bit 1: a second
  * warp issues the copies (else the MMA thread, before each MMA); bits 2-3: the
- * MMAs rotate over 2^bits independent accumulators (n * 2^bits <= 256).  *flops
- * receives the dense operation count (2*128*n*64 per MMA); time the kernel with
- * events on `stream`.  n: 16..256, multiple of 16; iters: 1..1e7;
- * copies_per_mma: 0..8; variant: 0..15.  Needs a registered workspace (its
+ * MMAs rotate over 2^bits independent accumulators (n * 2^bits <= 256); bits
+ * 4-5: the MMA thread commits its tensor operations to an mbarrier after every
+ * 1, 4 or 8 MMAs (values 1, 2, 3; nothing waits on it).  *flops receives the
+ * dense operation count (2*128*n*64 per MMA); time the kernel with events on
+ * `stream`.  n: 16..256, multiple of 16; iters: 1..1e7; copies_per_mma: 0..8;
+ * variant: 0..63.  Needs a registered workspace (its
  * status word records a timed-out final wait; moe_mxfp4_last_device_status
  * reads it).  Overwrites nothing else.
  */

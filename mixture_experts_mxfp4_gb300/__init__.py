@@ -16,6 +16,8 @@ import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_mxfp4.so")
+# bounds-checked variant (build.build(checked=True)): same ABI, test aid
+CHECKED_LIB_PATH = os.path.join(_PKG, "_lib", "libmoe_mxfp4_checked.so")
 
 STATUS = {
     0: "MOE_OK",

@@ -382,7 +382,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" {
 
-const char* moe_mxfp4_version(void) { return "moe_mxfp4 0.1 (sm_103a, tcgen05 mxf4)"; }
+#if MOE_CHECKED
+const char* moe_mxfp4_version(void) { return "moe_mxfp4 0.2 (sm_103a, tcgen05 mxf4; bounds-checked build)"; }
+#else
+const char* moe_mxfp4_version(void) { return "moe_mxfp4 0.2 (sm_103a, tcgen05 mxf4)"; }
+#endif
 
 int moe_mxfp4_pointer_kind(const void* ptr) {
     if (!ptr) return -1;
@@ -635,7 +639,7 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     }
     mark(1);
     if (!front) {
-        if (launch_quant(hidden, T, K, D, Dl, pl.a1s_stride, ws, stream) != cudaSuccess)
+        if (launch_quant(hidden, T, K, D, Dl, pl.a1s_stride, pl.cap, ws, stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     mark(2);
@@ -869,7 +873,7 @@ moe_status_t moe_mxfp4_set_single_launch(int mode) {
 moe_status_t moe_mxfp4_tensor_probe(int n, int iters, int copies_per_mma, int variant,
                                     double* flops, cudaStream_t stream) {
     if (n < 16 || n > 256 || n % 16 != 0 || iters < 1 || iters > 10000000 || copies_per_mma < 0 ||
-        copies_per_mma > 8 || variant < 0 || variant > 15 || !flops)
+        copies_per_mma > 8 || variant < 0 || variant > 63 || !flops)
         return MOE_ERR_INVALID_ARG;
     if (n << ((variant >> 2) & 3) > 256) return MOE_ERR_INVALID_ARG;  // accumulators fit in 256 columns
     int dev = 0;

@@ -80,6 +80,15 @@ __device__ __forceinline__ Item decode_item(const StageGeom& q, const int4* gtil
     return x;
 }
 
+// Checked build: an item's route-tile fields lie in range (expert id, slots
+// inside the sorted arrays, rows a positive multiple of 16 within the tile
+// width, tile index below the call's tile count).  Every weight row, route row
+// and accumulator column an item touches follows from these.
+__device__ __forceinline__ bool item_in_range(const GemmParams& p, const Item& x, int num_tiles) {
+    return x.e >= 0 && x.e < p.E && x.row0 >= 0 && x.nrows > 0 && x.nrows <= p.tile_rows &&
+           (x.nrows & 15) == 0 && x.row0 + x.nrows <= p.cap && x.tile >= 0 && x.tile < num_tiles;
+}
+
 // ---------------------------------------------------------------- front end
 //
 // Single-launch path (few routes): every CTA routes all routes in shared memory
@@ -217,9 +226,10 @@ __device__ int front_route(const GemmParams& p, int* scr, int* pos, int4* tcache
         const bool valid = (r < r_end) && e >= 0 && e < E;
         const uint32_t m = __match_any_sync(0xffffffffu, valid ? e : -1);
         if (valid) {
-            const int slot = seg[e] + hist[warp * E + e] + __popc(m & lt_mask);
+            int slot = seg[e] + hist[warp * E + e] + __popc(m & lt_mask);
+            if (!moe_check(slot >= 0 && slot < p.cap, p.ws.status)) slot = -1;  // (skipped below)
             pos[r] = slot;
-            if (write_global) {
+            if (write_global && slot >= 0) {
                 p.ws.sorted_ids[slot] = r;
                 p.ws.sorted_w[slot] = __ldg(p.topk_w + r);
                 p.ws.route_pos[r] = slot;
@@ -355,7 +365,7 @@ __device__ void front_quant(const GemmParams& p, const int* pos, uint4 first16) 
         if (active) {
             for (int k = 0; k < K; ++k) {
                 const int ps = pos[t * K + k];
-                if (ps >= 0) {
+                if (ps >= 0 && moe_check(ps < p.cap && gb < nblk, p.ws.status)) {
                     *reinterpret_cast<uint32_t*>(p.ws.a1q + (size_t)ps * (D / 2) + gb * 16 + qd * 4) = word;
                     if (qd == 0) p.ws.a1s[(size_t)ps * p.a1s_stride + gb] = (uint8_t)sc;
                 }
@@ -563,7 +573,12 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
         mbar_init(&drain[2], 1);
         mbar_init(&sbuf[0], 1);
         mbar_init(&sbuf[1], 1);
-        *abort_flag = 0;
+        // checked build: accumulators and per-slot scale-factor columns inside the allocation
+        bool geo = (uint32_t)p.acc_bufs * p.acc_cols <= p.sf_col0 &&
+                   p.sf_col0 + (uint32_t)NS * p.sf_cols <= p.tmem_cols && p.acc_bufs <= kMaxAccBufs && NS <= kMaxStages;
+        for (int ph2 = 0; ph2 < 2; ++ph2)
+            geo = geo && (uint32_t)((p.g[ph2].mblocks + 1) * 4 * p.g[ph2].natoms) <= p.sf_cols;
+        *abort_flag = moe_check(geo, p.ws.status) ? 0 : 1;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -706,6 +721,11 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                 const uint32_t arows = 128u * (uint32_t)MBp;
                 for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                     const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                    if (!moe_check(item_in_range(p, x, num_tiles), status) || *abort_flag) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
                     for (int ks = x.ks0; ks < x.ks1; ++ks) {
                         if (!resolved && n_st == defer_n) {
                             resolve();
@@ -856,6 +876,11 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
             const long g_phase_end = g + (long)(phs == 0 ? my_items0 : my_items1) * q.kstages;
             for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                if (!moe_check(item_in_range(p, x, num_tiles), status)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
                 if (!mbar_wait_warp(&tempty[a], aph ^ 1u, status, kErrTimeoutTmemEmpty, abort_flag)) {
                     ok = false;
                     break;
@@ -961,6 +986,11 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
             const StageGeom& q = p.g[phs];
             for (int m = 0, it = item_of(phs, 0); it >= 0 && ok; it = item_of(phs, ++m)) {
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                if (!moe_check(item_in_range(p, x, num_tiles), status)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
                 for (int ks = x.ks0; ks < x.ks1; ++ks) {
                     if (!mbar_wait_warp(&sfull[s], ph, status, kErrTimeoutFull, abort_flag)) {
                         ok = false;
@@ -1094,6 +1124,11 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                 g0 += per;
                 if (local % kEpi != grp) continue;
                 const Item x = decode_item(q, p.ws.tiles, it, tcache);
+                if (!moe_check(item_in_range(p, x, num_tiles), status)) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
                 // route metadata of the tile's first 16 slots, fetched before waiting
                 const int slot0 = x.row0 + (int)(lane & 15);
                 int rid_pre = ld_route(front, p.ws.sorted_ids + slot0);

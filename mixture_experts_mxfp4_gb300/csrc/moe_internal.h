@@ -167,7 +167,7 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream);
 // hidden rows hold Dl elements; quantised rows D (zero blocks past Dl)
-cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride,
+cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride, int cap,
                          const WsPtrs& ws, cudaStream_t stream);
 // Top-k sum: P rows by route id hold D columns, out rows Dl; a route counts where
 // route_pos >= 0 (its expert id is in [0, E)).

@@ -11,7 +11,9 @@
 // a second warp (into columns the MMAs do not read) instead of the MMA thread;
 // bits 2-3, the MMAs rotate over 2^(bits) independent accumulators (n columns
 // each, at most 256 columns in all) instead of accumulating into one, so that
-// consecutive MMAs do not depend on each other.
+// consecutive MMAs do not depend on each other; bits 4-5, the MMA thread
+// commits its tensor operations to an mbarrier (which nothing waits on) after
+// every 1, 4 or 8 MMAs (bits 1, 2, 3), as a pipeline releases its stages.
 //
 // Operand values do not matter for the timing: shared memory is zero-filled,
 // so every product is zero.  One thread per CTA issues every MMA; the tensor
@@ -29,7 +31,7 @@ constexpr uint32_t kProbeAOff = 0;            // A: 128 rows x 128 B (128-byte s
 constexpr uint32_t kProbeBOff = 16384;        // B: up to 256 rows x 128 B
 constexpr uint32_t kProbeSfOff = 16384 + 32768;  // zeroed scale-factor source (4 KB)
 constexpr uint32_t kProbeBarOff = kProbeSfOff + 4096;
-constexpr uint32_t kProbeSmem = kProbeBarOff + 64 + 1024;  // + alignment slack
+constexpr uint32_t kProbeSmem = kProbeBarOff + 64 + 1024;  // + alignment slack (barriers: 3 x 8 B, slot)
 
 __global__ void __launch_bounds__(kProbeThreads, 1)
     moe_mxf4_probe_kernel(int n, int iters, int copies_per_mma, int variant, uint32_t* status) {
@@ -38,12 +40,14 @@ __global__ void __launch_bounds__(kProbeThreads, 1)
                                                ~uintptr_t(1023));
     uint64_t* done = reinterpret_cast<uint64_t*>(smem + kProbeBarOff);
     uint64_t* done2 = done + 1;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kProbeBarOff + 16);
+    uint64_t* tick = done + 2;  // periodic commits (never waited on)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kProbeBarOff + 24);
     for (uint32_t i = threadIdx.x * 16u; i < kProbeBarOff; i += kProbeThreads * 16u)
         *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
         mbar_init(done, 1);
         mbar_init(done2, 1);
+        mbar_init(tick, 1);
         fence_barrier_init();
     }
     fence_proxy_async_smem();  // the zeros are read by the tensor core (async proxy)
@@ -87,11 +91,14 @@ __global__ void __launch_bounds__(kProbeThreads, 1)
         const uint64_t bd = smem_desc(smem_u32(smem + kProbeBOff), 16, 1024, 2);
         const uint32_t idesc = mxf4_idesc(128, (uint32_t)n, 0, 0);
         const uint32_t amask = (1u << ((variant >> 2) & 3)) - 1u;  // accumulators - 1
+        const int cbits = (variant >> 4) & 3;
+        const int cper = cbits == 1 ? 1 : cbits == 2 ? 4 : cbits == 3 ? 8 : 0;  // MMAs per commit
         for (int it = 0; it < iters; ++it) {
             if (!other_warp)
                 for (int c = 0; c < copies_per_mma; ++c) copy(sfa + 8u * (uint32_t)(c & 1));
             const uint32_t acc = (uint32_t)it & amask;
             mma_mxf4(tmem + acc * (uint32_t)n, ad, bd, idesc, sfa, sfb, (uint32_t)it > amask ? 1u : 0u);
+            if (cper && (it % cper) == cper - 1) tc_commit(tick);
         }
         tc_commit(done);
         wait_done(done);

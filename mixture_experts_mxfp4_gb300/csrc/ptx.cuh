@@ -23,7 +23,26 @@ enum : uint32_t {
     kErrTimeoutTile = 1u << 6,     // stage-2 producer waited for a stage-1 route tile
     kErrTimeoutFront = 1u << 7,    // single-launch path waited for routing or quantisation
     kErrCounterState = 1u << 8,    // a counter was already past its target (status region not zeroed)
+    kErrChecked = 1u << 9,         // bounds-checked build: an index, coordinate or column out of range
 };
+
+// Bounds checks of the checked build (compiled with -DMOE_CHECKED=1): a failed
+// check records kErrChecked in the status word and the caller skips the access
+// (or aborts the CTA through its bounded waits).  In the product build every
+// check is the constant true and costs nothing.
+#ifndef MOE_CHECKED
+#define MOE_CHECKED 0
+#endif
+__device__ __forceinline__ bool moe_check(bool ok, uint32_t* status) {
+#if MOE_CHECKED
+    if (!ok) atomicOr(status, kErrChecked);
+    return ok;
+#else
+    (void)ok;
+    (void)status;
+    return true;
+#endif
+}
 
 // Status word 15 on the single-launch path: 0 between calls, kFrontReady once
 // CTA 0 of the GEMM kernel has zeroed the call's counters and written the

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 
     if (tid < E) ws.seg_start[tid] = seg[tid];
     if (tid == 0) ws.seg_start[E] = seg[E];  // (E may equal the thread count)
-    if (tid < E && cnt > 0) {
+    if (tid < E && cnt > 0 && moe_check(tile_e + ntiles <= n_counters && seg_e + padded <= cap, ws.status)) {
         for (int j = 0; j < ntiles; ++j) {
             const int rows = min(tile_rows, padded - j * tile_rows);
             ws.tiles[tile_e + j] = make_int4(tid, seg_e + j * tile_rows, rows, 0);
@@ -157,9 +157,11 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         const uint32_t m = __match_any_sync(0xffffffffu, key);
         if (valid) {
             const int pos = seg[e] + hist[warp * E + e] + __popc(m & lt_mask);
-            ws.sorted_ids[pos] = r;
-            ws.sorted_w[pos] = topk_w[r];
-            ws.route_pos[r] = pos;
+            if (moe_check(pos >= 0 && pos < cap, ws.status)) {
+                ws.sorted_ids[pos] = r;
+                ws.sorted_w[pos] = topk_w[r];
+                ws.route_pos[r] = pos;
+            }
         } else if (r < r_end) {
             ws.route_pos[r] = -1;
         }
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
             }
         }
     }
-    if (tid < E && cnt > 0) {
+    if (tid < E && cnt > 0 && moe_check(tile_e + ntiles <= n_counters && seg_e + padded <= cap, ws.status)) {
         for (int j = 0; j < ntiles; ++j) {
             const int rows = min(tile_rows, padded - j * tile_rows);
             ws.tiles[tile_e + j] = make_int4(tid, seg_e + j * tile_rows, rows, 0);
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 // Every CTA: its chunk's routes to their slots (ids, weights, route_pos).
 __global__ void __launch_bounds__(kChunkThreads)
     moe_route_scatter_kernel(const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w,
-                             int R, int E, int chunk, const int* __restrict__ ccount, WsPtrs ws) {
+                             int R, int E, int chunk, int cap, const int* __restrict__ ccount, WsPtrs ws) {
     extern __shared__ int cs_smem[];
     int* hist = cs_smem;  // [kChunkWarps][E]: counts, then first slots per warp
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -336,9 +338,11 @@ __global__ void __launch_bounds__(kChunkThreads)
         const uint32_t m = __match_any_sync(0xffffffffu, valid ? e : -1);
         if (valid) {
             const int pos = hist[warp * E + e] + __popc(m & lt_mask);
-            ws.sorted_ids[pos] = r;
-            ws.sorted_w[pos] = topk_w[r];
-            ws.route_pos[r] = pos;
+            if (moe_check(pos >= 0 && pos < cap, ws.status)) {
+                ws.sorted_ids[pos] = r;
+                ws.sorted_w[pos] = topk_w[r];
+                ws.route_pos[r] = pos;
+            }
         } else if (r < r_end) {
             ws.route_pos[r] = -1;
         }
@@ -378,7 +382,7 @@ cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, in
         cfg.gridDim = dim3((unsigned)C);
         cfg.blockDim = dim3(kChunkThreads);
         cfg.dynamicSmemBytes = csmem;
-        return cudaLaunchKernelEx(&cfg, moe_route_scatter_kernel, topk_ids, topk_w, R, E, chunk,
+        return cudaLaunchKernelEx(&cfg, moe_route_scatter_kernel, topk_ids, topk_w, R, E, chunk, cap,
                                   static_cast<const int*>(ccount), ws);
     }
     const size_t smem = sizeof(int) * ((size_t)kRouteWarps * E + (E + 1) + 64);
@@ -426,7 +430,7 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float hi, float lo) {
 
 __global__ void __launch_bounds__(kQuantThreads)
     moe_quant_kernel(const __nv_bfloat16* __restrict__ hidden, int T, int K, int D, int Dl,
-                     int a1s_stride, WsPtrs ws) {
+                     int a1s_stride, int cap, WsPtrs ws) {
     grid_dep_launch();
     const int nblk = D / 32;
     const long gid = (long)blockIdx.x * kQuantThreads + threadIdx.x;
@@ -468,14 +472,14 @@ __global__ void __launch_bounds__(kQuantThreads)
     if (!active) return;
     for (int k = 0; k < K; ++k) {
         const int pos = ws.route_pos[t * K + k];
-        if (pos >= 0) {
+        if (pos >= 0 && moe_check(pos < cap, ws.status)) {
             *reinterpret_cast<uint4*>(ws.a1q + (size_t)pos * (D / 2) + g * 16) = codes;
             ws.a1s[(size_t)pos * a1s_stride + g] = (uint8_t)s;
         }
     }
 }
 
-cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride,
+cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1s_stride, int cap,
                          const WsPtrs& ws, cudaStream_t stream) {
     const long total = (long)T * (D / 32);
     cudaLaunchConfig_t cfg = {};
@@ -489,7 +493,7 @@ cudaError_t launch_quant(const void* hidden, int T, int K, int D, int Dl, int a1
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, moe_quant_kernel,
                               reinterpret_cast<const __nv_bfloat16*>(hidden), T, K, D, Dl,
-                              a1s_stride, ws);
+                              a1s_stride, cap, ws);
 }
 
 // ============================================================== top-k sum

@@ -190,3 +190,17 @@ def test_tuning_override_without_device(lib):
     finally:
         moe.set_tuning(0, 0)
     assert moe.get_plan(*shape).tile_rows == 16
+
+
+def test_checked_build_without_device(lib):
+    """The bounds-checked variant builds from the same sources with MOE_CHECKED=1,
+    loads without a GPU, exports every declared entry point and says what it is."""
+    from mixture_experts_mxfp4_gb300 import build
+
+    path = build.build(checked=True)
+    clib = ctypes.CDLL(path)
+    for s in _declared_symbols():
+        assert hasattr(clib, s), s
+    clib.moe_mxfp4_version.restype = ctypes.c_char_p
+    assert b"bounds-checked" in clib.moe_mxfp4_version()
+    assert b"bounds-checked" not in lib.moe_mxfp4_version()
