@@ -1129,10 +1129,34 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                     ok = false;
                     break;
                 }
-                // route metadata of the tile's first 16 slots, fetched before waiting
-                const int slot0 = x.row0 + (int)(lane & 15);
-                int rid_pre = ld_route(front, p.ws.sorted_ids + slot0);
-                float w_pre = phs == 1 ? ld_route(front, p.ws.sorted_w + slot0) : 0.0f;
+                // Route metadata, fetched before waiting for the accumulator.  Stage 1,
+                // and stage 2 with two weight blocks per item (narrow tiles): the ids
+                // (and weights) of the tile's first 16 slots (lane & 15; later chunks
+                // are loaded a chunk ahead).  Stage 2 with one weight block: the ids and
+                // weights of all the tile's slots, lane l holding rows l, l + 32, l + 64
+                // and l + 96 (sentinel past the tile's rows): there a chunk of 16 stores
+                // takes less time than one load from L2, and loading a chunk ahead left
+                // every chunk waiting for its metadata (measured prefill T=4096: GEMM
+                // kernel 485 -> 440 us).
+                const int MBi = mb_of(phs);
+                int rid_pre = 0;
+                float w_pre = 0.0f;
+                int rid4[4] = {R, R, R, R};
+                float w4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (phs == 0 || MBi > 1) {
+                    const int slot0 = x.row0 + (int)(lane & 15);
+                    rid_pre = ld_route(front, p.ws.sorted_ids + slot0);
+                    if (phs == 1) w_pre = ld_route(front, p.ws.sorted_w + slot0);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = 32 * j + (int)lane;
+                        if (r < x.nrows) {
+                            rid4[j] = ld_route(front, p.ws.sorted_ids + x.row0 + r);
+                            w4[j] = ld_route(front, p.ws.sorted_w + x.row0 + r);
+                        }
+                    }
+                }
                 if (!mbar_wait_warp(&tfull[a], aph, status, kErrTimeoutTmemFull, abort_flag)) {
                     ok = false;
                     break;
@@ -1242,7 +1266,7 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                                 atomicOr(status, kErrCounterState);
                         }
                     }
-                } else {
+                } else if (MB > 1) {
                     // chunk qi = (block h, 16 routes c); the next chunk's route ids and
                     // weights (lanes & 15) are loaded while this chunk is stored
                     int rid_l = rid_pre;
@@ -1275,6 +1299,29 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                         }
                         rid_l = rid_n;
                         w_l = w_n;
+                    }
+                } else {
+                    // one weight block: chunk c = rows 16c .. 16c + 15 of the tile, held
+                    // by lanes 16 (c & 1) .. +15 in register c >> 1
+                    // output feature of this lane
+                    const int n = x.f * 128 + 32 * (int)q4 + (int)lane;
+                    for (int c = 0; c < nchunks; ++c) {
+                        const int j = c >> 1;
+                        const int rid_l = j == 0 ? rid4[0] : j == 1 ? rid4[1] : j == 2 ? rid4[2] : rid4[3];
+                        const float w_l = j == 0 ? w4[0] : j == 1 ? w4[1] : j == 2 ? w4[2] : w4[3];
+                        const int lb = (c & 1) * 16;
+                        float v[16];
+                        load_acc(c, v);
+                        if (c + 1 == nchunks) {
+                            release();
+                            released = true;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int rid = __shfl_sync(0xffffffffu, rid_l, lb + i);
+                            const float wv = __shfl_sync(0xffffffffu, w_l, lb + i);
+                            if (rid < R) p.ws.P[(size_t)rid * p.D + n] = wv * v[i];
+                        }
                     }
                 }
                 if (!released) release();
