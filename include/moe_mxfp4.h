@@ -316,6 +316,19 @@ int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk);
 moe_status_t moe_mxfp4_set_kernel_timing(int mode);
 
 /*
+ * NVTX ranges for timeline profilers (process-wide; off by default).  on = 1:
+ * every forward call pushes one range named "moe_mxfp4 forward" (with the shape,
+ * the entry point and the launch mode) around its enqueue, with nested ranges
+ * "route", "quant", "gemm" and "topk_sum" around each kernel launch, so a
+ * timeline tool correlates them with the kernels.  The ranges are host-side (the
+ * enqueue), cost a few hundred nanoseconds per call without an attached tool
+ * and change nothing on the device.  on = 0 turns them off.  MOE_ERR_INVALID_ARG
+ * for other values.  The header-only NVTX of the CUDA toolkit is compiled in;
+ * nothing is linked.
+ */
+moe_status_t moe_mxfp4_set_nvtx(int on);
+
+/*
  * Tuning override for measurements (process-wide; results do not change, only
  * speed).  tile_rows: the GEMM route-tile width (maximum MMA N, routes per
  * tile): 16, 32, 64 or 128, or 0 for the library's choice by shape (the

@@ -45,6 +45,7 @@ EXPORTS = [
     "moe_mxfp4_version",
     "moe_mxfp4_num_kernels",
     "moe_mxfp4_set_kernel_timing",
+    "moe_mxfp4_set_nvtx",
     "moe_mxfp4_kernel_times",
     "moe_mxfp4_last_call_ms",
     "moe_mxfp4_forward_noalloc",
@@ -133,6 +134,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_num_kernels.argtypes = []
     lib.moe_mxfp4_set_kernel_timing.restype = i
     lib.moe_mxfp4_set_kernel_timing.argtypes = [i]
+    lib.moe_mxfp4_set_nvtx.restype = i
+    lib.moe_mxfp4_set_nvtx.argtypes = [i]
     lib.moe_mxfp4_set_single_launch.restype = i
     lib.moe_mxfp4_set_single_launch.argtypes = [i]
     lib.moe_mxfp4_set_tuning.restype = i
@@ -261,6 +264,11 @@ def tensor_probe(n, iters, copies_per_mma=0, variant=0, stream: int = 0) -> floa
 def call_launches(T, d_model, d_inter, E, topk) -> int:
     """Kernels one forward call of this shape launches under the current launch mode."""
     return int(load_library().moe_mxfp4_call_launches(T, d_model, d_inter, E, topk))
+
+
+def set_nvtx(on: bool):
+    """NVTX ranges around every forward call and kernel launch (off by default)."""
+    _check(load_library().moe_mxfp4_set_nvtx(1 if on else 0), "moe_mxfp4_set_nvtx")
 
 
 def set_kernel_timing(mode):

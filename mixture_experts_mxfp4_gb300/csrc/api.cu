@@ -4,6 +4,8 @@
 // on the caller's stream.  Nothing here allocates device memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <atomic>
@@ -37,6 +39,34 @@ struct Timing {
 
 std::mutex g_mu;
 WorkspaceReg g_ws[kMaxDevices];
+
+// NVTX ranges (moe_mxfp4_set_nvtx): a call range and one range per launch.
+std::atomic<int> g_nvtx{0};
+
+struct LaunchRange {
+    bool on;
+    explicit LaunchRange(const char* name) : on(g_nvtx.load(std::memory_order_relaxed) != 0) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~LaunchRange() {
+        if (on) nvtxRangePop();
+    }
+};
+
+struct CallRange {
+    bool on;
+    CallRange(const char* entry, int T, int D, int I, int E, int K, int launches)
+        : on(g_nvtx.load(std::memory_order_relaxed) != 0) {
+        if (!on) return;
+        char msg[160];
+        snprintf(msg, sizeof(msg), "moe_mxfp4 forward (%s) T=%d d_model=%d d_inter=%d E=%d topk=%d launches=%d",
+                 entry, T, D, I, E, K, launches);
+        nvtxRangePushA(msg);
+    }
+    ~CallRange() {
+        if (on) nvtxRangePop();
+    }
+};
 int g_num_sms[kMaxDevices];
 // moe_mxfp4_set_single_launch mode per device (0 separate, 1 single, 2 auto); -1 = unset
 int g_single_launch[kMaxDevices] = {};
@@ -631,21 +661,31 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
         std::lock_guard<std::mutex> lk(g_mu);
         g_last_ws[dev] = base;
     }
+    const CallRange call_range(Dl != D || Il != I ? "padded" : "mxfp4", T, D, I, E, K,
+                               front ? 2 : (T * K >= kRouteMultiMin ? 6 : 4));
     mark(0);
     if (!front) {
+        const LaunchRange r("route");
         if (launch_route(topk_ids, topk_weights, T, K, E, pl.tile_rows, pl.cap, n_counters, ws,
                          stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     mark(1);
     if (!front) {
+        const LaunchRange r("quant");
         if (launch_quant(hidden, T, K, D, Dl, pl.a1s_stride, pl.cap, ws, stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     mark(2);
-    if (launch_gemm(st->maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    {
+        const LaunchRange r(front ? "gemm (with routing and quantisation)" : "gemm");
+        if (launch_gemm(st->maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     mark(3);
-    if (launch_reduce(T, K, D, Dl, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    {
+        const LaunchRange r("topk_sum");
+        if (launch_reduce(T, K, D, Dl, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     mark(4);
     if (timed) {
         tm.recorded = true;
@@ -733,15 +773,28 @@ moe_status_t forward_w4a16_on_workspace(const void* hidden, const void* w13, con
     auto mark = [&](int i) {
         if (timed && (tm.mode == 1 || i == 0 || i == kNumKernels)) cudaEventRecord(tm.ev[i], stream);
     };
+    const CallRange call_range("w4a16", T, D, I, E, K, T * K >= kRouteMultiMin ? 6 : 4);
     mark(0);
-    if (launch_route(topk_ids, topk_weights, T, K, E, tr, pl.cap, pl.max_tiles, g.ws, stream) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    {
+        const LaunchRange r("route");
+        if (launch_route(topk_ids, topk_weights, T, K, E, tr, pl.cap, pl.max_tiles, g.ws, stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     mark(1);
-    if (launch_gather_bf16(hidden, T, K, D, g.ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    {
+        const LaunchRange r("gather_bf16");
+        if (launch_gather_bf16(hidden, T, K, D, g.ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     mark(2);
-    if (launch_w4a16_gemm(maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    {
+        const LaunchRange r("gemm_w4a16");
+        if (launch_w4a16_gemm(maps, g, sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     mark(3);
-    if (launch_reduce(T, K, D, D, out, g.ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    {
+        const LaunchRange r("topk_sum");
+        if (launch_reduce(T, K, D, D, out, g.ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     mark(4);
     if (timed) {
         tm.recorded = true;
@@ -899,6 +952,12 @@ moe_status_t moe_mxfp4_set_tuning(int tile_rows, int sf_copies) {
     if (sf_copies < 0 || sf_copies > 3) return MOE_ERR_INVALID_ARG;
     g_force_tile_rows.store(tile_rows);
     g_force_sf_copies.store(sf_copies);
+    return MOE_OK;
+}
+
+moe_status_t moe_mxfp4_set_nvtx(int on) {
+    if (on != 0 && on != 1) return MOE_ERR_INVALID_ARG;
+    g_nvtx.store(on, std::memory_order_relaxed);
     return MOE_OK;
 }
 

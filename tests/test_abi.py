@@ -192,6 +192,20 @@ def test_tuning_override_without_device(lib):
     assert moe.get_plan(*shape).tile_rows == 16
 
 
+def test_nvtx_switch_without_device(lib):
+    """The NVTX switch takes 0 and 1 and rejects anything else (no device needed:
+    the ranges are host-side)."""
+    import mixture_experts_mxfp4_gb300 as moe
+
+    try:
+        moe.set_nvtx(True)
+        moe.set_nvtx(False)
+        for bad in (-1, 2, 7):
+            assert lib.moe_mxfp4_set_nvtx(bad) == 1
+    finally:
+        moe.set_nvtx(False)
+
+
 def test_checked_build_without_device(lib):
     """The bounds-checked variant builds from the same sources with MOE_CHECKED=1,
     loads without a GPU, exports every declared entry point and says what it is."""

@@ -431,6 +431,25 @@ def test_launch_modes_bitwise_identical(moe):
     assert torch.equal(sids[0], sids[1])
 
 
+@pytest.mark.gpu
+def test_nvtx_ranges_change_nothing(moe, launch_mode):
+    """With NVTX ranges on (no profiler attached) the forward gives the same
+    output bit for bit as with them off, in both launch modes."""
+    w = workloads.WORKLOADS[workloads.DECODE_T16]
+    inp = workloads.make_inputs(w, seed=5)
+    outs = []
+    for on in (False, True):
+        moe.set_nvtx(on)
+        try:
+            m, t, out = run_gpu(moe, inp, w)
+            torch.cuda.synchronize()
+            assert m.device_status() == 0
+            outs.append(out.view(torch.int16).cpu())
+        finally:
+            moe.set_nvtx(False)
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_quantiser_every_bf16_value(moe, launch_mode):
     """Every finite bf16 value goes through the activation quantiser (the quant
     kernel, or the one inside the GEMM kernel in single-launch mode): once in
