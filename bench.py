@@ -329,7 +329,8 @@ def run_gpu(args, w, world, rank, local):
     # three launches from 4096 routes)
     launches = ((6 if w.T * w.K >= 4096 else 4) if bf16_act
                 else moe.call_launches(w.T, w.D, w.I, w.E, w.K))
-    single = launches == 1 and not bf16_act
+    # single launch: the GEMM kernel (routing and quantisation inside) and the top-k sum
+    single = launches == 2 and not bf16_act
     moe.set_kernel_timing(2)
     for _ in range(args.warmup):
         flush.zero_()
@@ -543,8 +544,8 @@ def run_gpu(args, w, world, rank, local):
         "us_per_call_l2_not_flushed": warm_us,
         "per_kernel_us": {n: (None if v is None else 1e3 * v / k_steps) for n, v in per_kernel.items()},
         "per_kernel_note": f"{k_steps} steps with events between kernels (serialised); null: "
-                           "nothing launched in that slot (top-k sum inside the GEMM kernel; "
-                           "routing and quantisation too in single-launch mode)",
+                           "nothing launched in that slot (single-launch mode: routing and "
+                           "quantisation run inside the GEMM kernel)",
         "dominant_kernel": dom,
         "roofline": roofline,
         "roofline_forward": {"bound": "hbm", "alg_bytes": b_total, "achieved": fwd_gbs,
