@@ -336,7 +336,9 @@ moe_status_t moe_mxfp4_set_nvtx(int on);
  * sf_copies: who copies the block scales to tensor memory: 1 the MMA-issuing
  * warps (two of them), 2 a separate warp, one 128-element chunk per copy, 3 a
  * separate warp, two chunks per copy where shared memory allows (else as 2),
- * 0 the library's choice (2, measured fastest).  Affects
+ * 4 a separate warp, one chunk per copy, with two MMA-issuing warps taking
+ * alternate pipeline stages where their accumulators fit in tensor memory (else
+ * as 2), 0 the library's choice.  Affects
  * calls made after it (their plan, moe_mxfp4_get_plan, follows it); the
  * workspace size does not depend on it.  MOE_ERR_INVALID_ARG for other values.
  */

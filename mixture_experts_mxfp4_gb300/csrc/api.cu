@@ -334,7 +334,10 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int
     // 4 slots (else as 2).  Measured (same GB300, alternating processes, trimmed
     // means of 400/300 calls): decode T=16 85.1 / 83.9 / 89.0 us for schemes
     // 1 / 2 / 3, decode T=128 169.5 / 168.9 / 184.6 us; dense T=512 291 us in
-    // every scheme (there 3 falls back to 2).  Scheme 2 is the default.
+    // every scheme (there 3 falls back to 2).  Scheme 2 is the default.  4: the
+    // scale-layout warp copies one chunk per instruction and two MMA warps take
+    // alternate stages (a single issuing thread serialises its MMAs; where the
+    // two warps' accumulators do not fit in TMEM it falls back to 2).
     int mode = sf_copies ? sf_copies : 2;
     auto wide_of = [](const StageGeom& q) {
         return q.natoms % 2 == 0 ? (uint32_t)((q.mblocks + 1) * (q.natoms / 2)) * 4096u : 0u;
@@ -354,7 +357,7 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int
     int ns = (int)(budget / g.slot_bytes);
     if (ns > kMaxStages) ns = kMaxStages;
     const int mbmax = mblocks2 > 1 ? mblocks2 : 1;
-    int mw = mode == 1 ? 2 : 1;
+    int mw = (mode == 1 || mode == 4) ? 2 : 1;
     // TMEM: acc_bufs accumulator buffers of one N-column accumulator per MMA warp
     // and weight block, plus each ring slot's scale factors ((mblocks + 1) atoms
     // of 4 columns per 128-element chunk).
@@ -378,7 +381,7 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int
     // With one MMA warp (wide route tiles) the scale-layout warp also copies each
     // stage's scale factors to TMEM, so the MMA warp issues MMAs only (measured:
     // dense T512 390 -> 340 us); two MMA warps overlap their copies better themselves.
-    g.sf_by_layout_warp = mw == 1 ? 1 : 0;
+    g.sf_by_layout_warp = (mode != 1 || mw == 1) ? 1 : 0;
     g.mma_warps = mw;
     g.acc_bufs = nb;
     g.num_stages = ns;
@@ -949,7 +952,7 @@ moe_status_t moe_mxfp4_tensor_probe(int n, int iters, int copies_per_mma, int va
 moe_status_t moe_mxfp4_set_tuning(int tile_rows, int sf_copies) {
     if (!(tile_rows == 0 || tile_rows == 16 || tile_rows == 32 || tile_rows == 64 || tile_rows == 128))
         return MOE_ERR_INVALID_ARG;
-    if (sf_copies < 0 || sf_copies > 3) return MOE_ERR_INVALID_ARG;
+    if (sf_copies < 0 || sf_copies > 4) return MOE_ERR_INVALID_ARG;
     g_force_tile_rows.store(tile_rows);
     g_force_sf_copies.store(sf_copies);
     return MOE_OK;

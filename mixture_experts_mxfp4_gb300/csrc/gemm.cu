@@ -515,7 +515,10 @@ __device__ __forceinline__ void front_exit(const GemmParams& p, int num_tiles) {
 // kSfMode: who copies the scale factors to TMEM: 0 the two MMA warps, each for
 // its own stages; 1 warp 3 (one MMA warp), one 128-element chunk per copy;
 // 2 warp 3 (one MMA warp), two chunks per copy where the stage holds an even
-// number of chunks (p.wide_sf; staging buffers outside the ring);
+// number of chunks (p.wide_sf; staging buffers outside the ring); 3 warp 3, one
+// chunk per copy, with two MMA warps taking alternate stages (a single issuing
+// thread serialises its MMAs at ~190 cycles each whatever N, two issue in
+// parallel: the probe measured N = 16 434 -> 1974 TFLOP/s);
 // kFront: single launch (routing and quantisation in this kernel; p.fused_front).
 // kKs1, kKs2: K-steps per stage of stage 1 / stage 2, kMb2: weight blocks per
 // stage-2 item (0: read from the geometry at run time).
@@ -529,6 +532,9 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                     const GemmParams p) {
     constexpr bool kSfByLayoutWarp = kSfMode != 0;
     constexpr bool kWide = kSfMode == 2;
+    // MMA-issuing warps: two when they copy their own scale factors (mode 0) or in
+    // mode 3, else one (the host geometry ties them; launch_gemm checks it)
+    constexpr int kMW = (kSfMode == 0 || kSfMode == 3) ? 2 : 1;
     constexpr int kThreads = 128 + 128 * kEpi;  // kEpi epilogue groups
     static_assert(!kFront || kThreads == kGemmThreads, "the front end assumes the 12-warp layout");
     extern __shared__ uint8_t smem_raw[];
@@ -565,7 +571,7 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
             mbar_init(&sfull[s], 1);
         }
         for (int a = 0; a < p.acc_bufs; ++a) {
-            mbar_init(&tfull[a], (uint32_t)(kSfByLayoutWarp ? 1 : 2));
+            mbar_init(&tfull[a], (uint32_t)kMW);  // every MMA warp commits once per item
             mbar_init(&tempty[a], 128);
         }
         mbar_init(&drain[0], 1);
@@ -597,9 +603,6 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
     // Single-launch path: route in shared memory (the ring is not in use yet);
     // otherwise the routing kernel's tile count.
     constexpr bool front = kFront;
-    // MMA-issuing warps: one exactly when warp 3 copies the scale factors (the host
-    // geometry ties the two; launch_gemm checks it)
-    constexpr int kMW = kSfByLayoutWarp ? 1 : 2;
     // the generic instantiation keeps one copy of each phase loop: its shapes
     // are small, where cold code after launch costs more than the loop
     constexpr int kPhaseUnroll = kKs1 ? 2 : 1;
@@ -1338,14 +1341,17 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
 
 cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                         cudaStream_t stream) {
-    if ((p.sf_by_layout_warp != 0) != (p.mma_warps == 1)) return cudaErrorInvalidValue;
-    if (p.wide_sf && !p.sf_by_layout_warp) return cudaErrorInvalidValue;
+    // copy scheme and MMA warps: MMA-warp copies with two MMA warps, layout-warp
+    // copies with one or (one chunk per copy) two
+    if (p.mma_warps != 1 && p.mma_warps != 2) return cudaErrorInvalidValue;
+    if (!p.sf_by_layout_warp && p.mma_warps != 2) return cudaErrorInvalidValue;
+    if (p.wide_sf && (!p.sf_by_layout_warp || p.mma_warps != 1)) return cudaErrorInvalidValue;
     // instantiation: copy scheme, front end, the stage shapes of the common
     // configurations (decode-like, dense-like, prefill-like) and the epilogue
     // groups, else a generic one with two epilogue groups
     const int ks1 = p.g[0].kstage_elems / 64, ks2 = p.g[1].kstage_elems / 64, mb2 = p.g[1].mblocks;
     const bool f = p.fused_front != 0;
-    const int mode = !p.sf_by_layout_warp ? 0 : p.wide_sf ? 2 : 1;
+    const int mode = !p.sf_by_layout_warp ? 0 : p.wide_sf ? 2 : p.mma_warps == 2 ? 3 : 1;
     const bool three = p.epi_groups == 3 && !f;
     using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                               CUtensorMap, CUtensorMap, GemmParams);
@@ -1358,23 +1364,27 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
                : (ks1 == 8 && ks2 == 4 && mb2 == 1) ? (three ? 8 : 3)
                : (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 5
                                                     : 4;
-    else
+    else if (mode == 2)
         spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 6 : 7;
-    static const KernelFn kernels[2][9] = {
+    else
+        spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 9 : 10;
+    static const KernelFn kernels[2][11] = {
         {moe_gemm_kernel<0, false, 8, 4, 2, 2>, moe_gemm_kernel<0, false, 0, 0, 0, 2>,
          moe_gemm_kernel<1, false, 8, 8, 1, 2>, moe_gemm_kernel<1, false, 8, 4, 1, 2>,
          moe_gemm_kernel<1, false, 0, 0, 0, 2>, moe_gemm_kernel<1, false, 8, 4, 2, 2>,
          moe_gemm_kernel<2, false, 8, 4, 2, 2>, moe_gemm_kernel<2, false, 0, 0, 0, 2>,
-         moe_gemm_kernel<1, false, 8, 4, 1, 3>},
+         moe_gemm_kernel<1, false, 8, 4, 1, 3>,
+         moe_gemm_kernel<3, false, 8, 4, 2, 2>, moe_gemm_kernel<3, false, 0, 0, 0, 2>},
         {moe_gemm_kernel<0, true, 8, 4, 2, 2>, moe_gemm_kernel<0, true, 0, 0, 0, 2>,
          moe_gemm_kernel<1, true, 8, 8, 1, 2>, moe_gemm_kernel<1, true, 8, 4, 1, 2>,
          moe_gemm_kernel<1, true, 0, 0, 0, 2>, moe_gemm_kernel<1, true, 8, 4, 2, 2>,
          moe_gemm_kernel<2, true, 8, 4, 2, 2>, moe_gemm_kernel<2, true, 0, 0, 0, 2>,
-         moe_gemm_kernel<1, true, 8, 4, 1, 2>}};
+         moe_gemm_kernel<1, true, 8, 4, 1, 2>,
+         moe_gemm_kernel<3, true, 8, 4, 2, 2>, moe_gemm_kernel<3, true, 0, 0, 0, 2>}};
     const int epi = (spec == 8 && !f) ? 3 : 2;  // the instantiation's epilogue groups
     const KernelFn kernel = kernels[f ? 1 : 0][spec];
     // Raise the dynamic shared-memory limit once per device and instantiation.
-    static bool limit_set[64][2][9];
+    static bool limit_set[64][2][11];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;

@@ -181,11 +181,11 @@ def test_tuning_override_without_device(lib):
     size = moe.workspace_size(*shape)
     try:
         for rows in (16, 32, 64, 128):
-            for copies in (0, 1, 2, 3):
+            for copies in (0, 1, 2, 3, 4):
                 moe.set_tuning(rows, copies)
                 assert moe.get_plan(*shape).tile_rows == rows
                 assert moe.workspace_size(*shape) == size
-        for bad in ((8, 0), (48, 0), (256, 0), (-1, 0), (0, 4), (0, -1)):
+        for bad in ((8, 0), (48, 0), (256, 0), (-1, 0), (0, 5), (0, -1)):
             assert lib.moe_mxfp4_set_tuning(*bad) == 1
     finally:
         moe.set_tuning(0, 0)

@@ -296,13 +296,14 @@ def test_forced_tile_widths_and_copy_schemes(moe, shape):
     """Every forced route-tile width and scale-factor copy scheme passes the
     parity checks.  With one MMA-issuing warp (copy schemes 2 and 3) the output
     does not depend on the width or the scheme, bit for bit; with two (scheme 1)
-    it does not depend on the width."""
+    it does not depend on the width; scheme 4 (layout-warp copies, two MMA warps
+    where their accumulators fit, else one) gives scheme 1's or scheme 2's output."""
     w = workloads.custom(*shape)
     inp = workloads.make_inputs(w, seed=9)
     outs = {}
     try:
         for rows in (16, 32, 64, 128):
-            for copies in (1, 2, 3):
+            for copies in (1, 2, 3, 4):
                 moe.set_tuning(rows, copies)
                 m, _, out, _ = full_check(moe, w, inp)
                 assert m.plan.tile_rows == rows
@@ -314,6 +315,9 @@ def test_forced_tile_widths_and_copy_schemes(moe, shape):
         assert torch.equal(outs[k], outs[one_warp[0]]), k
     for rows in (32, 64):
         assert torch.equal(outs[(rows, 1)], outs[(16, 1)]), rows
+    for rows in (16, 32, 64, 128):
+        assert (torch.equal(outs[(rows, 4)], outs[(rows, 1)]) or
+                torch.equal(outs[(rows, 4)], outs[(rows, 2)])), rows
 
 
 def test_empty_batch(moe):
