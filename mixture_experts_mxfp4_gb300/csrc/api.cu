@@ -368,11 +368,25 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int
     };
     // accumulator buffers: as many as fit, up to 4 (128-route tiles: 3, measured
     // dense T=512 290.7 -> 279.8 us and prefill T=4096 814 -> 802.6 us against 2)
-    int nb = 4;
-    if (cols_for(nb, mw, ns) > 512u) nb = 3;
-    if (cols_for(nb, mw, ns) > 512u) nb = 2;
-    if (cols_for(nb, mw, ns) > 512u) mw = 1;
+    auto pick_nb = [&]() {
+        int b = 4;
+        if (cols_for(b, mw, ns) > 512u) b = 3;
+        if (cols_for(b, mw, ns) > 512u) b = 2;
+        return b;
+    };
+    int nb = pick_nb();
+    if (cols_for(nb, mw, ns) > 512u) {  // two MMA warps' accumulators do not fit: one
+        mw = 1;
+        nb = pick_nb();
+    }
     while (ns > 1 && cols_for(nb, mw, ns) > 512u) --ns;
+    // An epilogue group's next item uses buffer (item % nb); its wait on that
+    // buffer's barrier parity is unambiguous only if the buffer's previous user has
+    // completed its MMAs, which the group's own previous item (item - groups)
+    // guarantees when nb >= groups (MMAs complete in order).  Fewer buffers than
+    // groups (a forced copy scheme whose two MMA warps fell back to one) get fewer
+    // groups.
+    if (g.epi_groups > nb) g.epi_groups = nb;
     // The MMA warps' look-ahead tests slot (g + mw) % ns by parity; that is only
     // unambiguous when the slot's previous stage (g + mw - ns) belonged to the
     // same warp, i.e. when ns is a multiple of mw (and ns > mw); otherwise it is

@@ -581,7 +581,8 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
         mbar_init(&sbuf[1], 1);
         // checked build: accumulators and per-slot scale-factor columns inside the allocation
         bool geo = (uint32_t)p.acc_bufs * p.acc_cols <= p.sf_col0 &&
-                   p.sf_col0 + (uint32_t)NS * p.sf_cols <= p.tmem_cols && p.acc_bufs <= kMaxAccBufs && NS <= kMaxStages;
+                   p.sf_col0 + (uint32_t)NS * p.sf_cols <= p.tmem_cols && p.acc_bufs <= kMaxAccBufs && NS <= kMaxStages &&
+                   p.acc_bufs >= kEpi;  // (see gemm_geometry: buffers >= epilogue groups)
         for (int ph2 = 0; ph2 < 2; ++ph2)
             geo = geo && (uint32_t)((p.g[ph2].mblocks + 1) * 4 * p.g[ph2].natoms) <= p.sf_cols;
         *abort_flag = moe_check(geo, p.ws.status) ? 0 : 1;
@@ -1382,6 +1383,9 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
          moe_gemm_kernel<1, true, 8, 4, 1, 2>,
          moe_gemm_kernel<3, true, 8, 4, 2, 2>, moe_gemm_kernel<3, true, 0, 0, 0, 2>}};
     const int epi = (spec == 8 && !f) ? 3 : 2;  // the instantiation's epilogue groups
+    // an epilogue group's accumulator-barrier parity is unambiguous only with at
+    // least as many buffers as groups (gemm_geometry keeps it so)
+    if (p.acc_bufs < epi) return cudaErrorInvalidValue;
     const KernelFn kernel = kernels[f ? 1 : 0][spec];
     // Raise the dynamic shared-memory limit once per device and instantiation.
     static bool limit_set[64][2][11];
