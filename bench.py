@@ -94,11 +94,21 @@ def measured_peaks():
         return HBM_FALLBACK_GBS, BF16_FALLBACK_TFLOPS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and blank space, so that editing a
+    comment does not mark a profile of the same code as stale."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the code (comments and spacing excluded) of the sources the GEMM
+    kernel and its launch geometry are built from; profile summaries record it."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -109,7 +119,7 @@ def profiled_traffic(workload: str):
         text = open(profile_summary(workload)).read()
     except OSError:
         return None
-    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_hash = re.search(r"kernel_code_sha256_16:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
         return None

@@ -35,17 +35,18 @@
 // Pipeline (one CTA per SM, persistent over work items):
 //   warp 0  TMA producer: one box each for the weight tile, the route tile and
 //           the two raw scale tiles per stage -> smem ring
-//   warp 1  MMA warp: copies a stage's scale factors to TMEM (tcgen05.cp) and
-//           issues tcgen05.mma.  With mma_warps = 2, warp 2 is a second MMA warp:
-//           the CTA's stages alternate between the two (each into its own
-//           accumulator), so two instruction streams keep the tensor pipe busy
-//           with narrow (small-N) MMAs
+//   warp 1  MMA warp: issues tcgen05.mma (and, in copy scheme 0, copies its
+//           stages' scale factors to TMEM with tcgen05.cp).  With two MMA warps
+//           (schemes 0 and 3) warp 2 is the second: the CTA's stages alternate
+//           between the two, each into its own accumulator, so two threads issue
+//           MMAs (one issuing thread serialises them)
 //   warp 2  also allocates / frees TMEM
 //   warp 3  rearranges each stage's raw scale tiles into the tcgen05
-//           scale-factor layout ahead of the MMA warps (with one MMA warp it
-//           also copies them to TMEM and signals when the copies have run)
-//   warps 4-11 (4-15)  epilogue: two (three) groups of four warps take items in turn; the two
-//           MMA warps' partial accumulators are summed in a fixed order
+//           scale-factor layout ahead of the MMA warps (schemes 1-3: it also
+//           copies them to TMEM and signals when the copies have run)
+//   warps 4-11 (4-15)  epilogue: two (three) groups of four warps take items in
+//           turn; with two MMA warps their partial accumulators are summed in a
+//           fixed order
 // Single-launch mode (few routes): the CTAs also route (in shared memory) and
 // quantise the hidden states before the first route-tile copies (front_route,
 // front_quant), so no routing or quantisation kernel runs before this one.
@@ -1089,7 +1090,7 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
-        // Two groups of four warps take alternate items, so one item's global
+        // The groups of four warps take items in turn, so one item's global
         // traffic overlaps the next item's TMEM reads.  Each group covers the 128
         // TMEM lanes (warp % 4 = lane quadrant).
         const uint32_t q4 = warp & 3u;           // TMEM lane quadrant of this warp

@@ -48,3 +48,15 @@ def test_algorithmic_bytes_of_the_decode_workload():
     assert total == 33 * per_expert + 2 * 16 * 7168 * 2 + 16 * 3 * 8
     _, gemm_bf16, _ = bench.alg_bytes(w, ids, bf16_act=True)
     assert gemm_bf16 == 33 * per_expert + 16 * 7168 * 2
+
+
+def test_kernel_code_hash_ignores_comments_only():
+    """The hash that ties a committed ncu summary to the GEMM sources changes with
+    the code and not with comments or spacing."""
+    import bench
+
+    code = "int f(int a) {\n  return a + 1;  // one\n}\n/* block\n comment */\n"
+    same = "int f(int a) { return a + 1; }\n// another comment\n"
+    other = "int f(int a) { return a + 2; }\n"
+    assert bench._code_only(code) == bench._code_only(same)
+    assert bench._code_only(code) != bench._code_only(other)
