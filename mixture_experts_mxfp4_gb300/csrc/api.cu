@@ -387,10 +387,14 @@ void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int
     // groups (a forced copy scheme whose two MMA warps fell back to one) get fewer
     // groups.
     if (g.epi_groups > nb) g.epi_groups = nb;
-    // The MMA warps' look-ahead tests slot (g + mw) % ns by parity; that is only
-    // unambiguous when the slot's previous stage (g + mw - ns) belonged to the
-    // same warp, i.e. when ns is a multiple of mw (and ns > mw); otherwise it is
-    // switched off.  Odd ring depths measured faster than trimming to even.
+    // Two MMA warps take alternate stages and wait for a slot's fill by barrier
+    // parity.  That parity is unambiguous only if the warp has seen the slot's
+    // previous fill, i.e. if the slot's previous stage (g - ns) was its own: ns
+    // even.  (With an odd ns a warp could take the slot's previous fill, still in
+    // flight behind a later one, for its own.)  The same holds for the MMA warps'
+    // look-ahead test of slot (g + mw) % ns.
+    if (mw == 2 && (ns & 1) && ns > 2) --ns;
+    if (mw == 2 && ns < 2) mw = 1;  // (one slot: a single MMA warp)
     g.lookahead = (ns % mw == 0 && ns > mw) ? 1 : 0;
     // With one MMA warp (wide route tiles) the scale-layout warp also copies each
     // stage's scale factors to TMEM, so the MMA warp issues MMAs only (measured:
