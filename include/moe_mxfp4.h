@@ -250,6 +250,46 @@ typedef struct {
 moe_status_t moe_mxfp4_get_plan(int T, int d_model, int d_inter, int E, int topk,
                                 moe_mxfp4_plan_t* plan);
 
+/* Launch geometry of the fused GEMM kernel for a shape (diagnostics and tests;
+ * it follows moe_mxfp4_set_tuning like the forward call).  Host-only; touches
+ * no device.  Returns a shape/argument status like the forward call.
+ * Properties every configuration keeps (the kernel checks the first three
+ * itself and reports a violation in the status word instead of running):
+ *   acc_bufs * acc_cols <= sf_col0, sf_col0 + num_stages * sf_cols <= tmem_cols
+ *   <= 512 (tensor-memory columns: accumulators, then each slot's scale factors);
+ *   acc_bufs >= epi_groups (an epilogue group waits for its item's buffer by
+ *   barrier parity, which is unambiguous only if the buffer's previous use has
+ *   completed; the group's own previous item, completed, implies that when there
+ *   are at least as many buffers as groups, since each MMA warp's operations
+ *   complete in issue order);
+ *   smem_bytes <= smem_limit;
+ *   mma_warps == 2 (alternate stages) implies an even num_stages (a warp waits
+ *   for a slot's fill by barrier parity, so it must have seen the slot's
+ *   previous fill: that stage must be its own). */
+typedef struct {
+    int tile_rows;          /* routes per route tile (the MMA's N)                          */
+    int stage1_k;           /* K elements per pipeline stage of the gate_up GEMM            */
+    int stage2_k;           /* K elements per pipeline stage of the down GEMM                */
+    int stage2_blocks;      /* 128-row weight blocks per down-GEMM work item                 */
+    int num_stages;         /* shared-memory ring slots                                     */
+    int mma_warps;          /* MMA-issuing warps (2: they take alternate stages)            */
+    int acc_bufs;           /* tensor-memory accumulator buffers                             */
+    int epi_groups;         /* epilogue groups of four warps                                  */
+    int sf_by_layout_warp;  /* the scale-layout warp copies the scale factors to TMEM too   */
+    int wide_sf;            /* two-chunk scale-factor copies from staging buffers            */
+    int lookahead;          /* MMA warps copy the next stage's scale factors early          */
+    unsigned slot_bytes;    /* bytes per ring slot                                           */
+    unsigned smem_bytes;    /* dynamic shared memory per CTA                                  */
+    unsigned smem_limit;    /* the kernel's dynamic shared-memory limit                       */
+    unsigned acc_cols;      /* TMEM columns per accumulator buffer                            */
+    unsigned sf_col0;       /* first TMEM column of the per-slot scale-factor regions         */
+    unsigned sf_cols;       /* TMEM scale-factor columns per ring slot                        */
+    unsigned tmem_cols;     /* TMEM columns allocated                                        */
+} moe_mxfp4_gemm_config_t;
+
+moe_status_t moe_mxfp4_get_gemm_config(int T, int d_model, int d_inter, int E, int topk,
+                                       moe_mxfp4_gemm_config_t* cfg);
+
 /* Workspace bytes and layout of the bf16-activation forward (regions a1b, a2b
  * instead of a1q .. a2s; bf16_act = 1). */
 size_t moe_mxfp4_workspace_size_w4a16(int T, int d_model, int d_inter, int E, int topk);

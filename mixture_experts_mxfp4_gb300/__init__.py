@@ -42,6 +42,7 @@ EXPORTS = [
     "moe_mxfp4_status_string",
     "moe_mxfp4_last_device_status",
     "moe_mxfp4_get_plan",
+    "moe_mxfp4_get_gemm_config",
     "moe_mxfp4_version",
     "moe_mxfp4_num_kernels",
     "moe_mxfp4_set_kernel_timing",
@@ -93,6 +94,18 @@ class Plan(ctypes.Structure):
         return int(self.offset[i]), int(self.bytes[i])
 
 
+class GemmConfig(ctypes.Structure):
+    """moe_mxfp4_gemm_config_t: launch geometry of the fused GEMM kernel."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "tile_rows", "stage1_k", "stage2_k", "stage2_blocks", "num_stages", "mma_warps", "acc_bufs",
+        "epi_groups", "sf_by_layout_warp", "wide_sf", "lookahead")] + \
+        [(n, ctypes.c_uint) for n in (
+            "slot_bytes", "smem_bytes", "smem_limit", "acc_cols", "sf_col0", "sf_cols", "tmem_cols")]
+
+    def as_dict(self):
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
 _lib = None
 
 
@@ -120,6 +133,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_last_device_status.argtypes = [P]
     lib.moe_mxfp4_get_plan.restype = i
     lib.moe_mxfp4_get_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+    lib.moe_mxfp4_get_gemm_config.restype = i
+    lib.moe_mxfp4_get_gemm_config.argtypes = [i, i, i, i, i, ctypes.POINTER(GemmConfig)]
     lib.moe_mxfp4_get_plan_w4a16.restype = i
     lib.moe_mxfp4_get_plan_w4a16.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
     lib.moe_mxfp4_workspace_size_w4a16.restype = ctypes.c_size_t
@@ -170,6 +185,14 @@ def get_plan(T, d_model, d_inter, E, topk) -> Plan:
     _check(load_library().moe_mxfp4_get_plan(T, d_model, d_inter, E, topk, ctypes.byref(pl)),
            "moe_mxfp4_get_plan")
     return pl
+
+
+def gemm_config(T, d_model, d_inter, E, topk) -> GemmConfig:
+    """Launch geometry of the fused GEMM kernel for this shape (host only)."""
+    cfg = GemmConfig()
+    _check(load_library().moe_mxfp4_get_gemm_config(T, d_model, d_inter, E, topk, ctypes.byref(cfg)),
+           "moe_mxfp4_get_gemm_config")
+    return cfg
 
 
 def get_plan_w4a16(T, d_model, d_inter, E, topk) -> Plan:

@@ -896,6 +896,35 @@ int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk) {
     return (long long)T * topk >= kRouteMultiMin ? 6 : 4;  // routing in three launches
 }
 
+moe_status_t moe_mxfp4_get_gemm_config(int T, int d_model, int d_inter, int E, int topk,
+                                       moe_mxfp4_gemm_config_t* cfg) {
+    if (!cfg) return MOE_ERR_INVALID_ARG;
+    const moe_status_t st = validate_shape(T, d_model, d_inter, E, topk);
+    if (st != MOE_OK) return st;
+    moe_mxfp4_plan_t pl;
+    moe::GemmParams gp;
+    shape_geometry(T, d_model, d_inter, E, topk, &pl, &gp);
+    cfg->tile_rows = gp.tile_rows;
+    cfg->stage1_k = gp.g[0].kstage_elems;
+    cfg->stage2_k = gp.g[1].kstage_elems;
+    cfg->stage2_blocks = gp.g[1].mblocks;
+    cfg->num_stages = gp.num_stages;
+    cfg->mma_warps = gp.mma_warps;
+    cfg->acc_bufs = gp.acc_bufs;
+    cfg->epi_groups = gp.epi_groups;
+    cfg->sf_by_layout_warp = gp.sf_by_layout_warp;
+    cfg->wide_sf = gp.wide_sf;
+    cfg->lookahead = gp.lookahead;
+    cfg->slot_bytes = gp.slot_bytes;
+    cfg->smem_bytes = gp.smem_bytes;
+    cfg->smem_limit = (unsigned)kGemmSmemLimit;
+    cfg->acc_cols = gp.acc_cols;
+    cfg->sf_col0 = gp.sf_col0;
+    cfg->sf_cols = gp.sf_cols;
+    cfg->tmem_cols = gp.tmem_cols;
+    return MOE_OK;
+}
+
 moe_status_t moe_mxfp4_get_plan_w4a16(int T, int d_model, int d_inter, int E, int topk,
                                       moe_mxfp4_plan_t* plan) {
     if (!plan) return MOE_ERR_INVALID_ARG;
