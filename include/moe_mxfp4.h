@@ -59,8 +59,14 @@ typedef enum {
 
 /*
  * Supported shapes: T >= 0; 1 <= topk <= 16; 1 <= E <= 1024;
- * d_model and d_inter each 128, 256 or a multiple of 512;
- * d_model a multiple of 128 and d_inter a multiple of 64 (both hold for the above).
+ * d_model a multiple of 128 and d_inter a multiple of 64 (MOE_ERR_UNSUPPORTED_SHAPE
+ * otherwise).  The kernels run each width at 128, 256 or a multiple of 512: a
+ * width that is none of these runs at the next one.  Such a call adds one launch
+ * that copies the weight scales into the workspace (region MOE_WS_WSCALE, rows
+ * padded to 16-byte multiples for the tensor-memory-access copies) and zeroes
+ * the intermediate's extra columns; the kernels read the weights' missing
+ * columns as zeros.  The bf16-activation forward takes only the widths 128, 256
+ * and multiples of 512.
  * Every pointer 16-byte aligned.
  */
 
@@ -118,8 +124,8 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const void* w13, const void* 
  * The result is the forward of the logical problem: the weights' first d_inter
  * gate rows, first d_inter up rows, first d_model columns (w13) and the first
  * d_model rows and d_inter columns (w2).  d_model, d_inter: multiples of 32 (one
- * scale block), at most the padded sizes; the padded sizes as for
- * moe_mxfp4_forward.  The padding may hold any e2m1 codes but no scale byte 255
+ * scale block), at most the padded sizes; the padded sizes 128, 256 or a
+ * multiple of 512 (where they differ from d_model, d_inter).  The padding may hold any e2m1 codes but no scale byte 255
  * (NaN): it is multiplied by zeros.  The workspace is that of the padded shape
  * (moe_mxfp4_workspace_size(T, d_model_pad, d_inter_pad, E, topk)).
  * moe_mxfp4_forward(..., d_model, d_inter, ...) is this call with no padding.
@@ -209,7 +215,11 @@ moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream
 
 /* ------------------------------------------------------------------ inspection */
 
-/* Workspace regions, for tests and tools that inspect intermediate results. */
+/* Workspace regions, for tests and tools that inspect intermediate results.
+ * Rows of the activation regions use the widths the kernels run at
+ * (d_model_run, d_inter_run of the plan: the call's widths where they are 128,
+ * 256 or a multiple of 512, else the next such width; the extra columns hold
+ * zeros). */
 typedef enum {
     MOE_WS_STATUS = 0,      /* u32 [1024]: [0] error bits; [15], [16], [17], [512..1024) the single-launch path's ready word, quantisation count, exit count and route-tile counters (zero between calls) */
     MOE_WS_COUNTERS = 1,    /* u32 [max_tiles]: finished stage-1 feature tiles per route tile (multi-kernel path; zeroed per call) */
@@ -220,15 +230,16 @@ typedef enum {
     MOE_WS_ROUTE_POS = 6,   /* i32 [T*topk]: slot of each route, -1 for ids outside [0, E)    */
     MOE_WS_NUM_VALID = 7,   /* i32 [4]: padded length, valid routes, tiles, 0                 */
     MOE_WS_TILES = 8,       /* i32 [cap/block_m][4]: {expert, first slot, rows, 0}            */
-    MOE_WS_A1Q = 9,         /* u8 [cap][d_model/2]: quantised hidden row of each slot's token */
+    MOE_WS_A1Q = 9,         /* u8 [cap][d_model_run/2]: quantised hidden row of each slot's token */
     MOE_WS_A1S = 10,        /* u8 [cap][a1s_stride]: its e8m0 scales                          */
-    MOE_WS_A2Q = 11,        /* u8 [cap][d_inter/2]: quantised SwiGLU output of each slot      */
+    MOE_WS_A2Q = 11,        /* u8 [cap][d_inter_run/2]: quantised SwiGLU output of each slot  */
     MOE_WS_A2S = 12,        /* u8 [cap][a2s_stride]: its e8m0 scales                          */
-    MOE_WS_P = 13,          /* f32 [T*topk][d_model]: w[t,k] * stage-2 output, by route id    */
+    MOE_WS_P = 13,          /* f32 [T*topk][d_model_run]: w[t,k] * stage-2 output, by route id */
     MOE_WS_PARTIAL = 14,    /* unused (0 bytes): no K split of stage 1                        */
     MOE_WS_A1B = 15,        /* bf16 [cap][d_model]: hidden row of each slot's token (bf16-activation plan only) */
     MOE_WS_A2B = 16,        /* bf16 [cap][d_inter]: bf16 SwiGLU output of each slot (bf16-activation plan only) */
-    MOE_WS_NUM_REGIONS = 17
+    MOE_WS_WSCALE = 17,     /* u8: the weight scales with rows of d_model_run/32 (w13_scale) and d_inter_run/32 (w2_scale) bytes, the extra bytes 127; only where a width is run wider (else 0 bytes) */
+    MOE_WS_NUM_REGIONS = 18
 } moe_ws_region_t;
 
 typedef struct {
@@ -240,6 +251,8 @@ typedef struct {
     int stage1_splits;  /* K splits of the stage-1 GEMM (1)                              */
     int max_tiles;      /* capacity of MOE_WS_TILES                                      */
     int bf16_act;       /* 1: layout of the bf16-activation forward (a1q..a2s empty, a1b/a2b used) */
+    int d_model_run;    /* width the kernels run d_model at (see the regions above)        */
+    int d_inter_run;    /* width the kernels run d_inter at                                 */
     size_t offset[MOE_WS_NUM_REGIONS]; /* byte offset of each region in the workspace     */
     size_t bytes[MOE_WS_NUM_REGIONS];  /* byte size of each region                        */
     size_t workspace_bytes;            /* total (== moe_mxfp4_workspace_size)              */

@@ -32,7 +32,7 @@ MOE_OK = 0
 
 REGIONS = ["status", "counters", "sorted_ids", "sorted_w", "block_expert", "seg_start",
            "route_pos", "num_valid", "tiles", "a1q", "a1s", "a2q", "a2s", "P", "partial",
-           "a1b", "a2b"]
+           "a1b", "a2b", "wscale"]
 
 # Exported C symbols (kept in step with include/moe_mxfp4.h).
 EXPORTS = [
@@ -84,6 +84,8 @@ class Plan(ctypes.Structure):
         ("stage1_splits", ctypes.c_int),
         ("max_tiles", ctypes.c_int),
         ("bf16_act", ctypes.c_int),
+        ("d_model_run", ctypes.c_int),
+        ("d_inter_run", ctypes.c_int),
         ("offset", ctypes.c_size_t * len(REGIONS)),
         ("bytes", ctypes.c_size_t * len(REGIONS)),
         ("workspace_bytes", ctypes.c_size_t),

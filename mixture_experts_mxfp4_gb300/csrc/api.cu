@@ -79,12 +79,28 @@ void* g_last_ws[kMaxDevices];
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Contraction widths the GEMM kernels take as they are: one stage of 128 or 256
+// elements, or stages of 512.
 bool supported_k(int k) { return k == 128 || k == 256 || (k > 0 && k % 512 == 0); }
+
+// Width the kernels run a width k at: k itself where supported, else the next
+// supported width (its extra columns are zero in the activations and read as
+// zero from the weights).
+int stored_k(int k) {
+    if (supported_k(k)) return k;
+    if (k < 128) return 128;
+    if (k < 256) return 256;
+    return (int)round_up((size_t)k, 512);
+}
+
+// Weights of widths the kernels do not run at natively (d_model a multiple of
+// 128, d_inter of 64, either not a supported width).
+bool widened(int D, int I) { return !supported_k(D) || !supported_k(I); }
 
 moe_status_t validate_shape(int T, int D, int I, int E, int K) {
     if (T < 0 || E < 1 || E > 1024 || K < 1 || K > 16) return MOE_ERR_INVALID_ARG;
     if (D <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
-    if (!supported_k(D) || !supported_k(I)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (D % 128 != 0 || I % 64 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((long long)T * K > (1LL << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
@@ -108,8 +124,13 @@ int choose_tile_rows(int T, int E, int K) {
 
 // bf16_act: layout of the bf16-activation forward (bf16 a1/a2 rows instead of
 // the MXFP4 codes and scales).
-void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, bool bf16_act = false) {
+// D, I: the widths of the weight tensors; the workspace rows use the widths the
+// kernels run at (stored_k).
+void fill_plan(int T, int Dw, int Iw, int E, int K, moe_mxfp4_plan_t* pl, bool bf16_act = false) {
     memset(pl, 0, sizeof(*pl));
+    const int D = stored_k(Dw), I = stored_k(Iw);
+    pl->d_model_run = D;
+    pl->d_inter_run = I;
     const long long R = (long long)T * K;
     const long long used = R < E ? R : E;
     long long cap = R + used * (kBlockM - 1);
@@ -141,6 +162,9 @@ void fill_plan(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, bool bf1
     b[MOE_WS_PARTIAL] = 0;  // (no K split)
     b[MOE_WS_A1B] = 0;
     b[MOE_WS_A2B] = 0;
+    // weight scales repacked to rows of D/32 and I/32 bytes (widths run wider)
+    b[MOE_WS_WSCALE] = widened(Dw, Iw) ? round_up((size_t)E * 2 * Iw * (D / 32), kAlign) + (size_t)E * Dw * (I / 32)
+                                        : 0;
     if (bf16_act) {
         pl->bf16_act = 1;
         b[MOE_WS_A1Q] = b[MOE_WS_A1S] = b[MOE_WS_A2Q] = b[MOE_WS_A2S] = 0;
@@ -258,6 +282,25 @@ bool make_operand_map(CUtensorMap* m, const void* base, uint64_t rows, int Kc, i
     return make_map_nd(m, base, 3, dims, strides, box, swz);
 }
 
+// Weight map for weights narrower than the width the kernels run at: rows of
+// Kw/2 bytes, one K box (kb bytes) per copy, the columns past the row read as
+// zeros (the copy's out-of-bounds fill).  halves = 2 as for make_operand_map.
+bool make_kbox_map(CUtensorMap* m, const void* base, uint64_t rows, int Kw, int kb, int box_rows,
+                   int halves, uint64_t half_stride) {
+    const uint64_t row_bytes = (uint64_t)Kw / 2;
+    const CUtensorMapSwizzle swz = kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (halves > 1) {
+        const uint64_t dims[3] = {row_bytes, rows, (uint64_t)halves};
+        const uint64_t strides[2] = {row_bytes, half_stride};
+        const uint32_t box[3] = {(uint32_t)kb, (uint32_t)box_rows, (uint32_t)halves};
+        return make_map_nd(m, base, 3, dims, strides, box, swz);
+    }
+    const uint64_t dims[2] = {row_bytes, rows};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {(uint32_t)kb, (uint32_t)box_rows};
+    return make_map_nd(m, base, 2, dims, strides, box, swz);
+}
+
 // Weight-scale map: [rows][S] e8m0 bytes; S >= 16 read 16 bytes per stage, S < 16
 // read through a [rows*S/16][16] view so that one box holds box_rows whole rows.
 // With halves = 2 a third dimension adds the rows `half_rows` further (w13 up rows).
@@ -311,12 +354,15 @@ uint32_t stage_geometry(StageGeom& q, int Kc, int tile_rows, int mblocks) {
 // hold either stage's layout.  Narrow route tiles (decode) use two MMA-issuing
 // warps: a single stream of scale-factor copies and narrow MMAs leaves the
 // tensor pipe idle between instructions, and a second stream fills it.
-void gemm_geometry(GemmParams& g, int D, int I, int tile_rows, int mblocks2, int sf_copies) {
+// D, I: the widths the kernels run at; Dw, Iw: the weights' (the feature tiles
+// cover those: the gate_up GEMM's outputs past Iw, which the down GEMM multiplies
+// by zero weight columns, are zeroed before the call instead).
+void gemm_geometry(GemmParams& g, int D, int I, int Dw, int Iw, int tile_rows, int mblocks2, int sf_copies) {
     g.tile_rows = tile_rows;
     const uint32_t b1 = stage_geometry(g.g[0], D, tile_rows, 1);
     const uint32_t b2 = stage_geometry(g.g[1], I, tile_rows, mblocks2);
-    g.g[0].n_ftiles = I / 64;
-    g.g[1].n_ftiles = D / (128 * mblocks2);
+    g.g[0].n_ftiles = Iw / 64;
+    g.g[1].n_ftiles = Dw / (128 * mblocks2);
     g.slot_bytes = b1 > b2 ? b1 : b2;
     // epilogue groups: three for 128-route tiles whose stage-2 items are a single
     // stage (the stage-2 epilogue bounds those, see kMaxEpiGroups), else two
@@ -548,6 +594,8 @@ struct LaunchState {
     CUtensorMap maps[8];  // stage-1 A, SA, B, SB, stage-2 A, SA, B, SB
     moe::GemmParams gp;
     moe_mxfp4_plan_t pl;
+    void* wscale13;  // repacked weight scales (weights narrower than the run widths)
+    void* wscale2;
     const void* key_ptr[5];
     int key_shape[7];  // T, D, I, E, K, forced tile width, forced copy scheme
     bool valid;
@@ -558,15 +606,18 @@ LaunchState g_cache[kMaxDevices][kCacheWays];
 int g_cache_next[kMaxDevices];
 
 // Plan and GEMM geometry of a shape (no device pointers).
+// D, I: the widths of the weight tensors.
 void shape_geometry(int T, int D, int I, int E, int K, moe_mxfp4_plan_t* pl, GemmParams* gp) {
     fill_plan(T, D, I, E, K, pl);
     memset(gp, 0, sizeof(*gp));
-    gp->D = D; gp->I = I; gp->E = E; gp->K = K; gp->R = T * K;
+    gp->D = stored_k(D); gp->I = stored_k(I); gp->E = E; gp->K = K; gp->R = T * K;
+    gp->Dw = D; gp->Iw = I;
+    gp->kt_boxes = widened(D, I) ? 1 : 0;
     gp->a1s_stride = pl->a1s_stride;
     gp->a2s_stride = pl->a2s_stride;
     // stage 2 on narrow tiles: two 128-row blocks of w2 per item share the route tile
     const int mb2 = (pl->tile_rows <= 64 && D % 256 == 0) ? 2 : 1;
-    gemm_geometry(*gp, D, I, pl->tile_rows, mb2, g_force_sf_copies.load(std::memory_order_relaxed));
+    gemm_geometry(*gp, gp->D, gp->I, D, I, pl->tile_rows, mb2, g_force_sf_copies.load(std::memory_order_relaxed));
 }
 
 // Whether a call of this shape routes and quantises inside the GEMM kernel under
@@ -598,17 +649,37 @@ bool build_state(LaunchState& st, const void* w13, const void* w13_scale, const 
     const int tr = pl.tile_rows;
     CUtensorMap* m = st.maps;
     bool ok = true;
+    // D, I: the weights' widths; Dr, Ir: the widths the kernels run at
+    const int Dr = gp.D, Ir = gp.I;
+    // weight scales the maps read: the caller's, or their copy with rows of Dr/32
+    // and Ir/32 bytes (made by the call's first launch)
+    const void* s13 = w13_scale;
+    const void* s2 = w2_scale;
+    st.wscale13 = st.wscale2 = nullptr;
+    if (gp.kt_boxes) {
+        uint8_t* wsc = static_cast<uint8_t*>(base) + pl.offset[MOE_WS_WSCALE];
+        s13 = wsc;
+        s2 = wsc + round_up((size_t)E * 2 * I * (Dr / 32), kAlign);
+        st.wscale13 = wsc;
+        st.wscale2 = const_cast<void*>(s2);
+    }
     // stage 1: A = 64 gate rows + the 64 up rows I rows further, both K-boxes of a stage
-    ok = ok && make_operand_map(&m[0], w13, (uint64_t)E * 2 * I, D, q1.kb, q1.nkt, 64, 2,
-                                (uint64_t)I * (D / 2));
-    ok = ok && make_scale_map(&m[1], w13_scale, (uint64_t)E * 2 * I, D / 32, 64, 2, (uint64_t)I);
-    ok = ok && make_operand_map(&m[2], ws.a1q, pl.cap, D, q1.kb, q1.nkt, tr, 1, 0);
+    if (gp.kt_boxes)
+        ok = ok && make_kbox_map(&m[0], w13, (uint64_t)E * 2 * I, D, q1.kb, 64, 2, (uint64_t)I * (D / 2));
+    else
+        ok = ok && make_operand_map(&m[0], w13, (uint64_t)E * 2 * I, D, q1.kb, q1.nkt, 64, 2,
+                                    (uint64_t)I * (D / 2));
+    ok = ok && make_scale_map(&m[1], s13, (uint64_t)E * 2 * I, Dr / 32, 64, 2, (uint64_t)I);
+    ok = ok && make_operand_map(&m[2], ws.a1q, pl.cap, Dr, q1.kb, q1.nkt, tr, 1, 0);
     ok = ok && make_map(&m[3], ws.a1s, pl.a1s_stride, pl.cap, pl.a1s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     // stage 2: A = 128 * mblocks rows of w2
-    ok = ok && make_operand_map(&m[4], w2, (uint64_t)E * D, I, q2.kb, q2.nkt, 128 * q2.mblocks, 1, 0);
-    ok = ok && make_scale_map(&m[5], w2_scale, (uint64_t)E * D, I / 32, 128 * q2.mblocks, 1, 0);
-    ok = ok && make_operand_map(&m[6], ws.a2q, pl.cap, I, q2.kb, q2.nkt, tr, 1, 0);
+    if (gp.kt_boxes)
+        ok = ok && make_kbox_map(&m[4], w2, (uint64_t)E * D, I, q2.kb, 128 * q2.mblocks, 1, 0);
+    else
+        ok = ok && make_operand_map(&m[4], w2, (uint64_t)E * D, I, q2.kb, q2.nkt, 128 * q2.mblocks, 1, 0);
+    ok = ok && make_scale_map(&m[5], s2, (uint64_t)E * D, Ir / 32, 128 * q2.mblocks, 1, 0);
+    ok = ok && make_operand_map(&m[6], ws.a2q, pl.cap, Ir, q2.kb, q2.nkt, tr, 1, 0);
     ok = ok && make_map(&m[7], ws.a2s, pl.a2s_stride, pl.cap, pl.a2s_stride, 16, tr,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     return ok;
@@ -682,8 +753,18 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
         std::lock_guard<std::mutex> lk(g_mu);
         g_last_ws[dev] = base;
     }
-    const CallRange call_range(Dl != D || Il != I ? "padded" : "mxfp4", T, D, I, E, K,
-                               front ? 2 : (T * K >= kRouteMultiMin ? 6 : 4));
+    // D, I: the weights' widths; Dr, Ir: the widths the kernels run at
+    const int Dr = gp.D, Ir = gp.I;
+    const int widen = gp.kt_boxes ? 1 : 0;
+    const CallRange call_range(widen ? "run wider" : Dl != D || Il != I ? "padded" : "mxfp4", T, D, I, E, K,
+                               widen + (front ? 2 : (T * K >= kRouteMultiMin ? 6 : 4)));
+    if (widen) {
+        const LaunchRange r("widen");
+        if (launch_widen(w13_scale, st->wscale13, (long)E * 2 * I, D / 32, Dr / 32, w2_scale, st->wscale2,
+                         (long)E * D, I / 32, Ir / 32, ws, Ir / 2, I / 2, pl.a2s_stride, I / 32, pl.cap,
+                         sms * 4, stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     mark(0);
     if (!front) {
         const LaunchRange r("route");
@@ -694,7 +775,7 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     mark(1);
     if (!front) {
         const LaunchRange r("quant");
-        if (launch_quant(hidden, T, K, D, Dl, pl.a1s_stride, pl.cap, ws, stream) != cudaSuccess)
+        if (launch_quant(hidden, T, K, Dr, Dl, pl.a1s_stride, pl.cap, ws, stream) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
     mark(2);
@@ -705,7 +786,7 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
     mark(3);
     {
         const LaunchRange r("topk_sum");
-        if (launch_reduce(T, K, D, Dl, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
+        if (launch_reduce(T, K, Dr, Dl, out, ws, stream) != cudaSuccess) return MOE_ERR_CUDA;
     }
     mark(4);
     if (timed) {
@@ -850,6 +931,8 @@ moe_status_t moe_mxfp4_forward_padded(const void* hidden, const void* w13, const
     moe_status_t st = validate_forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
                                        topk_weights, out, T, D, I, E, K);
     if (st == MOE_OK) st = validate_padded(D, I, d_model, d_inter);
+    // padded storage: widths the kernels run at as they are
+    if (st == MOE_OK && (d_model != D || d_inter != I) && widened(D, I)) st = MOE_ERR_UNSUPPORTED_SHAPE;
     if (st != MOE_OK || T == 0) return st;
     const size_t need = plan_workspace_bytes(T, D, I, E, K);
     int dev = 0;
@@ -892,8 +975,9 @@ int moe_mxfp4_call_launches(int T, int d_model, int d_inter, int E, int topk) {
     moe_mxfp4_plan_t pl;
     moe::GemmParams gp;
     shape_geometry(T, d_model, d_inter, E, topk, &pl, &gp);
-    if (single_launch_for(dev, T, E, topk, gp)) return 2;
-    return (long long)T * topk >= kRouteMultiMin ? 6 : 4;  // routing in three launches
+    const int widen = gp.kt_boxes ? 1 : 0;  // the weight-scale copy first
+    if (single_launch_for(dev, T, E, topk, gp)) return widen + 2;
+    return widen + ((long long)T * topk >= kRouteMultiMin ? 6 : 4);  // routing in three launches
 }
 
 moe_status_t moe_mxfp4_get_gemm_config(int T, int d_model, int d_inter, int E, int topk,
@@ -929,6 +1013,7 @@ moe_status_t moe_mxfp4_get_plan_w4a16(int T, int d_model, int d_inter, int E, in
                                       moe_mxfp4_plan_t* plan) {
     if (!plan) return MOE_ERR_INVALID_ARG;
     moe_status_t st = validate_shape(T, d_model, d_inter, E, topk);
+    if (st == MOE_OK && widened(d_model, d_inter)) st = MOE_ERR_UNSUPPORTED_SHAPE;  // native widths only
     if (st != MOE_OK) return st;
     fill_plan(T, d_model, d_inter, E, topk, plan, true);
     return MOE_OK;
@@ -948,6 +1033,7 @@ moe_status_t moe_mxfp4_forward_w4a16(const void* hidden, const void* w13, const 
     const int D = d_model, I = d_inter, K = topk;
     moe_status_t st = validate_forward(hidden, w13, w13_scale, w2, w2_scale, topk_ids,
                                        topk_weights, out, T, D, I, E, K);
+    if (st == MOE_OK && widened(D, I)) st = MOE_ERR_UNSUPPORTED_SHAPE;  // native widths only
     if (st != MOE_OK || T == 0) return st;
     const size_t need = moe_mxfp4_workspace_size_w4a16(T, D, I, E, K);
     int dev = 0;

@@ -742,8 +742,10 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                         }
                         uint8_t* st = smem + (size_t)s * p.slot_bytes;
                         const int kt0 = ks * q.nkt;  // first K box of the stage
-                        const int rg = phs == 0 ? x.e * 2 * p.I + x.f * 64
-                                                : x.e * p.D + x.f * 128 * MBp;
+                        // first weight row (rows of the weight tensors: 2 Iw per expert
+                        // in w13, Dw in w2)
+                        const int rg = phs == 0 ? x.e * 2 * p.Iw + x.f * 64
+                                                : x.e * p.Dw + x.f * 128 * MBp;
                         // weight scales, then the weight tile: they do not depend on stage 1
                         mbar_arrive_expect_tx(&sfull[s], arows * q.sr_a + (uint32_t)p.tile_rows * 16u);
                         mbar_arrive_expect_tx(&full[s], (arows + (uint32_t)p.tile_rows) * kbytes_stage);
@@ -753,13 +755,28 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                                 tma_load_3d(st + q.off_sa, mSA, 0, rg / (16 / q.sr_a), 0, &sfull[s]);
                             else
                                 tma_load_3d(st + q.off_sa, mSA, ks * 16, rg, 0, &sfull[s]);
-                            tma_load_4d_hint(st, mA, 0, rg, 0, kt0, &full[s], pol_w);
+                            if (p.kt_boxes) {
+                                // weights narrower than D: one copy per K box (each box
+                                // 128 rows, gate then up), zeros past the row
+                                for (int kt = 0; kt < q.nkt; ++kt)
+                                    tma_load_3d_hint(st + (size_t)kt * 128u * q.kb, mA, (kt0 + kt) * q.kb, rg, 0,
+                                                     &full[s], pol_w);
+                            } else {
+                                tma_load_4d_hint(st, mA, 0, rg, 0, kt0, &full[s], pol_w);
+                            }
                         } else {
                             if (q.a_scale_small)
                                 tma_load_2d(st + q.off_sa, mSA, 0, rg / (16 / q.sr_a), &sfull[s]);
                             else
                                 tma_load_2d(st + q.off_sa, mSA, ks * 16, rg, &sfull[s]);
-                            tma_load_3d_hint(st, mA, 0, rg, kt0, &full[s], pol_w);
+                            if (p.kt_boxes) {
+                                // weights narrower than I: one copy per K box of arows rows
+                                for (int kt = 0; kt < q.nkt; ++kt)
+                                    tma_load_2d_hint(st + (size_t)kt * arows * q.kb, mA, (kt0 + kt) * q.kb, rg,
+                                                     &full[s], pol_w);
+                            } else {
+                                tma_load_3d_hint(st, mA, 0, rg, kt0, &full[s], pol_w);
+                            }
                             const bool cached = x.tile < kTileCache;
                             if (!cached || !((tready[x.tile >> 5] >> (x.tile & 31)) & 1u)) {
                                 // the route tile's stage-1 output: every feature tile written

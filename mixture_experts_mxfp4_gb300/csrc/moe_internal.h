@@ -54,8 +54,12 @@ struct StageGeom {
 // its stage-2 items, through one shared-memory ring.
 struct GemmParams {
     WsPtrs ws;
-    int D, I, E, K, R;  // D, I: stored (padded) sizes
-    int Dl, Il;         // logical d_model, d_inter (multiples of 32, <= D, I)
+    int D, I, E, K, R;  // D, I: widths the kernels run at (native widths, >= Dw, Iw)
+    int Dl, Il;         // logical d_model, d_inter (multiples of 32, <= Dw, Iw)
+    int Dw, Iw;         // widths of the weight tensors: w13 [E][2 Iw][Dw/2], w2 [E][Dw][Iw/2]
+    int kt_boxes;       // weights narrower than D or I: one copy per K box of a stage, the
+                        // columns past Dw / Iw zero-filled by the copy (maps of the weights'
+                        // own widths); weight scales repacked to D/32, I/32 bytes per row
     int tile_rows;      // maximum MMA N (routes per tile), multiple of 16, <= 128
     StageGeom g[2];     // stage 1, stage 2
     int num_stages;     // shared-memory ring depth
@@ -163,6 +167,13 @@ moe_status_t forward_on_workspace(const void* hidden, const void* w13, const voi
                                   int K, int Dl, int Il, void* base, int dev, cudaStream_t stream);
 
 cudaError_t launch_check_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t stream);
+// Weights narrower than the widths the kernels run at: weight-scale rows of S
+// bytes copied to rows of Sp bytes (extra bytes 127), and the intermediate's
+// columns past the weights' width zeroed (a2q bytes [q_from, q_row), a2s bytes
+// [s_from, s_row) of each of the cap slots).
+cudaError_t launch_widen(const void* w13_scale, void* d13, long rows13, int S13, int Sp13, const void* w2_scale,
+                         void* d2, long rows2, int S2, int Sp2, const WsPtrs& ws, int q_row, int q_from,
+                         int s_row, int s_from, long cap, int grid, cudaStream_t stream);
 cudaError_t launch_route(const int32_t* topk_ids, const float* topk_w, int T, int K, int E,
                          int tile_rows, int cap, int n_counters, const WsPtrs& ws,
                          cudaStream_t stream);

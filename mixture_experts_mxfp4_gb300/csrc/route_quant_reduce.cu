@@ -548,6 +548,52 @@ cudaError_t launch_reduce(int T, int K, int D, int Dl, void* out, const WsPtrs& 
                               D, Dl, static_cast<const float*>(ws.P), reinterpret_cast<__nv_bfloat16*>(out));
 }
 
+// ============================================================== run-width copies
+//
+// A call whose weight widths the GEMM kernels do not run at as they are (they
+// run d_model, d_inter at the next width of 128, 256 or a multiple of 512): one
+// warp per row copies each weight-scale row of S bytes into a row of Sp bytes (a
+// multiple of 16, as the tensor-memory-access copies need), the extra bytes 127
+// (a scale of 1: the matching weight columns read as zeros), and sets to zero
+// the quantised intermediate's columns that the gate_up GEMM does not write
+// (codes from byte q_from and scale bytes from s_from, in every slot's row),
+// which the down GEMM multiplies by those zero weight columns.
+
+__global__ void __launch_bounds__(256) moe_widen_kernel(const uint8_t* __restrict__ s13, uint8_t* __restrict__ d13,
+                                                        long rows13, int S13, int Sp13,
+                                                        const uint8_t* __restrict__ s2, uint8_t* __restrict__ d2,
+                                                        long rows2, int S2, int Sp2, uint8_t* __restrict__ a2q,
+                                                        int q_row, int q_from, uint8_t* __restrict__ a2s,
+                                                        int s_row, int s_from, long cap) {
+    const int lane = threadIdx.x & 31;
+    const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+    const long nrows = rows13 + rows2 + 2 * cap;
+    for (long r = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < nrows; r += nwarps) {
+        if (r < rows13) {
+            for (int c = lane; c < Sp13; c += 32) d13[r * Sp13 + c] = c < S13 ? s13[r * S13 + c] : (uint8_t)127;
+        } else if (r < rows13 + rows2) {
+            const long k = r - rows13;
+            for (int c = lane; c < Sp2; c += 32) d2[k * Sp2 + c] = c < S2 ? s2[k * S2 + c] : (uint8_t)127;
+        } else if (r < rows13 + rows2 + cap) {
+            const long k = r - rows13 - rows2;
+            for (int c = q_from + lane; c < q_row; c += 32) a2q[k * q_row + c] = 0;
+        } else {
+            const long k = r - rows13 - rows2 - cap;
+            for (int c = s_from + lane; c < s_row; c += 32) a2s[k * s_row + c] = 0;
+        }
+    }
+}
+
+cudaError_t launch_widen(const void* w13_scale, void* d13, long rows13, int S13, int Sp13, const void* w2_scale,
+                         void* d2, long rows2, int S2, int Sp2, const WsPtrs& ws, int q_row, int q_from,
+                         int s_row, int s_from, long cap, int grid, cudaStream_t stream) {
+    moe_widen_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(w13_scale), static_cast<uint8_t*>(d13), rows13, S13, Sp13,
+        static_cast<const uint8_t*>(w2_scale), static_cast<uint8_t*>(d2), rows2, S2, Sp2, ws.a2q, q_row, q_from,
+        ws.a2s, s_row, s_from, cap);
+    return cudaGetLastError();
+}
+
 // ============================================================== wait self-check
 //
 // One thread waits on an mbarrier that nothing arrives on, through the same

@@ -98,8 +98,8 @@ def test_validation_codes_without_device(lib):
     assert call(K=0) == 1
     assert call(K=17) == 1
     assert call(D=0) == 1
-    assert call(D=384) == 2      # not 128, 256 or a multiple of 512
-    assert call(I=192) == 2
+    assert call(D=320) == 2      # d_model not a multiple of 128
+    assert call(I=96) == 2       # d_inter not a multiple of 64
     assert call(D=1000) == 2
     assert call(T=0) == 0        # empty input: nothing to do
     nulls = list(args)
@@ -108,7 +108,7 @@ def test_validation_codes_without_device(lib):
     mis = list(args)
     mis[0] = good + 8
     assert call(ptrs=mis) == 3
-    assert moe.workspace_size(16, 384, 128, 9, 3) == 0
+    assert moe.workspace_size(16, 320, 128, 9, 3) == 0
     with pytest.raises(moe.MoeError):
         moe.get_plan(16, 256, 100, 9, 3)
     # workspace registration checks alignment before any device call
@@ -127,9 +127,41 @@ def test_padded_validation_codes_without_device(lib):
     assert call(D=200) == 2       # logical size not a multiple of 32
     assert call(I=16) == 2        # below one scale block
     assert call(D=288) == 1       # logical size above the stored one
-    assert call(Ip=192) == 2      # stored size not 128, 256 or a multiple of 512
+    assert call(Ip=192) == 2      # padded stored size not 128, 256 or a multiple of 512
+    assert call(Ip=160) == 2      # stored size not a multiple of 64
     assert call(T=0) == 0
     assert moe.call_launches(16, 255, 128, 9, 3) == -1
+
+
+@pytest.mark.parametrize("shape,run", [((16, 2944, 384, 16, 4), (3072, 512)),
+                                       ((200, 1152, 768, 8, 3), (1536, 1024)),
+                                       ((16, 384, 192, 9, 3), (512, 256)),
+                                       ((8, 128, 64, 4, 2), (128, 128)),
+                                       ((16, 7168, 256, 257, 9), (7168, 256))])
+def test_run_widths_in_the_plan(lib, shape, run):
+    """Widths that are not 128, 256 or a multiple of 512 run at the next such width:
+    the activation regions use it, and the weight scales get a region of rows of
+    the run widths' scale bytes (none for widths run as they are)."""
+    import mixture_experts_mxfp4_gb300 as moe
+
+    T, D, I, E, K = shape
+    Dr, Ir = run
+    pl = moe.get_plan(*shape)
+    assert (pl.d_model_run, pl.d_inter_run) == (Dr, Ir)
+    assert pl.region("a1q")[1] == pl.cap * Dr // 2 and pl.region("a2q")[1] == pl.cap * Ir // 2
+    assert pl.region("P")[1] == T * K * Dr * 4
+    assert pl.a1s_stride >= Dr // 32 and pl.a2s_stride >= Ir // 32
+    w13s = E * 2 * I * (Dr // 32)
+    expect = 0 if (Dr, Ir) == (D, I) else (w13s + 255) // 256 * 256 + E * D * (Ir // 32)
+    assert pl.region("wscale")[1] == expect
+    assert moe.workspace_size(*shape) == pl.workspace_bytes
+    c = moe.gemm_config(*shape)
+    assert Dr % c.stage1_k == 0 and Ir % c.stage2_k == 0
+    # the bf16-activation forward takes only widths it runs as they are
+    if (Dr, Ir) != (D, I):
+        with pytest.raises(moe.MoeError):
+            moe.get_plan_w4a16(*shape)
+        assert moe.load_library().moe_mxfp4_workspace_size_w4a16(*shape) == 0
 
 
 def test_w4a16_entry_and_plan_without_device(lib):

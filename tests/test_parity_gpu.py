@@ -415,6 +415,54 @@ def test_padded_dims(moe, launch_mode, T, D, I, Dp, Ip, E, K):
     check_out(out, ref)
 
 
+@pytest.mark.parametrize("T,D,I,E,K", [
+    (64, 2944, 384, 16, 4),    # both widths run wider (3072, 512)
+    (200, 1152, 768, 8, 3),    # d_model 9 x 128, d_inter 768 (1536, 1024), 128-route tiles
+    (16, 384, 192, 9, 3),      # widths below 512 (512, 256)
+    (8, 128, 64, 4, 2),        # d_inter of one 64-feature tile (128)
+    (24, 7168, 320, 33, 4),    # d_model as it is, d_inter run wider (512)
+])
+def test_widths_run_wider(moe, launch_mode, T, D, I, E, K):
+    """d_model a multiple of 128 and d_inter of 64 that are not 128, 256 or a
+    multiple of 512, with the weights in their own (unpadded) layout: against the
+    oracle on the same weights, routing and quantised hidden rows bit-exact, the
+    intermediate within one e2m1 step, the activations' extra columns zero, every
+    output row within the row bound; the call adds one launch."""
+    w = workloads.custom(T, D, I, E, K)
+    inp = workloads.make_inputs(w, seed=13)
+    m, t, out = run_gpu(moe, inp, w)
+    assert out.shape == (T, D)
+    pl = m.plan
+    Dr, Ir = pl.d_model_run, pl.d_inter_run
+    assert (Dr, Ir) != (D, I)
+    assert moe.call_launches(T, D, I, E, K) in (3, 5, 7)  # the weight-scale copy + 2, 4 or 6
+    npi = workloads.to_numpy(inp)
+    routing = oracle.route(npi["topk_ids"], npi["topk_weights"], E, 16, cap=pl.cap)
+    ref = oracle.forward(**npi, threads=_threads(), want_h=False)
+    cap = pl.cap
+    get = lambda name, dt, shape: m.region(name, dt, shape).cpu().numpy()
+    ws = {"sorted_ids": get("sorted_ids", torch.int32, (cap,)),
+          "sorted_w": get("sorted_w", torch.float32, (cap,)),
+          "block_expert": get("block_expert", torch.int32, (cap // 16,)),
+          "seg_start": get("seg_start", torch.int32, (E + 1,)),
+          "route_pos": get("route_pos", torch.int32, (T * K,)),
+          "num_valid": get("num_valid", torch.int32, (4,)),
+          "tiles": get("tiles", torch.int32, (pl.max_tiles, 4))}
+    check_routing(ws, routing, w, pl.tile_rows)
+    a1q = get("a1q", torch.uint8, (cap, Dr // 2))
+    a1s = get("a1s", torch.uint8, (cap, pl.a1s_stride))
+    a2q = get("a2q", torch.uint8, (cap, Ir // 2))
+    a2s = get("a2s", torch.uint8, (cap, pl.a2s_stride))
+    ws.update({"a1q": a1q[:, : D // 2], "a1s": a1s, "a2q": a2q[:, : I // 2], "a2s": a2s})
+    check_a1(ws, ref, routing, w)
+    check_a2(ws, ref, routing, w)
+    n = int(routing["num_valid"][0])
+    valid = routing["sorted_ids"][:n] < w.R
+    assert (a1q[:n][valid, D // 2:] == 0).all()
+    assert (a2q[:n][valid, I // 2:] == 0).all()
+    check_out(out, ref)
+
+
 def test_launch_modes_bitwise_identical(moe):
     """Single-launch mode reproduces the separate-kernel output and workspace
     routing arrays bit for bit (same routing order, same quantisation)."""

@@ -273,7 +273,8 @@ def test_fewer_buffers_than_groups_is_caught():
 
 SHAPES = [(16, 7168, 256, 257, 9), (128, 7168, 256, 257, 9), (512, 7168, 2048, 33, 9),
           (4096, 7168, 256, 257, 9), (256, 512, 256, 5, 3), (96, 1024, 512, 3, 2),
-          (16, 256, 128, 9, 3), (200, 2048, 1024, 4, 3), (8, 128, 128, 1, 1), (64, 1536, 1024, 64, 6)]
+          (16, 256, 128, 9, 3), (200, 2048, 1024, 4, 3), (8, 128, 128, 1, 1), (64, 1536, 1024, 64, 6),
+          (64, 2944, 384, 16, 4), (16, 384, 192, 9, 3)]
 
 
 def test_geometry_keeps_the_rules():
@@ -307,7 +308,7 @@ def test_geometry_keeps_the_rules():
             assert c.sf_col0 + c.num_stages * c.sf_cols <= c.tmem_cols <= 512, where
             assert c.tmem_cols >= 32 and c.tmem_cols & (c.tmem_cols - 1) == 0, where
             assert c.num_stages * c.slot_bytes <= c.smem_bytes <= c.smem_limit, where
-            T, D, I, E, K = shape
-            assert D % c.stage1_k == 0 and I % c.stage2_k == 0, where
+            pl = moe.get_plan(*shape)  # widths the kernels run at
+            assert pl.d_model_run % c.stage1_k == 0 and pl.d_inter_run % c.stage2_k == 0, where
     finally:
         moe.set_tuning(0, 0)
