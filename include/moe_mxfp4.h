@@ -238,7 +238,7 @@ typedef enum {
     MOE_WS_PARTIAL = 14,    /* unused (0 bytes): no K split of stage 1                        */
     MOE_WS_A1B = 15,        /* bf16 [cap][d_model]: hidden row of each slot's token (bf16-activation plan only) */
     MOE_WS_A2B = 16,        /* bf16 [cap][d_inter]: bf16 SwiGLU output of each slot (bf16-activation plan only) */
-    MOE_WS_WSCALE = 17,     /* u8: the weight scales with rows of d_model_run/32 (w13_scale) and d_inter_run/32 (w2_scale) bytes, the extra bytes 127; only where a width is run wider (else 0 bytes) */
+    MOE_WS_WSCALE = 17,     /* u8: the weight scales with rows of d_model_run/32 (w13_scale) and d_inter_run/32 (w2_scale, from the next 256-byte boundary) bytes, the extra bytes 127; only where a width is run wider (else 0 bytes) */
     MOE_WS_NUM_REGIONS = 18
 } moe_ws_region_t;
 
