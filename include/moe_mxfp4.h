@@ -213,6 +213,23 @@ moe_status_t moe_mxfp4_last_device_status(cudaStream_t stream);
  */
 moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream);
 
+/*
+ * The forward's last step on its own: the deterministic top-k sum of per-route
+ * rows (for an expert-parallel combine, where the rows come back from the ranks
+ * that own the experts).
+ *   out[t] = bf16( sum over k = 0 .. topk-1 with route_pos[t*topk+k] >= 0 of
+ *                  P[t*topk+k] ), fp32 adds in ascending k from zero, one rounding
+ *   P          f32  [T*topk, d_model], rows by route id (w[t,k] * W2[e] . a2 in the
+ *              forward; here whatever the caller computed)
+ *   route_pos  i32  [T*topk]: >= 0 where the route counts, < 0 where it does not
+ *   out        bf16 [T, d_model]; a token with no counted route gets a zero row
+ * Device memory (or mapped pinned host memory), 16-byte aligned; d_model a
+ * multiple of 128, 1 <= topk <= 16.  The same kernel and order as the forward.
+ * Asynchronous on `stream`; T == 0 enqueues nothing.
+ */
+moe_status_t moe_mxfp4_topk_sum(const float* P, const int32_t* route_pos, void* out, int T,
+                                int d_model, int topk, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ inspection */
 
 /* Workspace regions, for tests and tools that inspect intermediate results.

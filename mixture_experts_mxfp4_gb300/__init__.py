@@ -43,6 +43,7 @@ EXPORTS = [
     "moe_mxfp4_last_device_status",
     "moe_mxfp4_get_plan",
     "moe_mxfp4_get_gemm_config",
+    "moe_mxfp4_topk_sum",
     "moe_mxfp4_version",
     "moe_mxfp4_num_kernels",
     "moe_mxfp4_set_kernel_timing",
@@ -135,6 +136,8 @@ def load_library(path: str = LIB_PATH):
     lib.moe_mxfp4_last_device_status.argtypes = [P]
     lib.moe_mxfp4_get_plan.restype = i
     lib.moe_mxfp4_get_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(Plan)]
+    lib.moe_mxfp4_topk_sum.restype = i
+    lib.moe_mxfp4_topk_sum.argtypes = [P, P, P, i, i, i, P]
     lib.moe_mxfp4_get_gemm_config.restype = i
     lib.moe_mxfp4_get_gemm_config.argtypes = [i, i, i, i, i, ctypes.POINTER(GemmConfig)]
     lib.moe_mxfp4_get_plan_w4a16.restype = i
@@ -187,6 +190,35 @@ def get_plan(T, d_model, d_inter, E, topk) -> Plan:
     _check(load_library().moe_mxfp4_get_plan(T, d_model, d_inter, E, topk, ctypes.byref(pl)),
            "moe_mxfp4_get_plan")
     return pl
+
+
+def topk_sum_ptr(P_ptr, route_pos_ptr, out_ptr, T, d_model, topk, stream=0) -> int:
+    """moe_mxfp4_topk_sum on raw pointers; returns the status code."""
+    return int(load_library().moe_mxfp4_topk_sum(ctypes.c_void_p(P_ptr), ctypes.c_void_p(route_pos_ptr),
+                                                 ctypes.c_void_p(out_ptr), T, d_model, topk,
+                                                 ctypes.c_void_p(stream)))
+
+
+def topk_sum(P, route_pos, out):
+    """Deterministic top-k sum (moe_mxfp4_topk_sum) of P (f32 [T*topk, d_model],
+    rows by route id) over the routes with route_pos >= 0 (int32 [T*topk]) into
+    out (bf16 [T, d_model]), on the current stream.  The tensors must be
+    contiguous and on the device."""
+    import torch
+
+    R, D = P.shape
+    T = out.shape[0]
+    if T == 0:
+        return out
+    if R % T != 0 or route_pos.numel() != R or out.shape[1] != D:
+        raise ValueError("P [T*topk, d_model], route_pos [T*topk], out [T, d_model]")
+    for x, dt in ((P, torch.float32), (route_pos, torch.int32), (out, torch.bfloat16)):
+        if x.dtype != dt or not x.is_contiguous():
+            raise ValueError("P f32, route_pos int32, out bf16, all contiguous")
+    stream = torch.cuda.current_stream(out.device).cuda_stream
+    _check(topk_sum_ptr(P.data_ptr(), route_pos.data_ptr(), out.data_ptr(), T, D, R // T, stream),
+           "moe_mxfp4_topk_sum")
+    return out
 
 
 def gemm_config(T, d_model, d_inter, E, topk) -> GemmConfig:

@@ -619,3 +619,18 @@ cudaError_t launch_check_wait(uint32_t* status, uint64_t limit_ns, cudaStream_t 
 }
 
 }  // namespace moe
+
+extern "C" moe_status_t moe_mxfp4_topk_sum(const float* P, const int32_t* route_pos, void* out, int T,
+                                           int d_model, int topk, cudaStream_t stream) {
+    if (T < 0 || topk < 1 || topk > 16 || d_model <= 0) return MOE_ERR_INVALID_ARG;
+    if (d_model % 128 != 0 || (long long)T * topk > (1LL << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!P || !route_pos || !out) return MOE_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(P) | reinterpret_cast<uintptr_t>(route_pos) |
+          reinterpret_cast<uintptr_t>(out)) & 15u) != 0)
+        return MOE_ERR_MISALIGNED;
+    moe::WsPtrs ws = {};
+    ws.route_pos = const_cast<int32_t*>(route_pos);
+    ws.P = const_cast<float*>(P);
+    return moe::launch_reduce(T, topk, d_model, d_model, out, ws, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -15,7 +15,9 @@ Each rank holds its own batch of tokens.  A forward on every rank:
    of its workspace (`library_local_forward`);
 3. combine: the rows go back to their tokens' ranks, which add each token's rows
    in ascending k in fp32 from zero and round once to bf16: the arithmetic and
-   the order of the single-GPU forward, so the result equals it bit for bit.
+   the order of the single-GPU forward, so the result equals it bit for bit.  On
+   the GPU the library's top-k sum kernel does it (moe_mxfp4_topk_sum); with CPU
+   tensors (gloo process groups) the same sum runs on the host.
 
 Communication uses the torch.distributed collectives of the caller's process
 group (all_to_all_single; NCCL for GPU tensors, gloo for CPU tensors).  Sending
@@ -113,6 +115,12 @@ def ep_forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch
     _a2a(back, rows, sc, rc, group)
     P = torch.zeros(T * K, D, dtype=torch.float32, device=dev)
     P[rid_s] = back
+    if dev.type == "cuda":
+        import mixture_experts_mxfp4_gb300 as moe
+
+        route_pos = torch.where(valid, 0, -1).to(torch.int32)  # >= 0: the route counts
+        out = torch.empty(T, D, dtype=torch.bfloat16, device=dev)
+        return moe.topk_sum(P, route_pos, out)
     P = P.view(T, K, D)
     vk = valid.view(T, K)
     acc = torch.zeros(T, D, dtype=torch.float32, device=dev)

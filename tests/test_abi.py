@@ -164,6 +164,19 @@ def test_run_widths_in_the_plan(lib, shape, run):
         assert moe.load_library().moe_mxfp4_workspace_size_w4a16(*shape) == 0
 
 
+def test_topk_sum_validation_without_device(lib):
+    import mixture_experts_mxfp4_gb300 as moe
+
+    good = 1 << 20
+    assert moe.topk_sum_ptr(good, good, good, 16, 256, 0) == 1      # topk 0
+    assert moe.topk_sum_ptr(good, good, good, 16, 256, 17) == 1     # topk above 16
+    assert moe.topk_sum_ptr(good, good, good, -1, 256, 3) == 1      # T < 0
+    assert moe.topk_sum_ptr(good, good, good, 16, 200, 3) == 2      # d_model not a multiple of 128
+    assert moe.topk_sum_ptr(good, good, good, 0, 256, 3) == 0       # empty: nothing enqueued
+    assert moe.topk_sum_ptr(good, 0, good, 16, 256, 3) == 1         # null pointer
+    assert moe.topk_sum_ptr(good + 4, good, good, 16, 256, 3) == 3  # misaligned
+
+
 def test_w4a16_entry_and_plan_without_device(lib):
     import mixture_experts_mxfp4_gb300 as moe
 

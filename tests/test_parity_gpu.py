@@ -463,6 +463,28 @@ def test_widths_run_wider(moe, launch_mode, T, D, I, E, K):
     check_out(out, ref)
 
 
+@pytest.mark.parametrize("name", [workloads.DECODE_T16, "decode_T128_D7168_I256_E257_K9"])
+def test_topk_sum_entry_matches_forward(moe, name):
+    """moe_mxfp4_topk_sum on the forward's own P rows and route map gives the
+    forward's output bit for bit (the same kernel and order), with one route made
+    invalid; a route map with every route of token 0 off gives it a zero row."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w, seed=17)
+    inp["topk_ids"][0, 1] = -1
+    m, t, out = run_gpu(moe, inp, w)
+    P = m.region("P", torch.float32, (w.R, w.D)).clone()
+    rpos = m.region("route_pos", torch.int32, (w.R,)).clone()
+    o2 = torch.full_like(out, float("nan"))
+    moe.topk_sum(P, rpos, o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o2.view(torch.int16), out.view(torch.int16))
+    rpos[: w.K] = -1
+    moe.topk_sum(P, rpos, o2)
+    torch.cuda.synchronize()
+    assert (o2[0].float() == 0).all()
+    assert torch.equal(o2[1:].view(torch.int16), out[1:].view(torch.int16))
+
+
 def test_launch_modes_bitwise_identical(moe):
     """Single-launch mode reproduces the separate-kernel output and workspace
     routing arrays bit for bit (same routing order, same quantisation)."""
