@@ -583,7 +583,8 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
         // checked build: accumulators and per-slot scale-factor columns inside the allocation
         bool geo = (uint32_t)p.acc_bufs * p.acc_cols <= p.sf_col0 &&
                    p.sf_col0 + (uint32_t)NS * p.sf_cols <= p.tmem_cols && p.acc_bufs <= kMaxAccBufs && NS <= kMaxStages &&
-                   p.acc_bufs >= kEpi;  // (see gemm_geometry: buffers >= epilogue groups)
+                   p.acc_bufs >= kEpi &&  // (see gemm_geometry: buffers >= epilogue groups)
+                   (kKs1 == 0 || !p.kt_boxes);  // per-K-box weight copies: generic kernels only
         for (int ph2 = 0; ph2 < 2; ++ph2)
             geo = geo && (uint32_t)((p.g[ph2].mblocks + 1) * 4 * p.g[ph2].natoms) <= p.sf_cols;
         *abort_flag = moe_check(geo, p.ws.status) ? 0 : 1;
@@ -755,9 +756,10 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                                 tma_load_3d(st + q.off_sa, mSA, 0, rg / (16 / q.sr_a), 0, &sfull[s]);
                             else
                                 tma_load_3d(st + q.off_sa, mSA, ks * 16, rg, 0, &sfull[s]);
-                            if (p.kt_boxes) {
-                                // weights narrower than D: one copy per K box (each box
-                                // 128 rows, gate then up), zeros past the row
+                            if (kKs1 == 0 && p.kt_boxes) {
+                                // weights narrower than D (generic instantiations only):
+                                // one copy per K box (each box 128 rows, gate then up),
+                                // zeros past the row
                                 for (int kt = 0; kt < q.nkt; ++kt)
                                     tma_load_3d_hint(st + (size_t)kt * 128u * q.kb, mA, (kt0 + kt) * q.kb, rg, 0,
                                                      &full[s], pol_w);
@@ -769,8 +771,9 @@ __global__ void __launch_bounds__(128 + 128 * kEpi, 1)
                                 tma_load_2d(st + q.off_sa, mSA, 0, rg / (16 / q.sr_a), &sfull[s]);
                             else
                                 tma_load_2d(st + q.off_sa, mSA, ks * 16, rg, &sfull[s]);
-                            if (p.kt_boxes) {
-                                // weights narrower than I: one copy per K box of arows rows
+                            if (kKs1 == 0 && p.kt_boxes) {
+                                // weights narrower than I (generic instantiations only): one
+                                // copy per K box of arows rows
                                 for (int kt = 0; kt < q.nkt; ++kt)
                                     tma_load_2d_hint(st + (size_t)kt * arows * q.kb, mA, (kt0 + kt) * q.kb, rg,
                                                      &full[s], pol_w);
@@ -1387,6 +1390,9 @@ cudaError_t launch_gemm(const CUtensorMap* maps, const GemmParams& p, int grid,
         spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 6 : 7;
     else
         spec = (ks1 == 8 && ks2 == 4 && mb2 == 2) ? 9 : 10;
+    // weights narrower than the run widths: the generic instantiation of the scheme
+    // (only it compiles the per-K-box weight copies)
+    if (p.kt_boxes) spec = mode == 0 ? 1 : mode == 1 ? 4 : mode == 2 ? 7 : 10;
     static const KernelFn kernels[2][11] = {
         {moe_gemm_kernel<0, false, 8, 4, 2, 2>, moe_gemm_kernel<0, false, 0, 0, 0, 2>,
          moe_gemm_kernel<1, false, 8, 8, 1, 2>, moe_gemm_kernel<1, false, 8, 4, 1, 2>,

@@ -59,7 +59,8 @@ struct GemmParams {
     int Dw, Iw;         // widths of the weight tensors: w13 [E][2 Iw][Dw/2], w2 [E][Dw][Iw/2]
     int kt_boxes;       // weights narrower than D or I: one copy per K box of a stage, the
                         // columns past Dw / Iw zero-filled by the copy (maps of the weights'
-                        // own widths); weight scales repacked to D/32, I/32 bytes per row
+                        // own widths; generic instantiations only); weight scales repacked
+                        // to D/32, I/32 bytes per row
     int tile_rows;      // maximum MMA N (routes per tile), multiple of 16, <= 128
     StageGeom g[2];     // stage 1, stage 2
     int num_stages;     // shared-memory ring depth
