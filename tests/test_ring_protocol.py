@@ -271,6 +271,21 @@ def test_fewer_buffers_than_groups_is_caught():
     assert _violations(400, 9000, ns=3, mma_warps=1, acc_bufs=2, epi_groups=3) > 0
 
 
+def _random_shapes(n, seed):
+    """Valid shapes drawn at random: d_model a multiple of 128, d_inter of 64 (the
+    widths run as they are and the ones run wider), T, E and topk over their ranges."""
+    rnd = random.Random(seed)
+    out = []
+    for _ in range(n):
+        D = 128 * rnd.choice([1, 2, 3, 4, 7, 8, 12, 23, 56, 64])
+        I = 64 * rnd.choice([1, 2, 3, 4, 5, 6, 8, 12, 16, 32])
+        E = rnd.choice([1, 3, 8, 33, 64, 257, 384, 1024])
+        K = rnd.randint(1, min(16, E))
+        T = rnd.choice([1, 5, 16, 64, 128, 512, 1024, 4096])
+        out.append((T, D, I, E, K))
+    return out
+
+
 SHAPES = [(16, 7168, 256, 257, 9), (128, 7168, 256, 257, 9), (512, 7168, 2048, 33, 9),
           (4096, 7168, 256, 257, 9), (256, 512, 256, 5, 3), (96, 1024, 512, 3, 2),
           (16, 256, 128, 9, 3), (200, 2048, 1024, 4, 3), (8, 128, 128, 1, 1), (64, 1536, 1024, 64, 6),
@@ -287,7 +302,8 @@ def test_geometry_keeps_the_rules():
     build.build()
     moe.load_library()
     try:
-        for shape, rows, copies in itertools.product(SHAPES, (0, 16, 32, 64, 128), range(5)):
+        for shape, rows, copies in itertools.product(SHAPES + _random_shapes(60, 7), (0, 16, 32, 64, 128),
+                                                     range(5)):
             moe.set_tuning(rows, copies)
             c = moe.gemm_config(*shape)
             where = (shape, rows, copies, c.as_dict())
