@@ -58,7 +58,7 @@ def _check(cond, what):
         raise _Violation(what)
 
 
-def _play(seed, ns, mma_warps, acc_bufs, epi_groups, items, stages_per_item):
+def _play(seed, ns, mma_warps, acc_bufs, epi_groups, items, stages_per_item, lookahead=False):
     """One random interleaving of the kernel's roles over one CTA's items.
 
     items[phase] work items of stages_per_item[phase] pipeline stages each; stage
@@ -66,8 +66,11 @@ def _play(seed, ns, mma_warps, acc_bufs, epi_groups, items, stages_per_item):
     warp w issues the stages with g % mma_warps == w into its own accumulator of
     the item's buffer (item index % acc_bufs); every MMA warp waits for the buffer
     and commits once per item; epilogue group e drains the items with index %
-    epi_groups == e.  Raises _Violation on a wrong-phase wait, a data hazard or a
-    deadlock."""
+    epi_groups == e.  With lookahead, an MMA warp about to issue a stage tests
+    (without waiting) whether its next stage's fill and scale factors are there,
+    and if so skips those waits at that stage (the kernel's copy look-ahead with
+    MMA-warp copies).  Raises _Violation on a wrong-phase wait or test, a data
+    hazard or a deadlock."""
     rnd = random.Random(seed)
     seq = []  # (item, first stage of the item, last stage of the item)
     per_item = []
@@ -92,7 +95,7 @@ def _play(seed, ns, mma_warps, acc_bufs, epi_groups, items, stages_per_item):
     events = []
     prod = {"g": 0}
     lay = {"g": 0}
-    mma = [{"g": 0, "item": 0, "state": "tempty", "queue": []} for _ in range(mma_warps)]
+    mma = [{"g": 0, "item": 0, "state": "tempty", "queue": [], "pre": -1} for _ in range(mma_warps)]
     epi = [{"next": e, "busy": False} for e in range(epi_groups)]
 
     def wait(bar, k, name):
@@ -143,13 +146,20 @@ def _play(seed, ns, mma_warps, acc_bufs, epi_groups, items, stages_per_item):
         if st["g"] < G and seq[st["g"]][0] == it:
             g = st["g"]
             s, k = g % ns, g // ns
-            if st["state"] == "stages":
+            if st["state"] == "stages" and st["pre"] != g:
                 if not wait(full[s], k, "full"):
                     return False
                 st["state"] = "sf"
                 return True
-            if not wait(sfready[s], k, "sfready"):
+            if st["pre"] != g and not wait(sfready[s], k, "sfready"):
                 return False
+            gn = g + mma_warps  # this warp's next stage
+            if lookahead and gn < G:
+                sn, kn = gn % ns, gn // ns
+                if full[sn].passes(kn) and sfready[sn].passes(kn):
+                    _check(full[sn].c == kn + 1 and sfready[sn].c == kn + 1,
+                           f"look-ahead test passed on phase {full[sn].c - 1} for phase {kn}")
+                    st["pre"] = gn
             _check(slot_data[s] == g and slot_sf[s] == g, "MMAs issued on another stage's data")
             _check(not buf_drain[a] and buf_item[a] in (None, "free", it),
                    "accumulator written while the epilogue reads it")
@@ -255,6 +265,19 @@ def _violations(n, seed0, **kw):
 def test_protocol_clean_under_the_geometry_rules(ns, mma_warps, acc_bufs, epi_groups):
     assert _violations(300, 1000, ns=ns, mma_warps=mma_warps, acc_bufs=acc_bufs,
                        epi_groups=epi_groups) == 0
+
+
+@pytest.mark.parametrize("ns", [4, 6])
+def test_lookahead_clean_with_an_even_ring(ns):
+    """The MMA warps' look-ahead (scheme 1: each warp copies its next stage's scale
+    factors early when that stage has landed) with the geometry's even ring."""
+    assert _violations(300, 3000, ns=ns, mma_warps=2, acc_bufs=4, epi_groups=2, lookahead=True) == 0
+
+
+def test_lookahead_with_an_odd_ring_is_caught():
+    """The same test with 3 slots: the slot of a warp's next stage last held the
+    other warp's stage, and the non-blocking test can pass on that fill."""
+    assert _violations(600, 7000, ns=3, mma_warps=2, acc_bufs=4, epi_groups=2, lookahead=True) > 0
 
 
 def test_odd_ring_depth_with_two_mma_warps_is_caught():
