@@ -215,8 +215,9 @@ moe_status_t moe_mxfp4_check_wait_timeout(uint32_t limit_us, cudaStream_t stream
 
 /*
  * The forward's last step on its own: the deterministic top-k sum of per-route
- * rows (for an expert-parallel combine, where the rows come back from the ranks
- * that own the experts).
+ * rows (solution.py, _reference_forward's sum of the weighted expert outputs
+ * over a token's top-k routes), for an expert-parallel combine, where the rows
+ * come back from the ranks that own the experts.
  *   out[t] = bf16( sum over k = 0 .. topk-1 with route_pos[t*topk+k] >= 0 of
  *                  P[t*topk+k] ), fp32 adds in ascending k from zero, one rounding
  *   P          f32  [T*topk, d_model], rows by route id (w[t,k] * W2[e] . a2 in the
